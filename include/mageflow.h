@@ -1,0 +1,311 @@
+/*
+ * mageflow.h - C ABI of libmageflow.so: the packed NR-MMDiT block forward and its
+ * rectified-flow epilogues on one NVIDIA B300 (sm_103a).
+ *
+ * Sources of the operations (page titles and sections):
+ *   [PR 2.2(2)]  PaperReading review of "Mage-Flow: An Efficient Native-Resolution Foundation
+ *                Model for Image Generation and Editing", section 2.2 (2): native-resolution
+ *                packing by cumulative offsets, attention restricted to each sample, per-sample
+ *                2-D RoPE plus a frame index for editing, the flow-matching objective and
+ *                z_t = (1 - t) z + t eps, editing loss on the target latent only.
+ *   [PR 2.2(3)]  same review, section 2.2 (3): packed CFG; fused norm / RoPE / gating /
+ *                residual chains that leave the model function unchanged.
+ *   [PR 5]       same review, section 5: MMDiT with per-modality projections and norms and
+ *                joint self-attention; rectified-flow ODE sampling; CFG from the difference of
+ *                the conditional and unconditional predictions.
+ *   [HA M]       hyper.ai summary of the paper, section 方法 (method): packing under a fixed
+ *                token budget, the loss, the frame dimension of the rotary embedding.
+ *   [HA E]       hyper.ai summary, section 实验 (experiments): packed CFG keeps the denoising
+ *                trajectory and raises throughput by 9-15 %.
+ *
+ * Conventions shared by every call
+ *   - Every call returns mf_status.  Nothing aborts and nothing throws across the ABI.
+ *     Arguments are validated on the host before any launch; on an error no kernel runs and
+ *     no output is touched.
+ *   - "device pointer" = memory the caller allocated on the current CUDA device (cudaMalloc,
+ *     a PyTorch tensor ...).  The caller owns it and keeps it alive until the stream has
+ *     finished the call.  Device pointers must be 16-byte aligned (256-byte aligned for
+ *     workspaces); otherwise MF_ERR_ALIGNMENT.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
+ *     call is asynchronous on that stream unless it says otherwise.
+ *   - Matrices are row-major.  Weights are bf16 stored [out_features][in_features]; biases
+ *     are bf16 [out_features].  Activations are bf16 [rows][features] unless stated.
+ *   - Token layouts of a pack (see mf_pack):
+ *       joint order   : sample by sample in pack order, each sample as
+ *                       [text tokens | frame 0 image tokens | frame 1 image tokens],
+ *                       image tokens row-major over the latent grid;
+ *       text stream   : the text tokens of all samples, in pack order (N_txt rows);
+ *       image stream  : the image tokens of all samples, in pack order (N_img rows);
+ *       stream-sorted : text stream rows followed by image stream rows (N_txt + N_img rows).
+ *   - Device faults are never used for error reporting.  Every wait inside a kernel is
+ *     bounded; a wait that runs out records MF_ERR_DEVICE_TIMEOUT in a device status word
+ *     that mf_check() returns.
+ */
+#ifndef MAGEFLOW_H
+#define MAGEFLOW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MF_OK = 0,
+  MF_ERR_INVALID_ARG = 1,      /* null pointer, bad size, bad shape or inconsistent pairing */
+  MF_ERR_SAMPLE_TOO_LONG = 2,  /* one sample alone exceeds the token budget */
+  MF_ERR_BUDGET = 3,           /* budget < 1 */
+  MF_ERR_ALIGNMENT = 4,        /* a device pointer is not aligned as required */
+  MF_ERR_CUDA = 5,             /* a CUDA runtime call failed (no device, launch failure ...) */
+  MF_ERR_DEVICE_TIMEOUT = 6,   /* a bounded wait inside a kernel ran out (see mf_check) */
+  MF_ERR_UNSUPPORTED = 7,      /* dims outside what the kernels implement */
+  MF_ERR_NOT_UPLOADED = 8,     /* the plan has no device copy (call mf_plan_upload) */
+  MF_ERR_WORKSPACE = 9         /* workspace smaller than the *_workspace_bytes() figure */
+} mf_status;
+
+/* Human-readable name of a status; never NULL. */
+const char* mf_status_str(mf_status s);
+
+/* ABI version: (major << 16) | minor. */
+int32_t mf_version(void);
+
+/* ------------------------------------------------------------------------------------ */
+/* Packing  [PR 2.2(2)], [HA M]                                                          */
+/* ------------------------------------------------------------------------------------ */
+
+/* One packing candidate.  The sample has txt_len text tokens and `frames` (1 or 2) latent
+ * frames of lat_h x lat_w patch tokens; frame 0 of a 2-frame sample is the clean editing
+ * source and the last frame is the target.  t is the sample's flow time in [0, 1].
+ * cfg_role: 0 plain, 1 conditional branch, 2 unconditional branch; cfg_pair is the index
+ * (in the candidate array) of the other branch of the same prompt, -1 for plain samples.
+ * Layout: 7 x 4 bytes, little-endian, no padding. */
+typedef struct {
+  int32_t txt_len;
+  int32_t frames;
+  int32_t lat_h;
+  int32_t lat_w;
+  float t;
+  int32_t cfg_role;
+  int32_t cfg_pair;
+} mf_sample;
+
+typedef struct mf_plan mf_plan; /* opaque; owned by the library, freed with mf_plan_free */
+
+/* Packs candidates first-fit in the order given: candidate i is taken iff its length
+ * txt_len + frames*lat_h*lat_w still fits the budget left by the candidates taken before it;
+ * otherwise it is skipped and packing goes on.  Taken samples keep their relative order.
+ * Builds every index buffer the kernels read (cu_seqlens, per-token (frame, row, col)
+ * positions, stream/joint row maps, CFG pair table, target-frame flags, the attention work
+ * list).  Host only: makes no CUDA call, so it works without a GPU.
+ *   samples : host array of n candidates (n >= 0; n == 0 gives an empty plan)
+ *   budget  : token budget (>= 1)
+ *   out     : receives a new plan; unchanged on error
+ * Errors: MF_ERR_BUDGET (budget < 1), MF_ERR_SAMPLE_TOO_LONG (a candidate longer than the
+ * budget), MF_ERR_INVALID_ARG (null pointer, n < 0, txt_len < 0, frames not in {1,2},
+ * lat_h or lat_w < 1, cfg_role not in {0,1,2}, a packed CFG branch whose partner is not
+ * packed or has another image shape). */
+mf_status mf_pack(const mf_sample* samples, int32_t n, int32_t budget, mf_plan** out);
+
+/* Copies the plan's index buffers to the current device (library-owned device memory,
+ * allocated on the first upload, freed by mf_plan_free).  Asynchronous on `stream`; the
+ * host copy must not be modified meanwhile (it never is: plans are immutable).
+ * Errors: MF_ERR_INVALID_ARG, MF_ERR_CUDA. */
+mf_status mf_plan_upload(mf_plan* plan, void* stream);
+
+/* Frees host and device memory of the plan.  The caller must make sure no stream still
+ * uses it.  NULL is a no-op. */
+void mf_plan_free(mf_plan* plan);
+
+typedef struct {
+  int32_t n_seq;      /* S: packed samples */
+  int32_t n_tok;      /* N: packed tokens (<= budget) */
+  int32_t n_txt;      /* text-stream rows */
+  int32_t n_img;      /* image-stream rows */
+  int32_t n_items;    /* attention work items (sequence, 128-row query tile) */
+  int32_t budget;
+  int32_t uploaded;   /* 1 after mf_plan_upload */
+  int32_t reserved;
+} mf_plan_info;
+
+mf_status mf_plan_get_info(const mf_plan* plan, mf_plan_info* info);
+
+/* Host views of the plan's index buffers (int32, owned by the plan, valid until
+ * mf_plan_free).  `which`:
+ *   0 order[S]        candidate index of each packed sample
+ *   1 cu_seqlens[S+1] joint-token offsets
+ *   2 cu_txt[S+1]     text-stream row offsets
+ *   3 cu_img[S+1]     image-stream row offsets
+ *   4 pos[N*3]        (frame, row, col) of each joint token; text tokens (0, 0, 0)
+ *   5 txt_seq[N_txt]  6 txt_joint[N_txt]   sample / joint token of each text row
+ *   7 img_seq[N_img]  8 img_joint[N_img]   sample / joint token of each image row
+ *   9 img_pair[N_img] CFG partner image row, -1 if none
+ *  10 img_target[N_img] 1 for target-frame rows, 0 for an edit's source frame
+ *  11 seq_role[S]     cfg_role of each packed sample
+ *  12 items[n_items*2] attention work list (sequence, query tile), longest sequences first
+ * Errors: MF_ERR_INVALID_ARG for an unknown `which` or null pointers. */
+mf_status mf_plan_array(const mf_plan* plan, int32_t which, const int32_t** data, int64_t* len);
+
+/* ------------------------------------------------------------------------------------ */
+/* Model dims and weights                                                                */
+/* ------------------------------------------------------------------------------------ */
+
+typedef struct {
+  int32_t hidden;     /* H; multiple of 64 */
+  int32_t heads;      /* nh; H / nh = head dim D, D in {64, 128} */
+  int32_t channels;   /* C: latent channels per patch token; 64 or 128 */
+  int32_t mlp_ratio;  /* MLP width = mlp_ratio * H */
+  int32_t freq_dim;   /* sinusoidal timestep features; 256 */
+} mf_dims;
+
+/* Timestep embedder, shared by every block and the final layer of a stack:
+ * c = SiLU(W_t2 SiLU(W_t1 phi(t) + b_t1) + b_t2), phi(t) = [cos a | sin a],
+ * a_j = 1000 t 10000^(-j / (F/2)).  W_t1 [H][F], W_t2 [H][H]. */
+typedef struct {
+  const void* w_t1; const void* b_t1;
+  const void* w_t2; const void* b_t2;
+} mf_temb_weights;
+
+/* One stream (text or image) of one block [PR 5]: the adaLN modulation (6 chunks of H in
+ * the order shift1, scale1, gate1, shift2, scale2, gate2), the fused QKV projection
+ * (q | k | v, each H wide), the attention output projection and the MLP. */
+typedef struct {
+  const void* w_mod; const void* b_mod;   /* [6H][H], [6H] */
+  const void* w_qkv; const void* b_qkv;   /* [3H][H], [3H] */
+  const void* w_o;   const void* b_o;     /* [H][H],  [H]  */
+  const void* w_1;   const void* b_1;     /* [rH][H], [rH] */
+  const void* w_2;   const void* b_2;     /* [H][rH], [H]  */
+} mf_stream_weights;
+
+typedef struct {
+  mf_temb_weights temb;
+  mf_stream_weights txt;
+  mf_stream_weights img;
+} mf_block_weights;
+
+/* ------------------------------------------------------------------------------------ */
+/* The block forward  [PR 2.2(2)], [PR 2.2(3)], [PR 5]                                   */
+/* ------------------------------------------------------------------------------------ */
+
+/* Workspace the block forward needs for this plan and dims (bytes). */
+size_t mf_block_workspace_bytes(const mf_plan* plan, const mf_dims* dims);
+
+/* Byte offsets inside that workspace of the intermediates a call leaves behind, for
+ * inspection: [0] c[S][H] f32, [1] mod[S][2][6H] f32 (stream 0 text, 1 image),
+ * [2] a[N_txt+N_img][H] bf16 (last LN+modulate output, stream-sorted),
+ * [3] q[N][H], [4] k[N][H], [5] v[N][H] bf16 in joint order (q, k after RoPE),
+ * [6] o[N_txt+N_img][H] bf16 attention output, stream-sorted,
+ * [7] hidden[N_txt+N_img][rH] bf16 (GELU output), stream-sorted.  n must be >= 8. */
+mf_status mf_block_workspace_layout(const mf_plan* plan, const mf_dims* dims, size_t* offsets,
+                                    int32_t n);
+
+/* One NR-MMDiT block over the whole pack, in place on x:
+ *   per sample s and stream m: (shift1, scale1, gate1, shift2, scale2, gate2) = W_mod c_s + b
+ *   a  = LN(x) (1 + scale1) + shift1                      (LN without affine, eps 1e-6)
+ *   q, k, v = a W_qkv^T + b_qkv, RoPE on q and k over (frame, row, col)
+ *   o  = softmax(q k^T / sqrt(D)) v, jointly over each sample's own tokens only
+ *   x += gate1 (o W_o^T + b_o)
+ *   x += gate2 (GELU(LN(x)(1 + scale2) + shift2) W_1^T + b_1) W_2^T + b_2)
+ * Text rows use w->txt, image rows w->img.
+ *   plan    : packed and uploaded plan
+ *   d_t     : device f32 [S] flow time per packed sample, or NULL to use the samples' t
+ *   d_x_txt : device bf16 [N_txt][H], in/out (may be NULL when N_txt == 0)
+ *   d_x_img : device bf16 [N_img][H], in/out
+ *   d_ws    : device workspace of mf_block_workspace_bytes() bytes, 256-byte aligned
+ * Errors: MF_ERR_INVALID_ARG, MF_ERR_UNSUPPORTED (dims), MF_ERR_NOT_UPLOADED,
+ * MF_ERR_WORKSPACE, MF_ERR_ALIGNMENT, MF_ERR_CUDA (launch failure). */
+mf_status mf_block_forward(const mf_plan* plan, const mf_dims* dims, const mf_block_weights* w,
+                           const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
+                           size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* Latent embed and final layer (stack ends)  [PR 2.2(2)]                                */
+/* ------------------------------------------------------------------------------------ */
+
+/* x_img = z_t W_in^T + b_in: patch latents [N_img][C] (bf16) to hidden [N_img][H] (bf16).
+ * W_in [H][C]. Errors: MF_ERR_INVALID_ARG, MF_ERR_UNSUPPORTED, MF_ERR_NOT_UPLOADED,
+ * MF_ERR_ALIGNMENT, MF_ERR_CUDA. */
+mf_status mf_embed(const mf_plan* plan, const mf_dims* dims, const void* w_in, const void* b_in,
+                   const void* d_zt, void* d_x_img, void* stream);
+
+size_t mf_final_workspace_bytes(const mf_plan* plan, const mf_dims* dims);
+
+/* v = (LN(x_img)(1 + scale) + shift) W_out^T + b_out on image rows, with
+ * (shift, scale) = W_fmod c_s + b_fmod (2 chunks of H), c_s the sample's timestep
+ * condition.  W_fmod [2H][H], W_out [C][H].
+ *   d_t : device f32 [S] or NULL (samples' t);  d_x_img : bf16 [N_img][H];
+ *   d_v : device f32 [N_img][C] output velocity. */
+mf_status mf_final(const mf_plan* plan, const mf_dims* dims, const mf_temb_weights* temb,
+                   const void* w_fmod, const void* b_fmod, const void* w_out, const void* b_out,
+                   const float* d_t, const void* d_x_img, float* d_v, void* d_ws,
+                   size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* Rectified-flow epilogues  [PR 2.2(2)], [PR 2.2(3)], [PR 5], [HA M], [HA E]            */
+/* ------------------------------------------------------------------------------------ */
+
+/* z_t = (1 - t_s) z + t_s eps on target-frame rows; source-frame rows of an edit sample
+ * stay clean (z_t = z).  d_z, d_eps: f32 [N_img][C]; d_t: f32 [S] or NULL (samples' t).
+ * Outputs (either may be NULL, not both): d_zt f32 [N_img][C], d_zt_bf16 bf16 [N_img][C]. */
+mf_status mf_interpolate(const mf_plan* plan, int32_t channels, const float* d_t, const float* d_z,
+                         const float* d_eps, float* d_zt, void* d_zt_bf16, void* stream);
+
+/* Packed CFG [PR 2.2(3)], [PR 5]: for each conditional image row r with unconditional
+ * partner u, v_out[r] = v_out[u] = v[u] + w (v[r] - v[u]); rows of plain samples are copied.
+ * Both branches receive the guided velocity so that one Euler step keeps them identical.
+ * d_v, d_v_out: f32 [N_img][C]; must not overlap unless equal (in place is allowed). */
+mf_status mf_cfg_combine(const mf_plan* plan, int32_t channels, float w, const float* d_v,
+                         float* d_v_out, void* stream);
+
+/* Euler step of the rectified-flow ODE from t to t - dt (dt > 0 moves towards data):
+ * z += dt v, since v ~ z - eps = -dz_t/dt.  d_z f32 [N_img][C] in place; d_v f32 [N_img][C];
+ * d_z_bf16: optional bf16 copy of the new z (the next embed's input), may be NULL. */
+mf_status mf_euler_step(const mf_plan* plan, int32_t channels, float dt, const float* d_v,
+                        float* d_z, void* d_z_bf16, void* stream);
+
+size_t mf_flow_loss_workspace_bytes(const mf_plan* plan);
+
+/* Flow-matching loss [PR 2.2(2)]: per sample s, loss_sum[s] = sum over its target-frame
+ * image elements of (v - (z - eps))^2 (f64), count[s] = number of those elements, and
+ * mean[0] = sum_s loss_sum[s] / sum_s count[s].  Deterministic (fixed reduction order).
+ * d_z, d_eps, d_v: f32 [N_img][C]; outputs are device arrays; d_ws: workspace of
+ * mf_flow_loss_workspace_bytes() bytes. */
+mf_status mf_flow_loss(const mf_plan* plan, int32_t channels, const float* d_z, const float* d_eps,
+                       const float* d_v, double* d_loss_sum, int64_t* d_count, double* d_mean,
+                       void* d_ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* Building blocks, exposed for testing and reuse                                        */
+/* ------------------------------------------------------------------------------------ */
+
+/* Varlen joint attention [PR 2.2(2)]: for every packed sample and head,
+ * o = softmax(q k^T / sqrt(D)) v over the sample's own tokens; nothing crosses samples.
+ * d_q, d_k, d_v: bf16 [N][H] joint order (heads contiguous inside a row);
+ * d_o: bf16 [N_txt + N_img][H] stream-sorted output. */
+mf_status mf_attention(const mf_plan* plan, int32_t heads, int32_t head_dim, const void* d_q,
+                       const void* d_k, const void* d_v, void* d_o, void* stream);
+
+/* Plain bf16 GEMM on the tensor cores: C[M][N] = A[M][K] B[N][K]^T (+ bias[N]).
+ * out_f32 = 0: C bf16, 1: C f32.  K must be a multiple of 64.  bias may be NULL. */
+mf_status mf_gemm(int32_t M, int32_t N, int32_t K, const void* d_a, const void* d_b,
+                  const void* d_bias, void* d_c, int32_t out_f32, void* stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* Device status                                                                         */
+/* ------------------------------------------------------------------------------------ */
+
+/* Synchronises `stream`, then returns and clears the device status word of the current
+ * device: MF_OK, or MF_ERR_DEVICE_TIMEOUT if a bounded wait ran out since the last check;
+ * MF_ERR_CUDA if the synchronisation itself failed. */
+mf_status mf_check(void* stream);
+
+/* Self-test of the bounded-wait path: launches one tiny kernel that waits on a barrier no
+ * one arrives at, with a limit of limit_us microseconds (1..1000000).  Returns (after a
+ * synchronisation) MF_ERR_DEVICE_TIMEOUT when the wait ran out as intended and the context
+ * is still usable, MF_OK never.  The status word is cleared again before returning. */
+mf_status mf_selftest_timeout(int32_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MAGEFLOW_H */

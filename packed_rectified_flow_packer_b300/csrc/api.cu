@@ -1,0 +1,661 @@
+// C ABI of libmageflow.so: argument validation, workspace layout, TMA descriptors and the
+// launch sequence of each call.  The operations themselves are specified in mageflow.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "attention.cuh"
+#include "gemm.cuh"
+#include "internal.h"
+#include "pointwise.cuh"
+
+namespace {
+
+using mf::bf16;
+
+__device__ unsigned int g_mf_status;  // OR of kernel status bits since the last mf_check
+
+// ------------------------------------------------------------------ per-device state
+struct DevInfo {
+  bool init = false;
+  int sms = 0;
+  unsigned* status = nullptr;
+};
+constexpr int kMaxDev = 64;
+DevInfo g_dev[kMaxDev];
+std::mutex g_mu;
+
+mf_status device_info(DevInfo** out, int* dev_out = nullptr) {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDev) return MF_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& di = g_dev[d];
+  if (!di.init) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess)
+      return MF_ERR_CUDA;
+    if (major != 10 || minor != 3) return MF_ERR_UNSUPPORTED;  // built for sm_103a only
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_mf_status) != cudaSuccess) return MF_ERR_CUDA;
+    di.status = static_cast<unsigned*>(p);
+    di.init = true;
+  }
+  *out = &di;
+  if (dev_out) *dev_out = d;
+  return MF_OK;
+}
+
+unsigned long long wait_limit_ns() {
+  static unsigned long long v = [] {
+    const char* e = std::getenv("MF_WAIT_LIMIT_MS");
+    long long ms = e ? std::atoll(e) : 4000;
+    if (ms < 1) ms = 1;
+    if (ms > 60000) ms = 60000;
+    return (unsigned long long)ms * 1000000ull;
+  }();
+  return v;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 matrix [rows][cols] (row-major, contiguous), boxes of box_rows x 64 columns,
+// 128-byte swizzle, zero fill outside the matrix.
+bool make_tmap(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ validation helpers
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+mf_status check_dims(const mf_dims* d) {
+  if (d == nullptr) return MF_ERR_INVALID_ARG;
+  if (d->hidden <= 0 || d->heads <= 0 || d->channels <= 0 || d->mlp_ratio <= 0 || d->freq_dim <= 0)
+    return MF_ERR_INVALID_ARG;
+  if (d->hidden % d->heads != 0) return MF_ERR_INVALID_ARG;
+  const int D = d->hidden / d->heads;
+  if (D != 64 && D != 128) return MF_ERR_UNSUPPORTED;
+  if (d->hidden % 256 != 0 || d->hidden > 4096) return MF_ERR_UNSUPPORTED;
+  if ((d->mlp_ratio * d->hidden) % 256 != 0) return MF_ERR_UNSUPPORTED;
+  if (d->channels != 64 && d->channels != 128) return MF_ERR_UNSUPPORTED;
+  if (d->freq_dim % 256 != 0) return MF_ERR_UNSUPPORTED;
+  return MF_OK;
+}
+
+mf_status check_plan(const mf_plan* p, int dev) {
+  if (p == nullptr) return MF_ERR_INVALID_ARG;
+  if (p->d_blob == nullptr) return MF_ERR_NOT_UPLOADED;
+  if (p->device != dev) return MF_ERR_INVALID_ARG;
+  return MF_OK;
+}
+
+mf_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MF_OK : MF_ERR_CUDA; }
+
+#define MF_TRY(x)                     \
+  do {                                \
+    mf_status _s = (x);               \
+    if (_s != MF_OK) return _s;       \
+  } while (0)
+#define MF_CUDA(x)                    \
+  do {                                \
+    if ((x) != cudaSuccess) return MF_ERR_CUDA; \
+  } while (0)
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ------------------------------------------------------------------ workspace layouts
+struct BlockLayout {
+  size_t off[8];  // c, mod, a, q, k, v, o, hidden
+  size_t sinus, h1;
+  size_t total;
+};
+
+BlockLayout block_layout(const mf_plan* p, const mf_dims* d) {
+  BlockLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = al256(o + bytes); return r; };
+  const size_t S = p->S, N = p->N, H = d->hidden, F = d->freq_dim, R = (size_t)d->mlp_ratio * H;
+  L.off[0] = take(S * H * 4);
+  L.off[1] = take(S * 12 * H * 4);
+  L.off[2] = take(N * H * 2);
+  L.off[3] = take(N * H * 2);
+  L.off[4] = take(N * H * 2);
+  L.off[5] = take(N * H * 2);
+  L.off[6] = take(N * H * 2);
+  L.off[7] = take(N * R * 2);
+  L.sinus = take(S * F * 4);
+  L.h1 = take(S * H * 4);
+  L.total = o;
+  return L;
+}
+
+struct FinalLayout {
+  size_t c, fmod, a, sinus, h1, total;
+};
+
+FinalLayout final_layout(const mf_plan* p, const mf_dims* d) {
+  FinalLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = al256(o + bytes); return r; };
+  const size_t S = p->S, H = d->hidden, F = d->freq_dim;
+  L.c = take(S * H * 4);
+  L.fmod = take(S * 2 * H * 4);
+  L.a = take((size_t)p->Ni * H * 2);
+  L.sinus = take(S * F * 4);
+  L.h1 = take(S * H * 4);
+  L.total = o;
+  return L;
+}
+
+// ------------------------------------------------------------------ GEMM driver
+struct GemmSpec {
+  int M, N, K;
+  const void* A;
+  const void* B;
+  const void* bias;
+  void* out;
+  int ldo;
+  int row_off;
+  int stream;
+};
+
+mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmParams& p,
+                   const DevInfo* di, cudaStream_t st) {
+  p.n_prob = 0;
+  p.tile_begin[0] = 0;
+  int begin = 0;
+  for (int s = 0; s < nspec; ++s) {
+    const GemmSpec& g = specs[s];
+    if (g.M <= 0) continue;
+    const int i = p.n_prob;
+    if (!make_tmap(&p.tmA[i], g.A, g.K, g.M, 128)) return MF_ERR_CUDA;
+    if (!make_tmap(&p.tmB[i], g.B, g.K, g.N, BN)) return MF_ERR_CUDA;
+    p.prob[i].M = g.M;
+    p.prob[i].N = g.N;
+    p.prob[i].K = g.K;
+    p.prob[i].row_off = g.row_off;
+    p.prob[i].stream = g.stream;
+    p.prob[i].ldo = g.ldo;
+    p.prob[i].bias = static_cast<const bf16*>(g.bias);
+    p.prob[i].out = g.out;
+    p.tiles_m[i] = (g.M + 127) / 128;
+    p.tiles_n[i] = (g.N + BN - 1) / BN;
+    begin += p.tiles_m[i] * p.tiles_n[i];
+    p.tile_begin[i + 1] = begin;
+    p.n_prob++;
+  }
+  if (p.n_prob == 0) return MF_OK;
+  if (p.n_prob == 1) p.tile_begin[2] = begin;
+  p.status = di->status;
+  p.wait_limit_ns = wait_limit_ns();
+  return cuda_status(mf::launch_gemm(p, BN, epi, di->sms, st));
+}
+
+mf_status conditioning(const mf_plan* p, const mf_dims* d, const mf_temb_weights* tw,
+                       const float* t, float* sinus, float* h1, float* c, cudaStream_t st) {
+  const int S = p->S, H = d->hidden, F = d->freq_dim;
+  MF_CUDA(mf::launch_sinusoid(t, S, F, sinus, st));
+  MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(tw->w_t1), static_cast<const bf16*>(tw->b_t1),
+                          sinus, S, F, H, h1, H, 0, 1, st));
+  MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(tw->w_t2), static_cast<const bf16*>(tw->b_t2), h1,
+                          S, H, H, c, H, 0, 1, st));
+  return MF_OK;
+}
+
+bool temb_ok(const mf_temb_weights* t) {
+  return t && t->w_t1 && t->b_t1 && t->w_t2 && t->b_t2 && aligned(t->w_t1, 16) &&
+         aligned(t->w_t2, 16);
+}
+
+bool stream_ok(const mf_stream_weights& s) {
+  const void* ptrs[] = {s.w_mod, s.b_mod, s.w_qkv, s.b_qkv, s.w_o, s.b_o, s.w_1, s.b_1, s.w_2, s.b_2};
+  for (const void* q : ptrs)
+    if (q == nullptr || !aligned(q, 16)) return false;
+  return true;
+}
+
+}  // namespace
+
+// ====================================================================== plan upload / free
+extern "C" mf_status mf_plan_upload(mf_plan* p, void* stream) {
+  if (p == nullptr) return MF_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MF_ERR_CUDA;
+  if (p->d_blob != nullptr) return p->device == dev ? MF_OK : MF_ERR_INVALID_ARG;
+
+  struct Part { const void* src; size_t bytes; size_t off; };
+  const int32_t* srcs[] = {p->cu.data(), p->cui.data(), p->pos.data(), p->srow_joint.data(),
+                           p->srow_seq.data(), p->joint_srow.data(), p->img_seq.data(),
+                           p->img_pair.data(), p->img_target.data(), p->seq_role.data(),
+                           p->items.data()};
+  size_t counts[] = {p->cu.size(), p->cui.size(), p->pos.size(), p->srow_joint.size(),
+                     p->srow_seq.size(), p->joint_srow.size(), p->img_seq.size(),
+                     p->img_pair.size(), p->img_target.size(), p->seq_role.size(),
+                     p->items.size()};
+  const int np = 11;
+  size_t off[12];
+  size_t o = 0;
+  for (int i = 0; i < np; ++i) {
+    off[i] = o;
+    o = (o + counts[i] * 4 + 63) & ~size_t(63);
+  }
+  off[np] = o;
+  o = (o + p->t.size() * 4 + 63) & ~size_t(63);
+  p->blob_bytes = o > 0 ? o : 64;
+
+  void* blob = nullptr;
+  if (cudaMalloc(&blob, p->blob_bytes) != cudaSuccess) return MF_ERR_CUDA;
+  // staged in one host buffer; the upload is synchronised before the buffer is released
+  char* host = static_cast<char*>(std::malloc(p->blob_bytes));
+  if (host == nullptr) { cudaFree(blob); return MF_ERR_CUDA; }
+  std::memset(host, 0, p->blob_bytes);
+  for (int i = 0; i < np; ++i)
+    if (counts[i]) std::memcpy(host + off[i], srcs[i], counts[i] * 4);
+  if (!p->t.empty()) std::memcpy(host + off[np], p->t.data(), p->t.size() * 4);
+  cudaError_t e = cudaMemcpyAsync(blob, host, p->blob_bytes, cudaMemcpyHostToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  std::free(host);
+  if (e != cudaSuccess) { cudaFree(blob); return MF_ERR_CUDA; }
+
+  char* b = static_cast<char*>(blob);
+  p->d_cu = reinterpret_cast<const int32_t*>(b + off[0]);
+  p->d_cui = reinterpret_cast<const int32_t*>(b + off[1]);
+  p->d_pos = reinterpret_cast<const int32_t*>(b + off[2]);
+  p->d_srow_joint = reinterpret_cast<const int32_t*>(b + off[3]);
+  p->d_srow_seq = reinterpret_cast<const int32_t*>(b + off[4]);
+  p->d_joint_srow = reinterpret_cast<const int32_t*>(b + off[5]);
+  p->d_img_seq = reinterpret_cast<const int32_t*>(b + off[6]);
+  p->d_img_pair = reinterpret_cast<const int32_t*>(b + off[7]);
+  p->d_img_target = reinterpret_cast<const int32_t*>(b + off[8]);
+  p->d_seq_role = reinterpret_cast<const int32_t*>(b + off[9]);
+  p->d_items = reinterpret_cast<const int32_t*>(b + off[10]);
+  p->d_t = reinterpret_cast<const float*>(b + off[11]);
+  p->d_blob = blob;
+  p->device = dev;
+  return MF_OK;
+}
+
+extern "C" void mf_plan_free(mf_plan* p) {
+  if (p == nullptr) return;
+  if (p->d_blob != nullptr) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    cudaFree(p->d_blob);
+    if (cur != p->device && cur >= 0) cudaSetDevice(cur);
+  }
+  delete p;
+}
+
+// ====================================================================== block forward
+extern "C" size_t mf_block_workspace_bytes(const mf_plan* p, const mf_dims* d) {
+  if (p == nullptr || check_dims(d) != MF_OK) return 0;
+  return block_layout(p, d).total;
+}
+
+extern "C" mf_status mf_block_workspace_layout(const mf_plan* p, const mf_dims* d, size_t* offsets,
+                                               int32_t n) {
+  if (p == nullptr || offsets == nullptr || n < 8) return MF_ERR_INVALID_ARG;
+  MF_TRY(check_dims(d));
+  BlockLayout L = block_layout(p, d);
+  for (int i = 0; i < 8; ++i) offsets[i] = L.off[i];
+  return MF_OK;
+}
+
+extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weights* w,
+                                      const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
+                                      size_t ws_bytes, void* stream) {
+  DevInfo* di = nullptr;
+  int dev = -1;
+  MF_TRY(device_info(&di, &dev));
+  MF_TRY(check_plan(p, dev));
+  MF_TRY(check_dims(d));
+  if (w == nullptr || !temb_ok(&w->temb) || !stream_ok(w->txt) || !stream_ok(w->img))
+    return MF_ERR_INVALID_ARG;
+  if (p->N == 0) return MF_OK;
+  if ((p->Nt > 0 && d_x_txt == nullptr) || (p->Ni > 0 && d_x_img == nullptr) || d_ws == nullptr)
+    return MF_ERR_INVALID_ARG;
+  if (!aligned(d_x_txt, 16) || !aligned(d_x_img, 16) || !aligned(d_ws, 256) || !aligned(d_t, 4))
+    return MF_ERR_ALIGNMENT;
+  const BlockLayout L = block_layout(p, d);
+  if (ws_bytes < L.total) return MF_ERR_WORKSPACE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(d_ws);
+  const int S = p->S, N = p->N, Nt = p->Nt, Ni = p->Ni, H = d->hidden, D = H / d->heads;
+  const int R = d->mlp_ratio * H;
+  const float* t = d_t ? d_t : p->d_t;
+  float* c = reinterpret_cast<float*>(ws + L.off[0]);
+  float* mod = reinterpret_cast<float*>(ws + L.off[1]);
+  bf16* a = reinterpret_cast<bf16*>(ws + L.off[2]);
+  bf16* q = reinterpret_cast<bf16*>(ws + L.off[3]);
+  bf16* k = reinterpret_cast<bf16*>(ws + L.off[4]);
+  bf16* v = reinterpret_cast<bf16*>(ws + L.off[5]);
+  bf16* o = reinterpret_cast<bf16*>(ws + L.off[6]);
+  bf16* hid = reinterpret_cast<bf16*>(ws + L.off[7]);
+  float* sinus = reinterpret_cast<float*>(ws + L.sinus);
+  float* h1 = reinterpret_cast<float*>(ws + L.h1);
+  bf16* xt = static_cast<bf16*>(d_x_txt);
+  bf16* xi = static_cast<bf16*>(d_x_img);
+
+  // 1. timestep condition c = SiLU(temb(t)) and the per-sample adaLN modulation of both streams
+  MF_TRY(conditioning(p, d, &w->temb, t, sinus, h1, c, st));
+  MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w->txt.w_mod), static_cast<const bf16*>(w->txt.b_mod),
+                          c, S, H, 6 * H, mod, 12 * H, 0, 0, st));
+  MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w->img.w_mod), static_cast<const bf16*>(w->img.b_mod),
+                          c, S, H, 6 * H, mod, 12 * H, 6 * H, 0, st));
+
+  // 2. a = LN(x)(1 + scale1) + shift1, stream-sorted
+  mf::LnModArgs ln{xt, xi, Nt, N, H, p->d_srow_seq, mod, 12LL * H, 6LL * H, 0, H, a};
+  MF_CUDA(mf::launch_ln_modulate(ln, st));
+
+  // 3. q | k | v = a W_qkv^T + b, RoPE, scattered to joint order
+  mf::GemmParams gp{};
+  gp.srow_seq = p->d_srow_seq;
+  gp.srow_joint = p->d_srow_joint;
+  gp.pos = p->d_pos;
+  gp.mod = mod;
+  gp.H = H;
+  gp.head_dim = D;
+  gp.q = q;
+  gp.k = k;
+  gp.v = v;
+  {
+    GemmSpec sp[2] = {{Nt, 3 * H, H, a, w->txt.w_qkv, w->txt.b_qkv, nullptr, 0, 0, 0},
+                      {Ni, 3 * H, H, a + (size_t)Nt * H, w->img.w_qkv, w->img.b_qkv, nullptr, 0, Nt, 1}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiQkvRope, 256, gp, di, st));
+  }
+
+  // 4. joint varlen attention -> o (stream-sorted)
+  {
+    mf::AttnParams ap{};
+    if (!make_tmap(&ap.tmQ, q, H, N, 128) || !make_tmap(&ap.tmK, k, H, N, 128) ||
+        !make_tmap(&ap.tmV, v, H, N, 128))
+      return MF_ERR_CUDA;
+    ap.cu = p->d_cu;
+    ap.items = p->d_items;
+    ap.joint_srow = p->d_joint_srow;
+    ap.out = o;
+    ap.H = H;
+    ap.heads = d->heads;
+    ap.n_items = p->n_items;
+    ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    ap.status = di->status;
+    ap.wait_limit_ns = wait_limit_ns();
+    MF_CUDA(mf::launch_attention(ap, D, st));
+  }
+
+  // 5. x += gate1 (o W_o^T + b_o)
+  gp.gate_off = 2 * H;
+  {
+    GemmSpec sp[2] = {{Nt, H, H, o, w->txt.w_o, w->txt.b_o, xt, H, 0, 0},
+                      {Ni, H, H, o + (size_t)Nt * H, w->img.w_o, w->img.b_o, xi, H, Nt, 1}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid, 256, gp, di, st));
+  }
+
+  // 6. a = LN(x)(1 + scale2) + shift2
+  ln.shift_off = 3 * H;
+  ln.scale_off = 4 * H;
+  MF_CUDA(mf::launch_ln_modulate(ln, st));
+
+  // 7. hidden = GELU(a W_1^T + b_1)
+  {
+    GemmSpec sp[2] = {{Nt, R, H, a, w->txt.w_1, w->txt.b_1, hid, R, 0, 0},
+                      {Ni, R, H, a + (size_t)Nt * H, w->img.w_1, w->img.b_1, hid + (size_t)Nt * R, R, Nt, 1}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGelu, 256, gp, di, st));
+  }
+
+  // 8. x += gate2 (hidden W_2^T + b_2)
+  gp.gate_off = 5 * H;
+  {
+    GemmSpec sp[2] = {{Nt, H, R, hid, w->txt.w_2, w->txt.b_2, xt, H, 0, 0},
+                      {Ni, H, R, hid + (size_t)Nt * R, w->img.w_2, w->img.b_2, xi, H, Nt, 1}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid, 256, gp, di, st));
+  }
+  return MF_OK;
+}
+
+// ====================================================================== embed / final
+extern "C" mf_status mf_embed(const mf_plan* p, const mf_dims* d, const void* w_in, const void* b_in,
+                              const void* d_zt, void* d_x_img, void* stream) {
+  DevInfo* di = nullptr;
+  int dev = -1;
+  MF_TRY(device_info(&di, &dev));
+  MF_TRY(check_plan(p, dev));
+  MF_TRY(check_dims(d));
+  if (w_in == nullptr || b_in == nullptr) return MF_ERR_INVALID_ARG;
+  if (p->Ni == 0) return MF_OK;
+  if (d_zt == nullptr || d_x_img == nullptr) return MF_ERR_INVALID_ARG;
+  if (!aligned(w_in, 16) || !aligned(b_in, 16) || !aligned(d_zt, 16) || !aligned(d_x_img, 16))
+    return MF_ERR_ALIGNMENT;
+  const int H = d->hidden, C = d->channels;
+  mf::GemmParams gp{};
+  GemmSpec sp[1] = {{p->Ni, H, C, d_zt, w_in, b_in, d_x_img, H, 0, 1}};
+  return run_gemm(sp, 1, mf::kEpiBiasBf16, H >= 256 ? 256 : 128, gp, di,
+                  static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t mf_final_workspace_bytes(const mf_plan* p, const mf_dims* d) {
+  if (p == nullptr || check_dims(d) != MF_OK) return 0;
+  return final_layout(p, d).total;
+}
+
+extern "C" mf_status mf_final(const mf_plan* p, const mf_dims* d, const mf_temb_weights* temb,
+                              const void* w_fmod, const void* b_fmod, const void* w_out,
+                              const void* b_out, const float* d_t, const void* d_x_img, float* d_v,
+                              void* d_ws, size_t ws_bytes, void* stream) {
+  DevInfo* di = nullptr;
+  int dev = -1;
+  MF_TRY(device_info(&di, &dev));
+  MF_TRY(check_plan(p, dev));
+  MF_TRY(check_dims(d));
+  if (!temb_ok(temb) || w_fmod == nullptr || b_fmod == nullptr || w_out == nullptr || b_out == nullptr)
+    return MF_ERR_INVALID_ARG;
+  if (p->Ni == 0) return MF_OK;
+  if (d_x_img == nullptr || d_v == nullptr || d_ws == nullptr) return MF_ERR_INVALID_ARG;
+  if (!aligned(w_fmod, 16) || !aligned(w_out, 16) || !aligned(b_out, 16) || !aligned(d_x_img, 16) ||
+      !aligned(d_v, 16) || !aligned(d_ws, 256) || !aligned(d_t, 4))
+    return MF_ERR_ALIGNMENT;
+  const FinalLayout L = final_layout(p, d);
+  if (ws_bytes < L.total) return MF_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(d_ws);
+  const int S = p->S, H = d->hidden, C = d->channels;
+  const float* t = d_t ? d_t : p->d_t;
+  float* c = reinterpret_cast<float*>(ws + L.c);
+  float* fmod = reinterpret_cast<float*>(ws + L.fmod);
+  bf16* a = reinterpret_cast<bf16*>(ws + L.a);
+  MF_TRY(conditioning(p, d, temb, t, reinterpret_cast<float*>(ws + L.sinus),
+                      reinterpret_cast<float*>(ws + L.h1), c, st));
+  MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w_fmod), static_cast<const bf16*>(b_fmod), c, S, H,
+                          2 * H, fmod, 2 * H, 0, 0, st));
+  mf::LnModArgs ln{static_cast<const bf16*>(d_x_img), nullptr, p->Ni, p->Ni, H,
+                   p->d_srow_seq + p->Nt, fmod, 2LL * H, 0, 0, H, a};
+  MF_CUDA(mf::launch_ln_modulate(ln, st));
+  mf::GemmParams gp{};
+  GemmSpec sp[1] = {{p->Ni, C, H, a, w_out, b_out, d_v, C, 0, 1}};
+  return run_gemm(sp, 1, mf::kEpiBiasF32, 128, gp, di, st);
+}
+
+// ====================================================================== rectified-flow epilogues
+namespace {
+mf_status check_latent_call(const mf_plan* p, int32_t C, DevInfo** di) {
+  int dev = -1;
+  MF_TRY(device_info(di, &dev));
+  MF_TRY(check_plan(p, dev));
+  if (C <= 0 || C % 4 != 0) return MF_ERR_INVALID_ARG;
+  return MF_OK;
+}
+}  // namespace
+
+extern "C" mf_status mf_interpolate(const mf_plan* p, int32_t C, const float* d_t, const float* d_z,
+                                    const float* d_eps, float* d_zt, void* d_zt_bf16, void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(check_latent_call(p, C, &di));
+  if (p->Ni == 0) return MF_OK;
+  if (d_z == nullptr || d_eps == nullptr || (d_zt == nullptr && d_zt_bf16 == nullptr))
+    return MF_ERR_INVALID_ARG;
+  if (!aligned(d_z, 16) || !aligned(d_eps, 16) || !aligned(d_zt, 16) || !aligned(d_zt_bf16, 16) ||
+      !aligned(d_t, 4))
+    return MF_ERR_ALIGNMENT;
+  return cuda_status(mf::launch_interpolate(p->d_img_seq, p->d_img_target, d_t ? d_t : p->d_t, p->Ni, C,
+                                            d_z, d_eps, d_zt, static_cast<bf16*>(d_zt_bf16),
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" mf_status mf_cfg_combine(const mf_plan* p, int32_t C, float w, const float* d_v,
+                                    float* d_v_out, void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(check_latent_call(p, C, &di));
+  if (p->Ni == 0) return MF_OK;
+  if (d_v == nullptr || d_v_out == nullptr || !std::isfinite(w)) return MF_ERR_INVALID_ARG;
+  if (!aligned(d_v, 16) || !aligned(d_v_out, 16)) return MF_ERR_ALIGNMENT;
+  const size_t bytes = (size_t)p->Ni * C * 4;
+  const char* a = reinterpret_cast<const char*>(d_v);
+  const char* b = reinterpret_cast<const char*>(d_v_out);
+  if (a != b && a < b + bytes && b < a + bytes) return MF_ERR_INVALID_ARG;  // partial overlap
+  return cuda_status(mf::launch_cfg(p->d_img_seq, p->d_seq_role, p->d_img_pair, p->Ni, C, w, d_v,
+                                    d_v_out, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" mf_status mf_euler_step(const mf_plan* p, int32_t C, float dt, const float* d_v, float* d_z,
+                                   void* d_z_bf16, void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(check_latent_call(p, C, &di));
+  if (p->Ni == 0) return MF_OK;
+  if (d_v == nullptr || d_z == nullptr || !std::isfinite(dt)) return MF_ERR_INVALID_ARG;
+  if (!aligned(d_v, 16) || !aligned(d_z, 16) || !aligned(d_z_bf16, 16)) return MF_ERR_ALIGNMENT;
+  return cuda_status(mf::launch_euler(p->Ni, C, dt, d_v, d_z, static_cast<bf16*>(d_z_bf16),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" size_t mf_flow_loss_workspace_bytes(const mf_plan* p) {
+  if (p == nullptr) return 0;
+  return al256((size_t)(p->Ni > 0 ? p->Ni : 1) * sizeof(double));
+}
+
+extern "C" mf_status mf_flow_loss(const mf_plan* p, int32_t C, const float* d_z, const float* d_eps,
+                                  const float* d_v, double* d_loss_sum, int64_t* d_count,
+                                  double* d_mean, void* d_ws, size_t ws_bytes, void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(check_latent_call(p, C, &di));
+  if (d_loss_sum == nullptr || d_count == nullptr || d_mean == nullptr) return MF_ERR_INVALID_ARG;
+  if (p->Ni > 0 && (d_z == nullptr || d_eps == nullptr || d_v == nullptr || d_ws == nullptr))
+    return MF_ERR_INVALID_ARG;
+  if (!aligned(d_z, 16) || !aligned(d_eps, 16) || !aligned(d_v, 16) || !aligned(d_loss_sum, 8) ||
+      !aligned(d_count, 8) || !aligned(d_mean, 8) || !aligned(d_ws, 256))
+    return MF_ERR_ALIGNMENT;
+  if (ws_bytes < mf_flow_loss_workspace_bytes(p)) return MF_ERR_WORKSPACE;
+  return cuda_status(mf::launch_flow_loss(p->d_cui, p->d_img_target, p->S, p->Ni, C, d_z, d_eps, d_v,
+                                          static_cast<double*>(d_ws), d_loss_sum,
+                                          reinterpret_cast<long long*>(d_count), d_mean,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+// ====================================================================== building blocks
+extern "C" mf_status mf_attention(const mf_plan* p, int32_t heads, int32_t head_dim, const void* d_q,
+                                  const void* d_k, const void* d_v, void* d_o, void* stream) {
+  DevInfo* di = nullptr;
+  int dev = -1;
+  MF_TRY(device_info(&di, &dev));
+  MF_TRY(check_plan(p, dev));
+  if (heads <= 0) return MF_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
+  if (p->N == 0) return MF_OK;
+  if (d_q == nullptr || d_k == nullptr || d_v == nullptr || d_o == nullptr) return MF_ERR_INVALID_ARG;
+  if (!aligned(d_q, 16) || !aligned(d_k, 16) || !aligned(d_v, 16) || !aligned(d_o, 16))
+    return MF_ERR_ALIGNMENT;
+  const int H = heads * head_dim;
+  mf::AttnParams ap{};
+  if (!make_tmap(&ap.tmQ, d_q, H, p->N, 128) || !make_tmap(&ap.tmK, d_k, H, p->N, 128) ||
+      !make_tmap(&ap.tmV, d_v, H, p->N, 128))
+    return MF_ERR_CUDA;
+  ap.cu = p->d_cu;
+  ap.items = p->d_items;
+  ap.joint_srow = p->d_joint_srow;
+  ap.out = static_cast<bf16*>(d_o);
+  ap.H = H;
+  ap.heads = heads;
+  ap.n_items = p->n_items;
+  ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+  ap.status = di->status;
+  ap.wait_limit_ns = wait_limit_ns();
+  return cuda_status(mf::launch_attention(ap, head_dim, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" mf_status mf_gemm(int32_t M, int32_t N, int32_t K, const void* d_a, const void* d_b,
+                             const void* d_bias, void* d_c, int32_t out_f32, void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(device_info(&di));
+  if (M < 0 || N <= 0 || K <= 0 || N % 32 != 0 || K % 64 != 0) return MF_ERR_INVALID_ARG;
+  if (M == 0) return MF_OK;
+  if (d_a == nullptr || d_b == nullptr || d_c == nullptr) return MF_ERR_INVALID_ARG;
+  if (!aligned(d_a, 16) || !aligned(d_b, 16) || !aligned(d_bias, 16) || !aligned(d_c, 16))
+    return MF_ERR_ALIGNMENT;
+  mf::GemmParams gp{};
+  GemmSpec sp[1] = {{M, N, K, d_a, d_b, d_bias, d_c, N, 0, 0}};
+  return run_gemm(sp, 1, out_f32 ? mf::kEpiBiasF32 : mf::kEpiBiasBf16, N <= 128 ? 128 : 256, gp, di,
+                  static_cast<cudaStream_t>(stream));
+}
+
+// ====================================================================== status
+extern "C" mf_status mf_check(void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(device_info(&di));
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MF_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, di->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MF_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(di->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MF_ERR_CUDA;
+    return MF_ERR_DEVICE_TIMEOUT;
+  }
+  return MF_OK;
+}
+
+extern "C" mf_status mf_selftest_timeout(int32_t limit_us, void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(device_info(&di));
+  if (limit_us < 1 || limit_us > 1000000) return MF_ERR_INVALID_ARG;
+  MF_TRY(mf_check(stream));  // start from a clean status word
+  if (mf::launch_timeout_selftest(di->status, (unsigned long long)limit_us * 1000ull,
+                                  static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MF_ERR_CUDA;
+  return mf_check(stream);
+}

@@ -1,0 +1,342 @@
+// Persistent grouped GEMM for sm_103a: TMA (128-byte swizzle) -> shared-memory ring ->
+// tcgen05.mma (one thread issues, f32 accumulators in TMEM, two accumulator buffers so the
+// epilogue of one tile overlaps the main loop of the next) -> tcgen05.ld epilogue warps.
+//
+// Warp roles (192 threads):  warp 0 lane 0 TMA producer; warp 1 TMEM allocator and lane 0
+// MMA issuer; warps 2..5 epilogue (warp w reads TMEM lanes 32*(w%4)..+31, i.e. tile rows).
+//
+// The fused epilogues implement the NR-MMDiT chains that the Mage-Flow pages list as fused
+// memory-bound work - norm, RoPE, gating, residual (PaperReading review of "Mage-Flow: An
+// Efficient Native-Resolution Foundation Model for Image Generation and Editing", §2.2 (3);
+// hyper.ai summary, 方法): bias, RoPE over (frame, row, col) with the scatter to joint order,
+// GELU, and the gated residual x += gate * y.
+#include "gemm.cuh"
+
+namespace mf {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kGroupM = 16;  // tile rasterisation: 16 row tiles share a sweep over N
+
+__device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& pi, int& m,
+                                            int& n) {
+  pi = (p.n_prob > 1 && tile >= p.tile_begin[1]) ? 1 : 0;
+  const int t = tile - p.tile_begin[pi];
+  const int tn = p.tiles_n[pi], tm = p.tiles_m[pi];
+  const int group = t / (kGroupM * tn);
+  const int first_m = group * kGroupM;
+  const int gm = min(kGroupM, tm - first_m);
+  const int local = t - group * kGroupM * tn;
+  m = first_m + local % gm;
+  n = local / gm;
+}
+
+__device__ __forceinline__ void load_bias32(const bf16* bias, int col0, float (&v)[32]) {
+  if (bias == nullptr) return;
+  const uint4* b = reinterpret_cast<const uint4*>(bias + col0);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u = __ldg(b + i);
+    float2 f0 = unpack_bf16x2(u.x), f1 = unpack_bf16x2(u.y), f2 = unpack_bf16x2(u.z),
+           f3 = unpack_bf16x2(u.w);
+    v[8 * i + 0] += f0.x; v[8 * i + 1] += f0.y; v[8 * i + 2] += f1.x; v[8 * i + 3] += f1.y;
+    v[8 * i + 4] += f2.x; v[8 * i + 5] += f2.y; v[8 * i + 6] += f3.x; v[8 * i + 7] += f3.y;
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(bf16* dst, const float (&v)[32]) {
+  uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    o[i] = u;
+  }
+}
+
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const GemmProblem& pr,
+                                               int row, int col0, const uint32_t (&r)[32],
+                                               const float* rope_inv, const int* rope_axis) {
+  if (row >= pr.M || col0 >= pr.N) return;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  load_bias32(pr.bias, col0, v);
+
+  if constexpr (EPI == kEpiBiasBf16 || EPI == kEpiGelu) {
+    if constexpr (EPI == kEpiGelu) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.7071067811865476f));
+    }
+    store_bf16x32(static_cast<bf16*>(pr.out) + (size_t)row * pr.ldo + col0, v);
+  } else if constexpr (EPI == kEpiBiasF32) {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(pr.out) + (size_t)row * pr.ldo + col0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else if constexpr (EPI == kEpiGateResid) {
+    const int srow = pr.row_off + row;
+    const int seq = __ldg(p.srow_seq + srow);
+    const float4* g = reinterpret_cast<const float4*>(
+        p.mod + ((size_t)seq * 2 + pr.stream) * 6 * (size_t)p.H + p.gate_off + col0);
+    bf16* x = static_cast<bf16*>(pr.out) + (size_t)row * pr.ldo + col0;
+    uint4* xv = reinterpret_cast<uint4*>(x);
+    float out[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 u = xv[i];
+      float4 ga = __ldg(g + 2 * i), gb = __ldg(g + 2 * i + 1);
+      float2 x0 = unpack_bf16x2(u.x), x1 = unpack_bf16x2(u.y), x2 = unpack_bf16x2(u.z),
+             x3 = unpack_bf16x2(u.w);
+      out[8 * i + 0] = fmaf(ga.x, v[8 * i + 0], x0.x);
+      out[8 * i + 1] = fmaf(ga.y, v[8 * i + 1], x0.y);
+      out[8 * i + 2] = fmaf(ga.z, v[8 * i + 2], x1.x);
+      out[8 * i + 3] = fmaf(ga.w, v[8 * i + 3], x1.y);
+      out[8 * i + 4] = fmaf(gb.x, v[8 * i + 4], x2.x);
+      out[8 * i + 5] = fmaf(gb.y, v[8 * i + 5], x2.y);
+      out[8 * i + 6] = fmaf(gb.z, v[8 * i + 6], x3.x);
+      out[8 * i + 7] = fmaf(gb.w, v[8 * i + 7], x3.y);
+    }
+    store_bf16x32(x, out);
+  } else if constexpr (EPI == kEpiQkvRope) {
+    const int srow = pr.row_off + row;
+    const int joint = __ldg(p.srow_joint + srow);
+    const int which = col0 / p.H;
+    const int cc = col0 - which * p.H;
+    bf16* dst = (which == 0 ? p.q : (which == 1 ? p.k : p.v)) + (size_t)joint * p.H + cc;
+    if (which < 2) {
+      const int* ps = p.pos + (size_t)joint * 3;
+      const float pa[3] = {(float)__ldg(ps), (float)__ldg(ps + 1), (float)__ldg(ps + 2)};
+      const int g0 = (cc % p.head_dim) >> 1;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float th = pa[rope_axis[g0 + i]] * rope_inv[g0 + i];
+        float s, c;
+        sincosf(th, &s, &c);
+        const float x0 = v[2 * i], x1 = v[2 * i + 1];
+        v[2 * i] = x0 * c - x1 * s;
+        v[2 * i + 1] = x0 * s + x1 * c;
+      }
+    }
+    store_bf16x32(dst, v);
+  }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int STAGES = (BN == 256) ? 4 : 6;
+  constexpr uint32_t A_BYTES = kBM * kBK * 2;
+  constexpr uint32_t B_BYTES = BN * kBK * 2;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN, false);
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  __shared__ float rope_inv[64];
+  __shared__ int rope_axis[64];
+
+  uint8_t* smem = align1024(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int total = p.tile_begin[p.n_prob];
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 128);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if constexpr (EPI == kEpiQkvRope) {
+    // pair g of a head: axis block (frame D/8 | row 7D/16 | col 7D/16), inverse frequency
+    // 10000^(-2j/width) for the pair's index j inside its block
+    const int D = p.head_dim;
+    if ((int)threadIdx.x < D / 2) {
+      const int g = threadIdx.x, d = 2 * g;
+      const int wf = D / 8, wr = 7 * D / 16;
+      int axis, j, width;
+      if (d < wf) { axis = 0; j = d / 2; width = wf; }
+      else if (d < wf + wr) { axis = 1; j = (d - wf) / 2; width = wr; }
+      else { axis = 2; j = (d - wf - wr) / 2; width = wr; }
+      rope_axis[g] = axis;
+      rope_inv[g] = (float)exp(-(2.0 * j / width) * 9.210340371976184);  // ln(10000)
+    }
+  }
+  if (warp == 1) tmem_alloc(&tmem_base_sh, TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.n_prob; ++i) {
+      tma_prefetch_desc(&p.tmA[i]);
+      tma_prefetch_desc(&p.tmB[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t armed = 0, armed_par = 0;  // bit s: stage s armed; its parity
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        int pi, m, n;
+        decode_tile(p, tile, pi, m, n);
+        const int nkb = p.prob[pi].K / kBK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, lim) || *(volatile int*)&abort_flag) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+          tma_load_2d(sa, &p.tmA[pi], kb * kBK, m * kBM, &full_bar[stage]);
+          tma_load_2d(sa + A_BYTES, &p.tmB[pi], kb * kBK, n * BN, &full_bar[stage]);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        *(volatile int*)&abort_flag = 1;
+        report_status(p.status, kStatusTimeout);
+        for (int s = 0; s < STAGES; ++s)  // let this thread's copies land before exiting
+          if (armed & (1u << s)) mbar_wait(&full_bar[s], (armed_par >> s) & 1u, lim);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        int pi, m, n;
+        decode_tile(p, tile, pi, m, n);
+        const int nkb = p.prob[pi].K / kBK;
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, lim) || *(volatile int*)&abort_flag) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16(d_tmem, sdesc_sw128(a0 + k * 32, 16, 1024), sdesc_sw128(b0 + k * 32, 16, 1024),
+                     IDESC, (kb | k) != 0 ? 1u : 0u);
+          mma_commit(&empty_bar[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(&tfull_bar[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (!ok) {
+        *(volatile int*)&abort_flag = 1;
+        report_status(p.status, kStatusTimeout);
+        mma_commit(&drain_bar);  // wait for this thread's MMAs before TMEM is freed
+        mbar_wait(&drain_bar, 0, lim);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue warps
+    const int q = warp & 3;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int pi, m, n;
+      decode_tile(p, tile, pi, m, n);
+      const bool ok = mbar_wait(&tfull_bar[acc], acc_phase, lim);
+      if (!__all_sync(0xffffffffu, ok) || __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
+        if (lane == 0) {
+          *(volatile int*)&abort_flag = 1;
+          report_status(p.status, kStatusTimeout);
+        }
+        break;
+      }
+      tc_fence_after();
+      const GemmProblem& pr = p.prob[pi];
+      const int row = m * kBM + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tmem_base, q * 32, acc * BN + c), r);
+        tmem_ld_wait();
+        tmem_reg_fence(r);
+        epilogue_chunk<EPI>(p, pr, row, n * BN + c, r, rope_inv, rope_axis);
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int BN, int EPI>
+cudaError_t launch_t(const GemmParams& p, int num_sms, cudaStream_t stream) {
+  constexpr int STAGES = (BN == 256) ? 4 : 6;
+  const int smem = STAGES * (kBM * kBK * 2 + BN * kBK * 2) + 1024;
+  auto kern = gemm_kernel<BN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int total = p.tile_begin[p.n_prob];
+  if (total <= 0) return cudaSuccess;
+  const int grid = total < num_sms ? total : num_sms;
+  kern<<<grid, 192, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmParams& p, int BN, int epi, int num_sms, cudaStream_t stream) {
+#define MF_GEMM_CASE(bn, ep) \
+  if (BN == bn && epi == ep) return launch_t<bn, ep>(p, num_sms, stream);
+  MF_GEMM_CASE(256, kEpiBiasBf16)
+  MF_GEMM_CASE(256, kEpiBiasF32)
+  MF_GEMM_CASE(256, kEpiQkvRope)
+  MF_GEMM_CASE(256, kEpiGateResid)
+  MF_GEMM_CASE(256, kEpiGelu)
+  MF_GEMM_CASE(128, kEpiBiasBf16)
+  MF_GEMM_CASE(128, kEpiBiasF32)
+  MF_GEMM_CASE(128, kEpiQkvRope)
+  MF_GEMM_CASE(128, kEpiGateResid)
+  MF_GEMM_CASE(128, kEpiGelu)
+#undef MF_GEMM_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mf

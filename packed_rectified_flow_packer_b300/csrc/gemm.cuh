@@ -1,0 +1,53 @@
+// Grouped, persistent bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA)
+// with the NR-MMDiT block's fused epilogues.  C[M][N] = A[M][K] B[N][K]^T for up to two
+// problems (text stream, image stream) in one launch.
+#pragma once
+
+#include "common.cuh"
+#include "mageflow.h"
+
+namespace mf {
+
+enum GemmEpi : int {
+  kEpiBiasBf16 = 0,   // out bf16 = acc + bias
+  kEpiBiasF32 = 1,    // out f32  = acc + bias
+  kEpiQkvRope = 2,    // q | k | v = acc + bias; RoPE on q, k; rows scattered to joint order
+  kEpiGateResid = 3,  // x += gate[seq] * (acc + bias), x bf16 in place
+  kEpiGelu = 4,       // out bf16 = GELU(acc + bias)
+};
+
+struct GemmProblem {
+  int M, N, K;
+  int row_off;            // first stream-sorted row of this problem (for the row maps)
+  int stream;             // modulation stream (0 text, 1 image)
+  int ldo;                // output leading dimension in elements
+  const bf16* bias;       // [N] or nullptr
+  void* out;              // output (or the residual x for kEpiGateResid)
+};
+
+struct GemmParams {
+  CUtensorMap tmA[2];     // A [M][K], box {64, 128}, 128-byte swizzle
+  CUtensorMap tmB[2];     // B [N][K], box {64, BN}, 128-byte swizzle
+  GemmProblem prob[2];
+  int n_prob;
+  int tiles_m[2], tiles_n[2];
+  int tile_begin[3];
+  // epilogue inputs shared by the problems
+  const int* srow_seq;    // [rows] sample of each stream-sorted row
+  const int* srow_joint;  // [rows] joint token of each stream-sorted row
+  const int* pos;         // [N_tok][3]
+  const float* mod;       // [S][2][6H] modulation
+  int H;
+  int head_dim;
+  int gate_off;           // float offset of the gate chunk inside a (sample, stream) mod row
+  bf16* q;                // [N_tok][H] joint order
+  bf16* k;
+  bf16* v;
+  unsigned* status;
+  unsigned long long wait_limit_ns;
+};
+
+// Launches the persistent kernel for tile width BN in {128, 256}.
+cudaError_t launch_gemm(const GemmParams& p, int BN, int epi, int num_sms, cudaStream_t stream);
+
+}  // namespace mf

@@ -1,0 +1,55 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "mageflow.h"
+
+// A pack and every index buffer the kernels read.  Built once by mf_pack (host only) and
+// immutable afterwards; mf_plan_upload copies the buffers to the device in one blob.
+struct mf_plan {
+  int32_t budget = 0;
+  int32_t S = 0, N = 0, Nt = 0, Ni = 0, n_items = 0;
+
+  std::vector<int32_t> order;       // [S]    candidate index per packed sample
+  std::vector<int32_t> cu;          // [S+1]  joint offsets (cu_seqlens)
+  std::vector<int32_t> cut;         // [S+1]  text-stream offsets
+  std::vector<int32_t> cui;         // [S+1]  image-stream offsets
+  std::vector<int32_t> pos;         // [N*3]  (frame, row, col) per joint token
+  std::vector<int32_t> txt_seq, txt_joint;   // [Nt]
+  std::vector<int32_t> img_seq, img_joint;   // [Ni]
+  std::vector<int32_t> img_pair;    // [Ni]  CFG partner row or -1
+  std::vector<int32_t> img_target;  // [Ni]  1 = target frame
+  std::vector<int32_t> seq_role;    // [S]   cfg_role
+  std::vector<int32_t> items;       // [n_items*2] (sequence, query tile), longest first
+  std::vector<float> t;             // [S]   flow time per packed sample
+
+  // stream-sorted rows: text rows 0..Nt-1, then image rows Nt..Nt+Ni-1
+  std::vector<int32_t> srow_joint;  // [Nt+Ni] joint token of each stream-sorted row
+  std::vector<int32_t> srow_seq;    // [Nt+Ni] sample of each stream-sorted row
+  std::vector<int32_t> joint_srow;  // [N]     stream-sorted row of each joint token
+
+  // device copy (one allocation, owned by the plan)
+  int device = -1;
+  void* d_blob = nullptr;
+  size_t blob_bytes = 0;
+  const int32_t* d_cu = nullptr;
+  const int32_t* d_cui = nullptr;
+  const int32_t* d_pos = nullptr;
+  const int32_t* d_srow_joint = nullptr;
+  const int32_t* d_srow_seq = nullptr;
+  const int32_t* d_joint_srow = nullptr;
+  const int32_t* d_img_seq = nullptr;
+  const int32_t* d_img_pair = nullptr;
+  const int32_t* d_img_target = nullptr;
+  const int32_t* d_seq_role = nullptr;
+  const int32_t* d_items = nullptr;
+  const float* d_t = nullptr;
+};
+
+namespace mf {
+
+constexpr int kQTile = 128;  // attention query / key tile rows
+}  // namespace mf

@@ -1,0 +1,365 @@
+// Memory-bound kernels of the packed NR-MMDiT path: timestep conditioning GEMVs, the
+// LN + adaLN-modulate prologue, and the rectified-flow epilogues (interpolation, packed CFG,
+// Euler step, flow-matching loss).  Vectorised 16-byte accesses; one warp per row where a
+// row reduction is needed.
+//
+// Definitions: PaperReading review of "Mage-Flow: An Efficient Native-Resolution Foundation
+// Model for Image Generation and Editing", §2.2 (2) (z_t = (1 - t) z + t eps and the loss
+// ||v - (z - eps)||^2, editing loss on the target latent only), §2.2 (3) (packed CFG, fused
+// norm / gating chains) and §5 (ODE sampling from noise to data; CFG from the difference of
+// the conditional and unconditional predictions); hyper.ai summary, 方法.
+#include "pointwise.cuh"
+
+namespace mf {
+namespace {
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z),
+         d = unpack_bf16x2(u.w);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------------ conditioning
+__global__ void sinusoid_kernel(const float* __restrict__ t, int S, int F, float* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int half = F / 2;
+  if (i >= S * half) return;
+  const int s = i / half, j = i - s * half;
+  // computed in double: the argument reaches 1000 rad
+  const double a = 1000.0 * (double)t[s] * exp(-9.210340371976184 * (double)j / (double)half);
+  out[(size_t)s * F + j] = (float)cos(a);
+  out[(size_t)s * F + half + j] = (float)sin(a);
+}
+
+template <int ACT>
+__global__ void gemv_kernel(const bf16* __restrict__ W, const bf16* __restrict__ b,
+                            const float* __restrict__ x, int S, int K, int O, float* __restrict__ y,
+                            int y_stride, int y_off) {
+  const int o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (o >= O) return;
+  const bf16* w = W + (size_t)o * K;
+  const float bias = b ? __bfloat162float(b[o]) : 0.0f;
+  for (int s0 = 0; s0 < S; s0 += 4) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = lane * 8; k < K; k += 256) {
+      float wf[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(w + k)), wf);
+#pragma unroll
+      for (int si = 0; si < 4; ++si) {
+        if (s0 + si < S) {
+          const float4* xv = reinterpret_cast<const float4*>(x + (size_t)(s0 + si) * K + k);
+          const float4 a = __ldg(xv), c = __ldg(xv + 1);
+          acc[si] += wf[0] * a.x + wf[1] * a.y + wf[2] * a.z + wf[3] * a.w + wf[4] * c.x +
+                     wf[5] * c.y + wf[6] * c.z + wf[7] * c.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int si = 0; si < 4; ++si) {
+      const float r = warp_sum(acc[si]) + bias;
+      if (lane == 0 && s0 + si < S)
+        y[(size_t)(s0 + si) * y_stride + y_off + o] = ACT == 1 ? silu_f(r) : r;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ LN + modulate
+template <int NV>
+__global__ void ln_modulate_kernel(const LnModArgs a) {
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= a.rows) return;
+  const int H = a.H;
+  const bool second = r >= a.n_first;
+  const bf16* x = second ? a.x_second + (size_t)(r - a.n_first) * H : a.x_first + (size_t)r * H;
+  float v[NV][8];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    unpack8(__ldg(reinterpret_cast<const uint4*>(x) + lane + 32 * i), v[i]);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s += v[i][u];
+  }
+  const float mean = warp_sum(s) / (float)H;
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float d = v[i][u] - mean;
+      q += d * d;
+    }
+  const float rstd = rsqrtf(warp_sum(q) / (float)H + 1e-6f);
+  const int seq = __ldg(a.row_seq + r);
+  const float* mrow = a.mod + (size_t)seq * a.seq_stride + (second ? a.stream_stride : 0);
+  const float4* sh = reinterpret_cast<const float4*>(mrow + a.shift_off);
+  const float4* sc = reinterpret_cast<const float4*>(mrow + a.scale_off);
+  uint4* out = reinterpret_cast<uint4*>(a.out + (size_t)r * H);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c4 = (lane + 32 * i) * 2;  // float4 index of element 8*(lane+32i)
+    const float4 s0 = __ldg(sh + c4), s1 = __ldg(sh + c4 + 1);
+    const float4 k0 = __ldg(sc + c4), k1 = __ldg(sc + c4 + 1);
+    const float shv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    const float scv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+    float o[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) o[u] = (v[i][u] - mean) * rstd * (1.0f + scv[u]) + shv[u];
+    uint4 w;
+    w.x = pack_bf16x2(o[0], o[1]);
+    w.y = pack_bf16x2(o[2], o[3]);
+    w.z = pack_bf16x2(o[4], o[5]);
+    w.w = pack_bf16x2(o[6], o[7]);
+    out[lane + 32 * i] = w;
+  }
+}
+
+// ------------------------------------------------------------------ rectified-flow epilogues
+__global__ void interpolate_kernel(const int* __restrict__ img_seq, const int* __restrict__ img_target,
+                                   const float* __restrict__ t, int Ni, int C,
+                                   const float* __restrict__ z, const float* __restrict__ eps,
+                                   float* __restrict__ zt, bf16* __restrict__ zt_bf16) {
+  const long long n4 = (long long)Ni * C / 4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(i * 4 / C);
+    const float4 a = reinterpret_cast<const float4*>(z)[i];
+    float4 o = a;
+    if (__ldg(img_target + r)) {
+      const float tt = __ldg(t + __ldg(img_seq + r));
+      const float4 e = reinterpret_cast<const float4*>(eps)[i];
+      const float u = 1.0f - tt;
+      o = make_float4(u * a.x + tt * e.x, u * a.y + tt * e.y, u * a.z + tt * e.z, u * a.w + tt * e.w);
+    }
+    if (zt) reinterpret_cast<float4*>(zt)[i] = o;
+    if (zt_bf16) {
+      uint2 w;
+      w.x = pack_bf16x2(o.x, o.y);
+      w.y = pack_bf16x2(o.z, o.w);
+      reinterpret_cast<uint2*>(zt_bf16)[i] = w;
+    }
+  }
+}
+
+// Each conditional row writes the guided velocity to itself and to its unconditional partner,
+// so in-place use is race-free (unconditional rows are only written by their partner).
+__global__ void cfg_kernel(const int* __restrict__ img_seq, const int* __restrict__ seq_role,
+                           const int* __restrict__ img_pair, int Ni, int C, float w,
+                           const float* v, float* out) {
+  const long long n4 = (long long)Ni * C / 4;
+  const int c4n = C / 4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(i / c4n);
+    const int c4 = (int)(i - (long long)r * c4n);
+    const int role = __ldg(seq_role + __ldg(img_seq + r));
+    if (role == 0) {
+      if (out != v) reinterpret_cast<float4*>(out)[i] = reinterpret_cast<const float4*>(v)[i];
+    } else if (role == 1) {
+      const int u = __ldg(img_pair + r);
+      const long long j = (long long)u * c4n + c4;
+      const float4 vc = reinterpret_cast<const float4*>(v)[i];
+      const float4 vu = reinterpret_cast<const float4*>(v)[j];
+      const float4 g = make_float4(vu.x + w * (vc.x - vu.x), vu.y + w * (vc.y - vu.y),
+                                   vu.z + w * (vc.z - vu.z), vu.w + w * (vc.w - vu.w));
+      reinterpret_cast<float4*>(out)[i] = g;
+      reinterpret_cast<float4*>(out)[j] = g;
+    }
+  }
+}
+
+__global__ void euler_kernel(long long n4, float dt, const float* __restrict__ v, float* z,
+                             bf16* __restrict__ z_bf16) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(v)[i];
+    float4 b = reinterpret_cast<float4*>(z)[i];
+    b.x = fmaf(dt, a.x, b.x);
+    b.y = fmaf(dt, a.y, b.y);
+    b.z = fmaf(dt, a.z, b.z);
+    b.w = fmaf(dt, a.w, b.w);
+    reinterpret_cast<float4*>(z)[i] = b;
+    if (z_bf16) {
+      uint2 w;
+      w.x = pack_bf16x2(b.x, b.y);
+      w.y = pack_bf16x2(b.z, b.w);
+      reinterpret_cast<uint2*>(z_bf16)[i] = w;
+    }
+  }
+}
+
+// per image row: sum over channels of (v - (z - eps))^2 in f64 (0 for source-frame rows)
+__global__ void loss_row_kernel(const int* __restrict__ img_target, int Ni, int C,
+                                const float* __restrict__ z, const float* __restrict__ eps,
+                                const float* __restrict__ v, double* __restrict__ ws) {
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= Ni) return;
+  double acc = 0.0;
+  if (__ldg(img_target + r)) {
+    const size_t base = (size_t)r * C;
+    for (int c = lane * 4; c < C; c += 128) {
+      const float4 a = *reinterpret_cast<const float4*>(z + base + c);
+      const float4 e = *reinterpret_cast<const float4*>(eps + base + c);
+      const float4 u = *reinterpret_cast<const float4*>(v + base + c);
+      const double d0 = (double)u.x - ((double)a.x - (double)e.x);
+      const double d1 = (double)u.y - ((double)a.y - (double)e.y);
+      const double d2 = (double)u.z - ((double)a.z - (double)e.z);
+      const double d3 = (double)u.w - ((double)a.w - (double)e.w);
+      acc += d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3;
+    }
+  }
+  acc = warp_sum_d(acc);
+  if (lane == 0) ws[r] = acc;
+}
+
+// one block per sample, fixed reduction order
+__global__ void loss_seq_kernel(const int* __restrict__ cu_img, const int* __restrict__ img_target,
+                                int C, const double* __restrict__ ws, double* __restrict__ loss_sum,
+                                long long* __restrict__ count) {
+  __shared__ double sd[256];
+  __shared__ long long sc[256];
+  const int s = blockIdx.x;
+  const int lo = cu_img[s], hi = cu_img[s + 1];
+  double a = 0.0;
+  long long n = 0;
+  for (int r = lo + threadIdx.x; r < hi; r += blockDim.x) {
+    a += ws[r];
+    n += img_target[r];
+  }
+  sd[threadIdx.x] = a;
+  sc[threadIdx.x] = n;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) {
+      sd[threadIdx.x] += sd[threadIdx.x + o];
+      sc[threadIdx.x] += sc[threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    loss_sum[s] = sd[0];
+    count[s] = sc[0] * (long long)C;
+  }
+}
+
+__global__ void loss_mean_kernel(int S, const double* __restrict__ loss_sum,
+                                 const long long* __restrict__ count, double* __restrict__ mean) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  double a = 0.0;
+  long long n = 0;
+  for (int s = 0; s < S; ++s) {
+    a += loss_sum[s];
+    n += count[s];
+  }
+  *mean = n > 0 ? a / (double)n : 0.0;
+}
+
+__global__ void timeout_selftest_kernel(unsigned* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // nobody arrives on `bar`: the bounded wait must give up and report
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, limit_ns)) report_status(status, kStatusTimeout);
+}
+
+int grid_for(long long n, int threads) {
+  long long g = (n + threads - 1) / threads;
+  if (g > 148LL * 16) g = 148LL * 16;
+  return g < 1 ? 1 : (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_sinusoid(const float* t, int S, int F, float* out, cudaStream_t st) {
+  const int n = S * (F / 2);
+  if (n <= 0) return cudaSuccess;
+  sinusoid_kernel<<<(n + 255) / 256, 256, 0, st>>>(t, S, F, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int K, int O, float* y,
+                        int y_stride, int y_off, int act, cudaStream_t st) {
+  if (S <= 0 || O <= 0) return cudaSuccess;
+  const int blocks = (O + 7) / 8;
+  if (act == 1)
+    gemv_kernel<1><<<blocks, 256, 0, st>>>(W, b, x, S, K, O, y, y_stride, y_off);
+  else
+    gemv_kernel<0><<<blocks, 256, 0, st>>>(W, b, x, S, K, O, y, y_stride, y_off);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ln_modulate(const LnModArgs& a, cudaStream_t st) {
+  if (a.rows <= 0) return cudaSuccess;
+  const int blocks = (a.rows + 7) / 8;
+  switch (a.H / 256) {
+#define MF_LN_CASE(nv) \
+  case nv: ln_modulate_kernel<nv><<<blocks, 256, 0, st>>>(a); break;
+    MF_LN_CASE(1) MF_LN_CASE(2) MF_LN_CASE(3) MF_LN_CASE(4) MF_LN_CASE(5) MF_LN_CASE(6)
+    MF_LN_CASE(7) MF_LN_CASE(8) MF_LN_CASE(9) MF_LN_CASE(10) MF_LN_CASE(11) MF_LN_CASE(12)
+    MF_LN_CASE(13) MF_LN_CASE(14) MF_LN_CASE(15) MF_LN_CASE(16)
+#undef MF_LN_CASE
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_interpolate(const int* img_seq, const int* img_target, const float* t, int Ni,
+                               int C, const float* z, const float* eps, float* zt, bf16* zt_bf16,
+                               cudaStream_t st) {
+  const long long n4 = (long long)Ni * C / 4;
+  if (n4 <= 0) return cudaSuccess;
+  interpolate_kernel<<<grid_for(n4, 256), 256, 0, st>>>(img_seq, img_target, t, Ni, C, z, eps, zt,
+                                                        zt_bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cfg(const int* img_seq, const int* seq_role, const int* img_pair, int Ni, int C,
+                       float w, const float* v, float* out, cudaStream_t st) {
+  const long long n4 = (long long)Ni * C / 4;
+  if (n4 <= 0) return cudaSuccess;
+  cfg_kernel<<<grid_for(n4, 256), 256, 0, st>>>(img_seq, seq_role, img_pair, Ni, C, w, v, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_euler(int Ni, int C, float dt, const float* v, float* z, bf16* z_bf16,
+                         cudaStream_t st) {
+  const long long n4 = (long long)Ni * C / 4;
+  if (n4 <= 0) return cudaSuccess;
+  euler_kernel<<<grid_for(n4, 256), 256, 0, st>>>(n4, dt, v, z, z_bf16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flow_loss(const int* cu_img, const int* img_target, int S, int Ni, int C,
+                             const float* z, const float* eps, const float* v, double* ws,
+                             double* loss_sum, long long* count, double* mean, cudaStream_t st) {
+  if (Ni > 0) loss_row_kernel<<<(Ni + 7) / 8, 256, 0, st>>>(img_target, Ni, C, z, eps, v, ws);
+  if (S > 0) loss_seq_kernel<<<S, 256, 0, st>>>(cu_img, img_target, C, ws, loss_sum, count);
+  loss_mean_kernel<<<1, 32, 0, st>>>(S, loss_sum, count, mean);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_timeout_selftest(unsigned* status, unsigned long long limit_ns, cudaStream_t st) {
+  timeout_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace mf

@@ -1,0 +1,50 @@
+// Row-wise and element-wise kernels of the NR-MMDiT path (memory-bound work).
+#pragma once
+
+#include "common.cuh"
+
+namespace mf {
+
+// phi(t) = [cos a | sin a], a_j = 1000 t 10000^(-j / (F/2)); out [S][F] f32.
+cudaError_t launch_sinusoid(const float* t, int S, int F, float* out, cudaStream_t st);
+
+// y[s][y_off + o] = act(W[o] . x[s] + b[o]) for o < O, W bf16 [O][K], x f32 [S][K];
+// act 0 = identity, 1 = SiLU.  K multiple of 256.
+cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int K, int O,
+                        float* y, int y_stride, int y_off, int act, cudaStream_t st);
+
+// out[r] = LN(x[r]) (1 + scale) + shift for stream-sorted rows r in [0, rows), where rows
+// below n_first come from x_first and the rest from x_second; (shift, scale) of row r are
+// read at mod + seq(r) * seq_stride + stream(r) * stream_stride + {shift_off, scale_off},
+// seq(r) = row_seq[r], stream(r) = (r >= n_first).  H multiple of 256, <= 4096.
+struct LnModArgs {
+  const bf16* x_first;
+  const bf16* x_second;
+  int n_first;
+  int rows;
+  int H;
+  const int* row_seq;
+  const float* mod;
+  long long seq_stride;
+  long long stream_stride;
+  int shift_off;
+  int scale_off;
+  bf16* out;
+};
+cudaError_t launch_ln_modulate(const LnModArgs& a, cudaStream_t st);
+
+cudaError_t launch_interpolate(const int* img_seq, const int* img_target, const float* t, int Ni,
+                               int C, const float* z, const float* eps, float* zt,
+                               bf16* zt_bf16, cudaStream_t st);
+cudaError_t launch_cfg(const int* img_seq, const int* seq_role, const int* img_pair, int Ni, int C,
+                       float w, const float* v, float* out, cudaStream_t st);
+cudaError_t launch_euler(int Ni, int C, float dt, const float* v, float* z, bf16* z_bf16,
+                         cudaStream_t st);
+// ws: [Ni] doubles
+cudaError_t launch_flow_loss(const int* cu_img, const int* img_target, int S, int Ni, int C,
+                             const float* z, const float* eps, const float* v, double* ws,
+                             double* loss_sum, long long* count, double* mean, cudaStream_t st);
+cudaError_t launch_timeout_selftest(unsigned* status, unsigned long long limit_ns,
+                                    cudaStream_t st);
+
+}  // namespace mf

@@ -1,0 +1,169 @@
+"""GPU parity of the library's building blocks through the C ABI: the bounded-wait status
+path, the tcgen05 GEMM, varlen attention and the rectified-flow epilogues, each against the
+oracle (or, for the plain GEMM, an fp64 matmul of the same bf16 operands)."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import model as M
+from oracle import pack as opack
+from tests.helpers import assert_close, stats
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import packed_rectified_flow_packer_b300 as mf
+    from packed_rectified_flow_packer_b300.device import to_bf16, to_f32
+
+
+def _bf16_np(t):
+    return t.float().cpu().numpy()
+
+
+def test_bounded_wait_reports_timeout():
+    """A wait that nothing completes gives up after its limit and reports a status; the
+    context stays usable afterwards."""
+    st = mf.mf_selftest_timeout(2000)
+    assert mf.STATUS[st] == "MF_ERR_DEVICE_TIMEOUT"
+    mf.mf_check()                                  # status word is clean again
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum()) == 8.0
+
+
+GEMM_SHAPES = [(1, 64, 64), (100, 128, 64), (128, 256, 128), (129, 384, 256), (300, 512, 1024),
+               (1000, 96, 192), (257, 256, 3072)]
+
+
+@pytest.mark.parametrize("M_,N_,K_", GEMM_SHAPES)
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_gemm(M_, N_, K_, out_f32):
+    g = np.random.default_rng(M_ * 7 + N_ + K_)
+    a = synth.round_bf16(g.standard_normal((M_, K_)).astype(np.float32))
+    b = synth.round_bf16((g.standard_normal((N_, K_)) * 0.05).astype(np.float32))
+    bias = synth.round_bf16(g.standard_normal(N_).astype(np.float32))
+    ref = a.astype(np.float64) @ b.astype(np.float64).T + bias
+    A, Bm, bb = to_bf16(a), to_bf16(b), to_bf16(bias)
+    c = torch.zeros((M_, N_), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    mf.mf_gemm(A, Bm, c, bias=bb, out_f32=out_f32)
+    mf.mf_check()
+    got = c.float().cpu().numpy()
+    s = stats(got, ref)
+    assert s["rel"] <= (1e-4 if out_f32 else 8e-3) and s["cos"] >= 0.99999, s
+
+
+def _attn_plan(samples):
+    ref = opack.build_plan(samples, sum(s.length for s in samples))
+    plan = mf.mf_pack(samples, sum(s.length for s in samples))
+    mf.mf_plan_upload(plan)
+    return ref, plan
+
+
+ATTN_SAMPLES = [synth.Sample(3, 1, 1, 2, 0.5), synth.Sample(0, 1, 1, 1, 0.5),
+                synth.Sample(27, 1, 10, 10, 0.5), synth.Sample(28, 1, 10, 10, 0.5),
+                synth.Sample(29, 1, 10, 10, 0.5), synth.Sample(44, 1, 16, 16, 0.5),
+                synth.Sample(100, 2, 16, 16, 0.5)]
+
+
+@pytest.mark.parametrize("heads,D", [(2, 128), (4, 64)])
+@pytest.mark.parametrize("growth", [0.0, 6.0])
+def test_attention_ragged(heads, D, growth):
+    """Ragged samples (1 .. 612 tokens, tile tails on both sides of 128).  `growth` scales the
+    keys up along each sample so later key tiles raise the running max by large steps (the
+    rescaling path)."""
+    ref, plan = _attn_plan(ATTN_SAMPLES)
+    N, H = ref.n_tok, heads * D
+    g = np.random.default_rng(heads + int(growth))
+    q = synth.round_bf16(g.standard_normal((N, H)).astype(np.float32))
+    k = g.standard_normal((N, H)).astype(np.float32)
+    if growth:
+        for s in range(ref.n_seq):
+            a, b = ref.cu_seqlens[s], ref.cu_seqlens[s + 1]
+            k[a:b] *= (1.0 + growth * np.arange(b - a) / max(1, b - a))[:, None]
+    k = synth.round_bf16(k)
+    v = synth.round_bf16(g.standard_normal((N, H)).astype(np.float32))
+    o = torch.zeros((N, H), dtype=torch.bfloat16, device="cuda")
+    mf.mf_attention(plan, heads, D, to_bf16(q), to_bf16(k), to_bf16(v), o)
+    mf.mf_check()
+    got = _bf16_np(o)
+    # oracle, one sample at a time, mapped to stream-sorted rows
+    want = np.zeros((N, H))
+    srow_of_joint = np.empty(N, np.int64)
+    srow_of_joint[ref.txt_joint] = np.arange(ref.n_txt)
+    srow_of_joint[ref.img_joint] = ref.n_txt + np.arange(ref.n_img)
+    for s in range(ref.n_seq):
+        a, b = ref.cu_seqlens[s], ref.cu_seqlens[s + 1]
+        os_ = M.attention(q[a:b].reshape(-1, heads, D), k[a:b].reshape(-1, heads, D),
+                          v[a:b].reshape(-1, heads, D)).reshape(-1, H)
+        want[srow_of_joint[a:b]] = os_
+    for s in range(ref.n_seq):
+        a, b = ref.cu_seqlens[s], ref.cu_seqlens[s + 1]
+        rows = srow_of_joint[a:b]
+        assert_close(got[rows], want[rows], f"attention sample {s} (len {b - a})")
+
+
+def _latent_case():
+    samples = [synth.Sample(5, 1, 3, 4, 0.3, 1, 1), synth.Sample(0, 1, 3, 4, 0.3, 2, 0),
+               synth.Sample(7, 2, 2, 5, 0.8), synth.Sample(2, 1, 6, 1, 0.55)]
+    budget = sum(s.length for s in samples)
+    ref = opack.build_plan(samples, budget)
+    plan = mf.mf_pack(samples, budget)
+    mf.mf_plan_upload(plan)
+    return samples, ref, plan
+
+
+@pytest.mark.parametrize("C", [64, 128])
+def test_rectified_flow_epilogues(C):
+    samples, ref, plan = _latent_case()
+    Ni = ref.n_img
+    g = np.random.default_rng(C)
+    z, e, v = (g.standard_normal((Ni, C)).astype(np.float32) for _ in range(3))
+    Z, E, V = to_f32(z), to_f32(e), to_f32(v)
+    # interpolation (edit source rows stay clean)
+    zt = torch.zeros((Ni, C), device="cuda")
+    ztb = torch.zeros((Ni, C), dtype=torch.bfloat16, device="cuda")
+    mf.mf_interpolate(plan, C, None, Z, E, zt, ztb)
+    # Euler step in place
+    zz = Z.clone()
+    mf.mf_euler_step(plan, C, 0.25, V, zz)
+    # packed CFG
+    vo = torch.zeros((Ni, C), device="cuda")
+    mf.mf_cfg_combine(plan, C, 4.0, V, vo)
+    vin = V.clone()
+    mf.mf_cfg_combine(plan, C, 4.0, vin, vin)     # in place
+    # loss
+    ls = torch.zeros(ref.n_seq, dtype=torch.float64, device="cuda")
+    cnt = torch.zeros(ref.n_seq, dtype=torch.int64, device="cuda")
+    mean = torch.zeros(1, dtype=torch.float64, device="cuda")
+    ws = torch.empty(mf.mf_flow_loss_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
+    mf.mf_flow_loss(plan, C, Z, E, V, ls, cnt, mean, ws)
+    mf.mf_check()
+
+    want_zt, want_cfg, sums, counts = [], np.array(v, np.float64), [], []
+    for k, cidx in enumerate(ref.order):
+        s = samples[cidx]
+        a, b = ref.cu_img[k], ref.cu_img[k + 1]
+        tgt = M.target_mask(s)
+        want_zt.append(M.interpolate(z[a:b], e[a:b], np.float32(s.t), tgt))
+        sm, n = M.flow_loss(v[a:b], z[a:b], e[a:b], tgt)
+        sums.append(sm)
+        counts.append(n)
+        if s.cfg_role == 1:
+            pk = list(ref.order).index(s.cfg_pair)
+            pa, pb = ref.cu_img[pk], ref.cu_img[pk + 1]
+            gv = M.cfg_combine(v[a:b], v[pa:pb], 4.0)
+            want_cfg[a:b] = gv
+            want_cfg[pa:pb] = gv
+    np.testing.assert_allclose(zt.cpu().numpy(), np.concatenate(want_zt), rtol=1e-6, atol=1e-6)
+    np.testing.assert_array_equal(ztb.float().cpu().numpy(),
+                                  synth.round_bf16(zt.cpu().numpy()))
+    np.testing.assert_allclose(zz.cpu().numpy(), M.euler_step(z, v, 0.25), rtol=1e-6, atol=1e-6)
+    np.testing.assert_allclose(vo.cpu().numpy(), want_cfg, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(vin.cpu().numpy(), want_cfg, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(ls.cpu().numpy(), sums, rtol=1e-12)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), counts)
+    assert abs(mean.item() - M.mean_loss(sums, counts)) <= 1e-12 * abs(M.mean_loss(sums, counts))
+    # deterministic: a second run gives the same bits
+    ls2 = torch.zeros_like(ls)
+    mf.mf_flow_loss(plan, C, Z, E, V, ls2, cnt, mean, ws)
+    assert torch.equal(ls, ls2)

@@ -1,0 +1,219 @@
+"""GPU parity of the packed block forward and the stack paths through the C ABI, against the
+fp64 oracle run one sample at a time (so every check is also a packed == unpacked check)."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import model as M
+from oracle import pack as opack
+from tests.helpers import assert_close, oracle_stack, stream_concat
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import packed_rectified_flow_packer_b300 as mf
+    from packed_rectified_flow_packer_b300.device import (DeviceModel, Workspace, run_stack, to_bf16,
+                                                          to_f32)
+
+
+def _f(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+class Case:
+    def __init__(self, samples, dims, n_blocks, seed, budget=None):
+        self.samples, self.dims = samples, dims
+        self.budget = budget or sum(s.length for s in samples)
+        self.w = synth.model_weights(dims, n_blocks, seed)
+        self.batch = synth.batch_inputs(samples, dims, seed)
+        self.ref = opack.build_plan(samples, self.budget)
+        self.plan = mf.mf_pack(samples, self.budget)
+        mf.mf_plan_upload(self.plan)
+        self.model = DeviceModel(self.w)
+        self.ws = Workspace(self.plan, self.model.dims)
+        H, C = dims.hidden, dims.channels
+        self.x_txt_np = stream_concat(self.batch.x_txt, self.ref.order, H)
+        self.z_np = stream_concat(self.batch.z, self.ref.order, C)
+        self.eps_np = stream_concat(self.batch.eps, self.ref.order, C)
+        self.t_np = np.array([samples[c].t for c in self.ref.order], np.float32)
+
+
+def _block_intermediates(case, x_txt, x_img, k):
+    """Oracle intermediates of block 0 for packed sample k (joint order inside the sample)."""
+    s = case.samples[case.ref.order[k]]
+    d, bw = case.dims, case.w.blocks[0]
+    H, nh = d.hidden, d.heads
+    c = M.condition(s.t, case.w.temb, d.freq_dim)
+    mods = {st: M.modulation(c, bw[st]["w_mod"], bw[st]["b_mod"], 6) for st in M.STREAMS}
+    xt = x_txt[case.ref.cu_txt[k]:case.ref.cu_txt[k + 1]]
+    xi = x_img[case.ref.cu_img[k]:case.ref.cu_img[k + 1]]
+    a = {"txt": M.modulate(xt, mods["txt"][0], mods["txt"][1]),
+         "img": M.modulate(xi, mods["img"][0], mods["img"][1])}
+    qkv = np.concatenate([M.linear(a[st], bw[st]["w_qkv"], bw[st]["b_qkv"]) for st in M.STREAMS])
+    L = len(qkv)
+    pos = np.concatenate([np.zeros((len(xt), 3), np.int64), M.image_positions(s.frames, s.lat_h, s.lat_w)])
+    q = M.apply_rope(qkv[:, :H].reshape(L, nh, -1), pos).reshape(L, H)
+    kk = M.apply_rope(qkv[:, H:2 * H].reshape(L, nh, -1), pos).reshape(L, H)
+    v = qkv[:, 2 * H:]
+    o = M.attention(q.reshape(L, nh, -1), kk.reshape(L, nh, -1), v.reshape(L, nh, -1)).reshape(L, H)
+    return {"c": c, "mod_txt": np.concatenate(mods["txt"]), "mod_img": np.concatenate(mods["img"]),
+            "q": q, "k": kk, "v": v, "o": o}
+
+
+def test_tiny_block_and_intermediates():
+    """The tiny configuration (H=256, 4 heads x 64, two samples 16+8x8 and 16+4x12): the
+    block alone on the GPU's own embed output, and every intermediate the call leaves."""
+    d = synth.TINY
+    case = Case(synth.tiny_samples(), d, 1, seed=0)
+    ref, H, C = case.ref, d.hidden, d.channels
+    x_txt = to_bf16(case.x_txt_np)
+    x_img = torch.empty((ref.n_img, H), dtype=torch.bfloat16, device="cuda")
+    mf.mf_embed(case.plan, case.model.dims, case.model.embed["w_in"], case.model.embed["b_in"],
+                to_bf16(case.z_np), x_img)
+    mf.mf_check()
+    emb = _f(x_img)
+    assert_close(emb, M.embed(case.z_np, case.w.embed), "embed")
+    x_txt0 = _f(x_txt)
+    mf.mf_block_forward(case.plan, case.model.dims, case.model.block_structs[0], None, x_txt, x_img,
+                        case.ws.block)
+    mf.mf_check()
+    # intermediates left in the workspace
+    off = mf.mf_block_workspace_layout(case.plan, case.model.dims)
+    wsb = case.ws.block
+    S, N = ref.n_seq, ref.n_tok
+    view = lambda i, n, dt: wsb[off[i]:off[i] + n * (4 if dt == torch.float32 else 2)].view(dt)  # noqa: E731
+    cgpu = view(0, S * H, torch.float32).cpu().numpy().reshape(S, H)
+    modg = view(1, S * 12 * H, torch.float32).cpu().numpy().reshape(S, 2, 6 * H)
+    qg = _f(view(3, N * H, torch.bfloat16).reshape(N, H))
+    kg = _f(view(4, N * H, torch.bfloat16).reshape(N, H))
+    vg = _f(view(5, N * H, torch.bfloat16).reshape(N, H))
+    og = _f(view(6, N * H, torch.bfloat16).reshape(N, H))
+    for k in range(S):
+        it = _block_intermediates(case, x_txt0, emb, k)
+        a, b = ref.cu_seqlens[k], ref.cu_seqlens[k + 1]
+        assert_close(cgpu[k], it["c"], f"c[{k}]")
+        assert_close(modg[k, 0], it["mod_txt"], f"mod_txt[{k}]")
+        assert_close(modg[k, 1], it["mod_img"], f"mod_img[{k}]")
+        assert_close(qg[a:b], it["q"], f"q[{k}]")
+        assert_close(kg[a:b], it["k"], f"k[{k}]")
+        assert_close(vg[a:b], it["v"], f"v[{k}]")
+        rows = np.concatenate([np.arange(ref.cu_txt[k], ref.cu_txt[k + 1]),
+                               ref.n_txt + np.arange(ref.cu_img[k], ref.cu_img[k + 1])])
+        assert_close(og[rows], it["o"], f"o[{k}]")
+    # the block output vs the oracle on the same inputs; also on the update (out - in)
+    xt_ref, xi_ref, _ = oracle_stack(case.samples, ref, case.w, case.batch, d.heads,
+                                     x_img_in=emb, n_blocks=1)
+    got_t, got_i = _f(x_txt), _f(x_img)
+    assert_close(got_t, xt_ref, "block x_txt")
+    assert_close(got_i, xi_ref, "block x_img")
+    assert_close(got_t - x_txt0, xt_ref - x_txt0, "block delta txt", rel=3e-2, cos=0.999)
+    assert_close(got_i - emb, xi_ref - emb, "block delta img", rel=3e-2, cos=0.999)
+
+
+def _stack_and_loss(case, n_blocks):
+    d, ref = case.dims, case.ref
+    H, C = d.hidden, d.channels
+    Z, E = to_f32(case.z_np), to_f32(case.eps_np)
+    ztb = torch.empty((ref.n_img, C), dtype=torch.bfloat16, device="cuda")
+    mf.mf_interpolate(case.plan, C, None, Z, E, None, ztb)
+    x_txt = to_bf16(case.x_txt_np)
+    x_img = torch.empty((ref.n_img, H), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((ref.n_img, C), dtype=torch.float32, device="cuda")
+    run_stack(case.plan, case.model, x_txt, ztb, x_img, v, case.ws, n_blocks=n_blocks)
+    ls = torch.zeros(ref.n_seq, dtype=torch.float64, device="cuda")
+    cnt = torch.zeros(ref.n_seq, dtype=torch.int64, device="cuda")
+    mean = torch.zeros(1, dtype=torch.float64, device="cuda")
+    mf.mf_flow_loss(case.plan, C, Z, E, v, ls, cnt, mean, case.ws.loss)
+    mf.mf_check()
+    # oracle: interpolate (source frames clean), then the stack, one sample at a time
+    zt = []
+    for k, c in enumerate(ref.order):
+        s = case.samples[c]
+        a, b = ref.cu_img[k], ref.cu_img[k + 1]
+        zt.append(M.interpolate(case.z_np[a:b], case.eps_np[a:b], np.float32(s.t), M.target_mask(s)))
+    zt = np.concatenate(zt)
+    _, _, v_ref = oracle_stack(case.samples, ref, case.w, case.batch, d.heads, zt=synth.round_bf16(
+        zt.astype(np.float32)), n_blocks=n_blocks)
+    vg = v.cpu().numpy()
+    assert_close(vg, v_ref, "velocity v")
+    sums = [M.flow_loss(v_ref[ref.cu_img[k]:ref.cu_img[k + 1]], case.z_np[ref.cu_img[k]:ref.cu_img[k + 1]],
+                        case.eps_np[ref.cu_img[k]:ref.cu_img[k + 1]],
+                        M.target_mask(case.samples[c]))[0] for k, c in enumerate(ref.order)]
+    assert_close(ls.cpu().numpy(), sums, "loss sums", rel=2e-2)
+    return vg, v_ref
+
+
+def test_tiny_stack_with_loss():
+    case = Case(synth.tiny_samples(), synth.TINY, 1, seed=1)
+    _stack_and_loss(case, 1)
+
+
+MID = synth.Dims(hidden=512, heads=4, channels=128)
+
+
+def _mid_samples(seed, n=6):
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        out.append(synth.Sample(int(g.integers(0, 140)), 1, int(g.integers(2, 24)), int(g.integers(2, 24)),
+                                float(g.uniform())))
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_mid_pack_block(seed):
+    """A ragged pack at H=512 (4 heads x 128): several GEMM row tiles with tails, samples that
+    span several attention tiles, text lengths from 0 up."""
+    samples = _mid_samples(seed)
+    case = Case(samples, MID, 1, seed=seed + 10)
+    _stack_and_loss(case, 1)
+
+
+def test_mid_edit_stack():
+    """Editing structure at H=512: 2 frames (clean source, noisy target), 3-axis RoPE, loss on
+    target frames only, 2 blocks."""
+    samples = [synth.Sample(40, 2, 8, 12, 0.37), synth.Sample(77, 2, 10, 10, 0.81)]
+    case = Case(samples, MID, 2, seed=5)
+    _stack_and_loss(case, 2)
+
+
+def test_mid_cfg_sampler():
+    """Packed CFG sampler at H=512: cond + uncond branches of two prompts in one pack, 2 blocks,
+    4 Euler steps from t=1 with w=4, against separate (unpacked) cond / uncond oracle runs."""
+    d = MID
+    samples = [synth.Sample(20, 1, 8, 8, 1.0, 1, 1), synth.Sample(0, 1, 8, 8, 1.0, 2, 0),
+               synth.Sample(20, 1, 6, 11, 1.0, 1, 3), synth.Sample(0, 1, 6, 11, 1.0, 2, 2)]
+    budget = sum(s.length for s in samples)
+    w = synth.model_weights(d, 2, 7)
+    batch = synth.cfg_batch(samples, d, 7)
+    ref = opack.build_plan(samples, budget)
+    plan = mf.mf_pack(samples, budget)
+    mf.mf_plan_upload(plan)
+    model = DeviceModel(w)
+    ws = Workspace(plan, model.dims)
+    H, C = d.hidden, d.channels
+    grid = [1.0, 0.75, 0.5, 0.25, 0.0]
+    z = to_f32(stream_concat(batch.z, ref.order, C))
+    zb = z.to(torch.bfloat16)
+    x_txt0 = to_bf16(stream_concat(batch.x_txt, ref.order, H))
+    x_img = torch.empty((ref.n_img, H), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((ref.n_img, C), dtype=torch.float32, device="cuda")
+    tt = torch.empty(ref.n_seq, dtype=torch.float32, device="cuda")
+    for a, b in zip(grid[:-1], grid[1:]):
+        tt.fill_(a)
+        x_txt = x_txt0.clone()
+        run_stack(plan, model, x_txt, zb, x_img, v, ws, t=tt)
+        mf.mf_cfg_combine(plan, C, 4.0, v, v)
+        mf.mf_euler_step(plan, C, a - b, v, z, zb)
+    mf.mf_check()
+    zg = z.cpu().numpy()
+    for k, c in enumerate(ref.order):
+        s = samples[c]
+        if s.cfg_role != 1:
+            continue
+        zref = M.sample_cfg(batch.x_txt[c], batch.z[c], s, samples[s.cfg_pair], w, d.heads, 4.0, grid)
+        a, b = ref.cu_img[k], ref.cu_img[k + 1]
+        assert_close(zg[a:b], zref, f"cfg sample {c}")
+        pk = list(ref.order).index(s.cfg_pair)
+        np.testing.assert_array_equal(zg[a:b], zg[ref.cu_img[pk]:ref.cu_img[pk + 1]])
