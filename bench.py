@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Throughput of the packed NR-MMDiT hot path on B300: packed tokens/s per block forward.
+
+Workload (default): the native-resolution pack - eight seeded packs of up to 16384 tokens
+(candidates with H, W uniform over multiples of 16 in [512, 2048], 32-512 text tokens,
+logit-normal t, first-fit), one NR-MMDiT block (H=3072, 24 heads x 128, MLP 4x, bf16 weights
+N(0, 0.02)).  One step = one pack through the whole path: z_t interpolation, latent embed,
+the block (conditioning, LN+modulate, QKV+RoPE, varlen attention, out-proj+gate, LN+modulate,
+MLP+GELU, MLP+gate), the final layer and the flow-matching loss.  Step k uses pack k mod 8.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {mageflow,reference}]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on bounded samples of
+the same workload.  Multi-GPU: one process per GPU (torchrun), each rank its own packs (weak
+scaling); the only collectives are the timing barrier and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "packed tokens/s per NR-MMDiT block fwd (1×B300) and % of bf16 tensor peak"
+BUDGET = 16384
+N_PACKS = 8
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=240)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mageflow", "reference"], default="mageflow")
+    ap.add_argument("--e2e-steps", type=int, default=16)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def config_dict(dims):
+    return {"workload": "native-resolution pack, 16384-token budget, 8 seeded packs (first-fit over 64 "
+                        "candidates each), 1 NR-MMDiT block + latent embed/final layer + flow loss",
+            "budget": BUDGET, "packs": N_PACKS, "hidden": dims.hidden, "heads": dims.heads,
+            "head_dim": dims.head_dim, "mlp_ratio": dims.mlp_ratio, "latent_channels": dims.channels,
+            "l2": "working set > L2 (0.68 GB block weights + ~1.1 GB activations per step); no flush"}
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d["bf16_tflops_sustained"], "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample(dims, weights, cands, order, n_tokens):
+    """A bounded sample of the workload for the CPU oracle: the first packed sample of a pack,
+    cut to its text plus its first image rows so that it holds about n_tokens tokens."""
+    s = cands[order[0]]
+    rows = max(1, min(s.lat_h, (n_tokens - s.txt_len) // s.lat_w))
+    sub = synth.Sample(s.txt_len, 1, rows, s.lat_w, s.t)
+    x = synth.round_bf16(synth.normal(0, "cpu.x_txt", (sub.txt_len, dims.hidden)))
+    z = synth.round_bf16(synth.normal(0, "cpu.z", (sub.img_len, dims.channels)))
+    return sub, x, z
+
+
+def time_oracle(dims, weights, sub, x, z, budget_s):
+    from oracle import model as M
+    n, t0 = 0, time.perf_counter()
+    while True:
+        M.forward(x, z, sub, sub.t, weights, dims.heads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 50:
+            return n * sub.length / el, el, n
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            return max(int(i.get("num_threads", 1)) for i in info)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline(dims, weights, cands, order, seconds):
+    sub, x, z = oracle_sample(dims, weights, cands, order, 2048)
+    tps, el, n = time_oracle(dims, weights, sub, x, z, seconds)
+    return {"value": tps, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"fp64 NumPy oracle: embed + 1 block + final layer on one sample of pack 0 cut to "
+                      f"{sub.txt_len} text + {sub.lat_h}x{sub.lat_w} image tokens ({sub.length} tokens), "
+                      f"{n} runs in {el:.1f} s"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_id)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the GPU arm
+def run_mageflow(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import packed_rectified_flow_packer_b300 as mf
+    from packed_rectified_flow_packer_b300.device import DeviceModel, to_bf16, to_f32
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    dims = synth.FULL
+    H, C = dims.hidden, dims.channels
+    weights = synth.model_weights(dims, 1, seed=0)
+    model = DeviceModel(weights, device=dev)
+    d = model.dims
+
+    packs = []
+    for i in range(N_PACKS):
+        seed = rank * N_PACKS + i
+        cands = synth.native_candidates(seed)
+        plan = mf.mf_pack(cands, BUDGET)
+        mf.mf_plan_upload(plan)
+        x, z, e = synth.pack_inputs(cands, plan.array("order"), dims, seed)
+        packs.append({"seed": seed, "cands": cands, "plan": plan, "n_tok": plan.n_tok, "n_img": plan.n_img,
+                      "n_seq": plan.n_seq, "x_txt": to_bf16(x, dev), "z": to_f32(z, dev), "eps": to_f32(e, dev),
+                      "x_np": x, "z_np": z, "e_np": e})
+    wsb = max(mf.mf_block_workspace_bytes(p["plan"], d) for p in packs)
+    wsf = max(mf.mf_final_workspace_bytes(p["plan"], d) for p in packs)
+    wsl = max(mf.mf_flow_loss_workspace_bytes(p["plan"]) for p in packs)
+    ws_block = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ws_final = torch.empty(wsf, dtype=torch.uint8, device=dev)
+    ws_loss = torch.empty(wsl, dtype=torch.uint8, device=dev)
+    x_txt = torch.empty((BUDGET, H), dtype=torch.bfloat16, device=dev)
+    x_img = torch.empty((BUDGET, H), dtype=torch.bfloat16, device=dev)
+    ztb = torch.empty((BUDGET, C), dtype=torch.bfloat16, device=dev)
+    v = torch.empty((BUDGET, C), dtype=torch.float32, device=dev)
+    ls = torch.zeros(64, dtype=torch.float64, device=dev)
+    cnt = torch.zeros(64, dtype=torch.int64, device=dev)
+    mean = torch.zeros(1, dtype=torch.float64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    emb, fin, blk = model.embed, model.final, model.block_structs[0]
+
+    def device_step(p, timed_block=None):
+        plan = p["plan"]
+        nt = p["x_txt"].shape[0]
+        x_txt[:nt].copy_(p["x_txt"])
+        mf.mf_interpolate(plan, C, None, p["z"], p["eps"], None, ztb)
+        mf.mf_embed(plan, d, emb["w_in"], emb["b_in"], ztb, x_img)
+        if timed_block is not None:
+            timed_block[0].record(stream)
+        mf.mf_block_forward(plan, d, blk, None, x_txt, x_img, ws_block)
+        if timed_block is not None:
+            timed_block[1].record(stream)
+        mf.mf_final(plan, d, model.temb_struct, fin["w_fmod"], fin["b_fmod"], fin["w_out"], fin["b_out"],
+                    None, x_img, v, ws_final)
+        mf.mf_flow_loss(plan, C, p["z"], p["eps"], v, ls, cnt, mean, ws_loss)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        device_step(packs[i % N_PACKS])
+    mf.mf_check()
+    barrier()
+
+    # ---- timed region: K steps, device-resident inputs
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    sampler = ClockSampler(("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or local_rank)
+    time.sleep(0.3)
+    mf.mf_trace_enable(True)
+    l0 = mf.mf_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(stream)
+    tokens = 0
+    for i in range(args.steps):
+        p = packs[i % N_PACKS]
+        device_step(p)
+        tokens += p["n_tok"]
+    ev1.record(stream)
+    barrier()
+    launches = mf.mf_launch_count() - l0
+    trace = mf.mf_trace_read()
+    mf.mf_trace_enable(False)
+    clocks = sampler.stop()
+    mf.mf_check()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+        n = torch.tensor([tokens], dtype=torch.float64, device=dev)
+        dist.all_reduce(n)
+        tokens = int(n.item())
+
+    # ---- block-only timing (untraced): events around each block call
+    block_ms, block_tok = 0.0, 0
+    pairs = []
+    for i in range(min(args.steps, 4 * N_PACKS)):
+        p = packs[i % N_PACKS]
+        pr = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        device_step(p, pr)
+        pairs.append((pr, p))
+    torch.cuda.synchronize(dev)
+    block_flops = 0.0
+    for (a, b), p in pairs:
+        block_ms += a.elapsed_time(b)
+        block_tok += p["n_tok"]
+        cu = p["plan"].array("cu_seqlens").astype(np.float64)
+        block_flops += 24.0 * H * H * p["n_tok"] + 4.0 * H * float((np.diff(cu) ** 2).sum()) \
+            + 2.0 * 2 * 6.0 * H * H * p["n_seq"]
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        pinned = []
+        for p in packs:
+            pinned.append({"x": torch.from_numpy(p["x_np"]).to(torch.bfloat16).pin_memory(),
+                           "z": torch.from_numpy(p["z_np"]).pin_memory(),
+                           "e": torch.from_numpy(p["e_np"]).pin_memory()})
+        zdev = torch.empty((BUDGET, C), dtype=torch.float32, device=dev)
+        edev = torch.empty((BUDGET, C), dtype=torch.float32, device=dev)
+        host_out = torch.empty(64 * 2 + 1, dtype=torch.float64).pin_memory()
+        h2d = d2h = 0
+        e_tok = 0
+        warm = 2
+        t_start = None
+        for i in range(args.e2e_steps + warm):
+            if i == warm:
+                torch.cuda.synchronize(dev)
+                t_start = time.perf_counter()
+                h2d = d2h = e_tok = 0
+            p = packs[i % N_PACKS]
+            hp = pinned[i % N_PACKS]
+            plan = mf.mf_pack(p["cands"], BUDGET)                        # host packer
+            mf.mf_plan_upload(plan)                                      # index buffers H2D
+            nt, ni = hp["x"].shape[0], hp["z"].shape[0]
+            x_txt[:nt].copy_(hp["x"], non_blocking=True)
+            zdev[:ni].copy_(hp["z"], non_blocking=True)
+            edev[:ni].copy_(hp["e"], non_blocking=True)
+            mf.mf_interpolate(plan, C, None, zdev, edev, None, ztb)
+            mf.mf_embed(plan, d, emb["w_in"], emb["b_in"], ztb, x_img)
+            mf.mf_block_forward(plan, d, blk, None, x_txt, x_img, ws_block)
+            mf.mf_final(plan, d, model.temb_struct, fin["w_fmod"], fin["b_fmod"], fin["w_out"], fin["b_out"],
+                        None, x_img, v, ws_final)
+            mf.mf_flow_loss(plan, C, zdev, edev, v, ls, cnt, mean, ws_loss)
+            S = plan.n_seq
+            host_out[:S].copy_(ls[:S], non_blocking=True)
+            host_out[64:64 + S].copy_(cnt[:S].double(), non_blocking=True)
+            host_out[128:129].copy_(mean, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            info = plan.info()
+            plan_bytes = 4 * (2 * (S + 1) + 3 * info.n_tok + 3 * info.n_tok + 3 * info.n_img + 2 * S +
+                              2 * info.n_items)
+            h2d += (hp["x"].numel() * 2 + hp["z"].numel() * 4 + hp["e"].numel() * 4 + plan_bytes)
+            d2h += 16 * S + 8
+            e_tok += plan.n_tok
+            del plan
+        e_el = time.perf_counter() - t_start
+        e2e = {"value": e_tok / e_el, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d / args.e2e_steps),
+               "d2h_bytes_per_step": int(d2h / args.e2e_steps),
+               "includes": "host first-fit packing, plan upload, pinned H2D of text/latents/noise, "
+                           "device path, D2H of per-sample loss sums, counts and mean"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    # ---- roofline of the dominant kernel, from the traced region
+    peaks = read_peaks()
+    kernels = {}
+    for k, e in trace.items():
+        if e["launches"] == 0:
+            continue
+        row = {"launches": e["launches"], "ms_total": round(e["ms"], 3),
+               "ms_avg": round(e["ms"] / e["launches"], 4), "share": None}
+        if e["flops"] > 0 and e["ms"] > 0:
+            row["tflops"] = round(e["flops"] / (e["ms"] / 1e3) / 1e12, 1)
+        if e["bytes"] > 0 and e["ms"] > 0:
+            row["gbs"] = round(e["bytes"] / (e["ms"] / 1e3) / 1e9, 1)
+        kernels[k] = row
+    tot_ms = sum(e["ms"] for e in trace.values())
+    for k in kernels:
+        kernels[k]["share"] = round(trace[k]["ms"] / tot_ms, 4) if tot_ms else None
+    dom = max((k for k in trace if trace[k]["flops"] > 0), key=lambda k: trace[k]["ms"])
+    de = trace[dom]
+    achieved = de["flops"] / (de["ms"] / 1e3) / 1e12
+    gemm_kinds = ("gemm_qkv", "gemm_oproj", "gemm_up", "gemm_down")
+    g_fl = sum(trace[k]["flops"] for k in gemm_kinds)
+    g_ms = sum(trace[k]["ms"] for k in gemm_kinds)
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            traffic = json.load(f).get(dom)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                "peak_kind": f"sustained bf16 ({peaks['source']}); timed inside a long step",
+                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": traffic,
+                "flops_per_launch": de["flops"] / de["launches"],
+                "all_gemms_tflops": round(g_fl / (g_ms / 1e3) / 1e12, 1) if g_ms else None,
+                "attention_tflops": kernels.get("attn", {}).get("tflops")}
+    blk_tflops = block_flops / (block_ms / 1e3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(dims, weights, packs[0]["cands"], packs[0]["plan"].array("order"), args.cpu_seconds)
+    value = tokens / elapsed
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) text embeddings, latents and noise; N(0,0.02) weights)",
+            "config": config_dict(dims), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(launches), "clocks": clocks,
+            "block": {"ms_avg": round(block_ms / len(pairs), 4), "tokens_per_s": round(block_tok / (block_ms / 1e3), 1),
+                      "tflops": round(blk_tflops, 1), "frac_of_burst": round(blk_tflops / peaks["bf16_tflops"], 4),
+                      "frac_of_sustained": round(blk_tflops / peaks["bf16_tflops_sustained"], 4),
+                      "flops_note": "24 H^2 N + 4 H sum L_i^2 + modulation; diagonal attention blocks only"},
+            "kernels": kernels, "peaks": peaks}
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------------- the reference (oracle) arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    dims = synth.FULL
+    weights = synth.model_weights(dims, 1, seed=0)
+    cands = synth.native_candidates(0)
+    from oracle import pack as opack
+    order = opack.build_plan(cands, BUDGET).order
+    # size each step so that the whole run stays within about two minutes
+    sub, x, z = oracle_sample(dims, weights, cands, order, 256)
+    t0 = time.perf_counter()
+    from oracle import model as M
+    M.forward(x, z, sub, sub.t, weights, dims.heads)
+    t256 = time.perf_counter() - t0
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    n_tok = int(min(4096, max(64, 256 * per_step / max(t256, 1e-3))))
+    sub, x, z = oracle_sample(dims, weights, cands, order, n_tok)
+    for _ in range(args.warmup):
+        M.forward(x, z, sub, sub.t, weights, dims.heads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        M.forward(x, z, sub, sub.t, weights, dims.heads)
+    el = time.perf_counter() - t0
+    value = args.steps * sub.length / el
+    sample = (f"fp64 NumPy oracle: embed + 1 block + final layer on one sample of pack 0 cut to "
+              f"{sub.txt_len} text + {sub.lat_h}x{sub.lat_w} image tokens ({sub.length} tokens) per step")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(dims),
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_mageflow(args, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -305,6 +305,47 @@ mf_status mf_check(void* stream);
  * is still usable, MF_OK never.  The status word is cleared again before returning. */
 mf_status mf_selftest_timeout(int32_t limit_us, void* stream);
 
+/* ------------------------------------------------------------------------------------ */
+/* Per-kernel timing and launch counting                                                 */
+/* ------------------------------------------------------------------------------------ */
+
+/* Kinds of kernels the library launches. */
+typedef enum {
+  MF_K_COND = 0,        /* timestep features and conditioning / modulation GEMVs */
+  MF_K_LN = 1,          /* LN + adaLN-modulate prologue */
+  MF_K_GEMM_QKV = 2,    /* QKV projection + RoPE + scatter to joint order */
+  MF_K_ATTN = 3,        /* varlen joint attention */
+  MF_K_GEMM_OPROJ = 4,  /* attention output projection + gated residual */
+  MF_K_GEMM_UP = 5,     /* MLP up-projection + GELU */
+  MF_K_GEMM_DOWN = 6,   /* MLP down-projection + gated residual */
+  MF_K_GEMM_EMBED = 7,  /* latent embed C -> H */
+  MF_K_GEMM_FINAL = 8,  /* final layer H -> C */
+  MF_K_GEMM_PLAIN = 9,  /* mf_gemm */
+  MF_K_LATENT = 10,     /* interpolate, packed CFG, Euler step */
+  MF_K_LOSS = 11,       /* flow-matching loss reduction */
+  MF_K_COUNT = 12
+} mf_kernel_kind;
+
+typedef struct {
+  int64_t launches;  /* kernel launches of this kind since tracing was enabled */
+  double ms;         /* summed device time between the events around those launches */
+  double flops;      /* summed algorithmic FLOPs (dense contractions: 2 per multiply-add) */
+  double bytes;      /* summed algorithmic HBM bytes (memory-bound kinds) */
+} mf_trace_entry;
+
+/* on != 0 starts recording (clearing earlier records); on == 0 stops.  While on, every
+ * launch of the library outside stream capture is bracketed by two CUDA events recorded on
+ * its stream; this costs two event records per launch.  Host-side, not thread-safe with
+ * concurrent library calls on other threads. */
+mf_status mf_trace_enable(int32_t on);
+
+/* Waits for the recorded events, writes one entry per mf_kernel_kind (n >= MF_K_COUNT) and
+ * clears the records.  Errors: MF_ERR_INVALID_ARG, MF_ERR_CUDA. */
+mf_status mf_trace_read(mf_trace_entry* entries, int32_t n);
+
+/* Number of kernels the library has launched in this process (all kinds, tracing or not). */
+int64_t mf_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,7 +13,7 @@ import os
 
 import numpy as np
 
-__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_attention", "mf_gemm", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
+__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_attention", "mf_gemm", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmageflow.so")
 
@@ -67,6 +67,14 @@ class mf_block_weights(C.Structure):
     _fields_ = [("temb", mf_temb_weights), ("txt", mf_stream_weights), ("img", mf_stream_weights)]
 
 
+class mf_trace_entry(C.Structure):
+    _fields_ = [("launches", C.c_int64), ("ms", C.c_double), ("flops", C.c_double),
+                ("bytes", C.c_double)]
+
+
+KERNEL_KINDS = ("cond", "ln", "gemm_qkv", "attn", "gemm_oproj", "gemm_up", "gemm_down", "gemm_embed",
+                "gemm_final", "gemm_plain", "latent", "loss")
+
 _P = C.c_void_p
 _S = C.c_int   # mf_status
 _sigs = {
@@ -94,6 +102,9 @@ _sigs = {
     "mf_gemm": (_S, [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P, C.c_int32, _P]),
     "mf_check": (_S, [_P]),
     "mf_selftest_timeout": (_S, [C.c_int32, _P]),
+    "mf_trace_enable": (_S, [C.c_int32]),
+    "mf_trace_read": (_S, [C.POINTER(mf_trace_entry), C.c_int32]),
+    "mf_launch_count": (C.c_int64, []),
 }
 for _name, (_res, _args) in _sigs.items():
     _f = getattr(lib, _name)
@@ -309,3 +320,20 @@ def mf_status_str(s: int) -> str:
 
 def mf_version() -> int:
     return lib.mf_version()
+
+
+# ------------------------------------------------------------------ tracing
+def mf_trace_enable(on: bool = True):
+    _ok(lib.mf_trace_enable(1 if on else 0), "mf_trace_enable")
+
+
+def mf_trace_read() -> dict:
+    """{kind: {"launches", "ms", "flops", "bytes"}} since tracing was enabled (then cleared)."""
+    arr = (mf_trace_entry * len(KERNEL_KINDS))()
+    _ok(lib.mf_trace_read(arr, len(KERNEL_KINDS)), "mf_trace_read")
+    return {k: {"launches": e.launches, "ms": e.ms, "flops": e.flops, "bytes": e.bytes}
+            for k, e in zip(KERNEL_KINDS, arr)}
+
+
+def mf_launch_count() -> int:
+    return lib.mf_launch_count()

@@ -6,7 +6,9 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "attention.cuh"
 #include "gemm.cuh"
@@ -61,6 +63,59 @@ unsigned long long wait_limit_ns() {
   }();
   return v;
 }
+
+// ------------------------------------------------------------------ tracing
+struct TraceRec {
+  int kind;
+  cudaEvent_t a, b;
+  double flops, bytes;
+  int nk;
+};
+
+struct TraceState {
+  bool on = false;
+  std::vector<TraceRec> recs;
+  std::vector<cudaEvent_t> pool;
+};
+TraceState g_trace;
+std::mutex g_trace_mu;
+std::atomic<long long> g_launches{0};
+
+cudaEvent_t trace_event() {
+  if (!g_trace.pool.empty()) {
+    cudaEvent_t e = g_trace.pool.back();
+    g_trace.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Counts the kernels of one library launch and, while tracing is on, brackets it with events.
+class Trace {
+ public:
+  Trace(int kind, cudaStream_t st, double flops, double bytes, int nk) : st_(st) {
+    g_launches += nk;
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (!g_trace.on) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
+    rec_ = TraceRec{kind, trace_event(), trace_event(), flops, bytes, nk};
+    if (rec_.a == nullptr || rec_.b == nullptr) return;
+    active_ = cudaEventRecord(rec_.a, st) == cudaSuccess;
+  }
+  ~Trace() {
+    if (!active_) return;
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (cudaEventRecord(rec_.b, st_) == cudaSuccess) g_trace.recs.push_back(rec_);
+  }
+
+ private:
+  cudaStream_t st_;
+  TraceRec rec_{};
+  bool active_ = false;
+};
 
 // ------------------------------------------------------------------ TMA descriptors
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -194,7 +249,7 @@ struct GemmSpec {
 };
 
 mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmParams& p,
-                   const DevInfo* di, cudaStream_t st) {
+                   const DevInfo* di, cudaStream_t st, int kind) {
   p.n_prob = 0;
   p.tile_begin[0] = 0;
   int begin = 0;
@@ -222,12 +277,16 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
   if (p.n_prob == 1) p.tile_begin[2] = begin;
   p.status = di->status;
   p.wait_limit_ns = wait_limit_ns();
+  double flops = 0;
+  for (int i = 0; i < p.n_prob; ++i) flops += 2.0 * p.prob[i].M * (double)p.prob[i].N * p.prob[i].K;
+  Trace tr(kind, st, flops, 0, 1);
   return cuda_status(mf::launch_gemm(p, BN, epi, di->sms, st));
 }
 
 mf_status conditioning(const mf_plan* p, const mf_dims* d, const mf_temb_weights* tw,
                        const float* t, float* sinus, float* h1, float* c, cudaStream_t st) {
   const int S = p->S, H = d->hidden, F = d->freq_dim;
+  Trace tr(MF_K_COND, st, 2.0 * S * ((double)F * H + (double)H * H), 2.0 * ((double)F * H + (double)H * H), 3);
   MF_CUDA(mf::launch_sinusoid(t, S, F, sinus, st));
   MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(tw->w_t1), static_cast<const bf16*>(tw->b_t1),
                           sinus, S, F, H, h1, H, 0, 1, st));
@@ -375,14 +434,20 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
 
   // 1. timestep condition c = SiLU(temb(t)) and the per-sample adaLN modulation of both streams
   MF_TRY(conditioning(p, d, &w->temb, t, sinus, h1, c, st));
-  MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w->txt.w_mod), static_cast<const bf16*>(w->txt.b_mod),
-                          c, S, H, 6 * H, mod, 12 * H, 0, 0, st));
-  MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w->img.w_mod), static_cast<const bf16*>(w->img.b_mod),
-                          c, S, H, 6 * H, mod, 12 * H, 6 * H, 0, st));
+  {
+    Trace tr(MF_K_COND, st, 2.0 * 2 * S * 6.0 * H * H, 2.0 * 2 * 6.0 * H * H, 2);
+    MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w->txt.w_mod), static_cast<const bf16*>(w->txt.b_mod),
+                            c, S, H, 6 * H, mod, 12 * H, 0, 0, st));
+    MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w->img.w_mod), static_cast<const bf16*>(w->img.b_mod),
+                            c, S, H, 6 * H, mod, 12 * H, 6 * H, 0, st));
+  }
 
   // 2. a = LN(x)(1 + scale1) + shift1, stream-sorted
   mf::LnModArgs ln{xt, xi, Nt, N, H, p->d_srow_seq, mod, 12LL * H, 6LL * H, 0, H, a};
-  MF_CUDA(mf::launch_ln_modulate(ln, st));
+  {
+    Trace tr(MF_K_LN, st, 0, 4.0 * N * H, 1);
+    MF_CUDA(mf::launch_ln_modulate(ln, st));
+  }
 
   // 3. q | k | v = a W_qkv^T + b, RoPE, scattered to joint order
   mf::GemmParams gp{};
@@ -398,7 +463,7 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
   {
     GemmSpec sp[2] = {{Nt, 3 * H, H, a, w->txt.w_qkv, w->txt.b_qkv, nullptr, 0, 0, 0},
                       {Ni, 3 * H, H, a + (size_t)Nt * H, w->img.w_qkv, w->img.b_qkv, nullptr, 0, Nt, 1}};
-    MF_TRY(run_gemm(sp, 2, mf::kEpiQkvRope, 256, gp, di, st));
+    MF_TRY(run_gemm(sp, 2, mf::kEpiQkvRope, 256, gp, di, st, MF_K_GEMM_QKV));
   }
 
   // 4. joint varlen attention -> o (stream-sorted)
@@ -417,6 +482,7 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
     ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     ap.status = di->status;
     ap.wait_limit_ns = wait_limit_ns();
+    Trace tr(MF_K_ATTN, st, 4.0 * p->sum_L2 * H, 0, 1);
     MF_CUDA(mf::launch_attention(ap, D, st));
   }
 
@@ -425,19 +491,22 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
   {
     GemmSpec sp[2] = {{Nt, H, H, o, w->txt.w_o, w->txt.b_o, xt, H, 0, 0},
                       {Ni, H, H, o + (size_t)Nt * H, w->img.w_o, w->img.b_o, xi, H, Nt, 1}};
-    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid, 256, gp, di, st));
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid, 256, gp, di, st, MF_K_GEMM_OPROJ));
   }
 
   // 6. a = LN(x)(1 + scale2) + shift2
   ln.shift_off = 3 * H;
   ln.scale_off = 4 * H;
-  MF_CUDA(mf::launch_ln_modulate(ln, st));
+  {
+    Trace tr(MF_K_LN, st, 0, 4.0 * N * H, 1);
+    MF_CUDA(mf::launch_ln_modulate(ln, st));
+  }
 
   // 7. hidden = GELU(a W_1^T + b_1)
   {
     GemmSpec sp[2] = {{Nt, R, H, a, w->txt.w_1, w->txt.b_1, hid, R, 0, 0},
                       {Ni, R, H, a + (size_t)Nt * H, w->img.w_1, w->img.b_1, hid + (size_t)Nt * R, R, Nt, 1}};
-    MF_TRY(run_gemm(sp, 2, mf::kEpiGelu, 256, gp, di, st));
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGelu, 256, gp, di, st, MF_K_GEMM_UP));
   }
 
   // 8. x += gate2 (hidden W_2^T + b_2)
@@ -445,7 +514,7 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
   {
     GemmSpec sp[2] = {{Nt, H, R, hid, w->txt.w_2, w->txt.b_2, xt, H, 0, 0},
                       {Ni, H, R, hid + (size_t)Nt * R, w->img.w_2, w->img.b_2, xi, H, Nt, 1}};
-    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid, 256, gp, di, st));
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid, 256, gp, di, st, MF_K_GEMM_DOWN));
   }
   return MF_OK;
 }
@@ -467,7 +536,7 @@ extern "C" mf_status mf_embed(const mf_plan* p, const mf_dims* d, const void* w_
   mf::GemmParams gp{};
   GemmSpec sp[1] = {{p->Ni, H, C, d_zt, w_in, b_in, d_x_img, H, 0, 1}};
   return run_gemm(sp, 1, mf::kEpiBiasBf16, H >= 256 ? 256 : 128, gp, di,
-                  static_cast<cudaStream_t>(stream));
+                  static_cast<cudaStream_t>(stream), MF_K_GEMM_EMBED);
 }
 
 extern "C" size_t mf_final_workspace_bytes(const mf_plan* p, const mf_dims* d) {
@@ -502,14 +571,20 @@ extern "C" mf_status mf_final(const mf_plan* p, const mf_dims* d, const mf_temb_
   bf16* a = reinterpret_cast<bf16*>(ws + L.a);
   MF_TRY(conditioning(p, d, temb, t, reinterpret_cast<float*>(ws + L.sinus),
                       reinterpret_cast<float*>(ws + L.h1), c, st));
-  MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w_fmod), static_cast<const bf16*>(b_fmod), c, S, H,
-                          2 * H, fmod, 2 * H, 0, 0, st));
+  {
+    Trace tr(MF_K_COND, st, 2.0 * S * 2.0 * H * H, 2.0 * 2.0 * H * H, 1);
+    MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w_fmod), static_cast<const bf16*>(b_fmod), c, S, H,
+                            2 * H, fmod, 2 * H, 0, 0, st));
+  }
   mf::LnModArgs ln{static_cast<const bf16*>(d_x_img), nullptr, p->Ni, p->Ni, H,
                    p->d_srow_seq + p->Nt, fmod, 2LL * H, 0, 0, H, a};
-  MF_CUDA(mf::launch_ln_modulate(ln, st));
+  {
+    Trace tr(MF_K_LN, st, 0, 4.0 * p->Ni * H, 1);
+    MF_CUDA(mf::launch_ln_modulate(ln, st));
+  }
   mf::GemmParams gp{};
   GemmSpec sp[1] = {{p->Ni, C, H, a, w_out, b_out, d_v, C, 0, 1}};
-  return run_gemm(sp, 1, mf::kEpiBiasF32, 128, gp, di, st);
+  return run_gemm(sp, 1, mf::kEpiBiasF32, 128, gp, di, st, MF_K_GEMM_FINAL);
 }
 
 // ====================================================================== rectified-flow epilogues
@@ -533,6 +608,8 @@ extern "C" mf_status mf_interpolate(const mf_plan* p, int32_t C, const float* d_
   if (!aligned(d_z, 16) || !aligned(d_eps, 16) || !aligned(d_zt, 16) || !aligned(d_zt_bf16, 16) ||
       !aligned(d_t, 4))
     return MF_ERR_ALIGNMENT;
+  Trace tr(MF_K_LATENT, static_cast<cudaStream_t>(stream), 0,
+           (double)p->Ni * C * (8.0 + (d_zt ? 4.0 : 0.0) + (d_zt_bf16 ? 2.0 : 0.0)), 1);
   return cuda_status(mf::launch_interpolate(p->d_img_seq, p->d_img_target, d_t ? d_t : p->d_t, p->Ni, C,
                                             d_z, d_eps, d_zt, static_cast<bf16*>(d_zt_bf16),
                                             static_cast<cudaStream_t>(stream)));
@@ -549,6 +626,7 @@ extern "C" mf_status mf_cfg_combine(const mf_plan* p, int32_t C, float w, const 
   const char* a = reinterpret_cast<const char*>(d_v);
   const char* b = reinterpret_cast<const char*>(d_v_out);
   if (a != b && a < b + bytes && b < a + bytes) return MF_ERR_INVALID_ARG;  // partial overlap
+  Trace tr(MF_K_LATENT, static_cast<cudaStream_t>(stream), 0, (double)p->Ni * C * 8.0, 1);
   return cuda_status(mf::launch_cfg(p->d_img_seq, p->d_seq_role, p->d_img_pair, p->Ni, C, w, d_v,
                                     d_v_out, static_cast<cudaStream_t>(stream)));
 }
@@ -560,6 +638,8 @@ extern "C" mf_status mf_euler_step(const mf_plan* p, int32_t C, float dt, const 
   if (p->Ni == 0) return MF_OK;
   if (d_v == nullptr || d_z == nullptr || !std::isfinite(dt)) return MF_ERR_INVALID_ARG;
   if (!aligned(d_v, 16) || !aligned(d_z, 16) || !aligned(d_z_bf16, 16)) return MF_ERR_ALIGNMENT;
+  Trace tr(MF_K_LATENT, static_cast<cudaStream_t>(stream), 0,
+           (double)p->Ni * C * (12.0 + (d_z_bf16 ? 2.0 : 0.0)), 1);
   return cuda_status(mf::launch_euler(p->Ni, C, dt, d_v, d_z, static_cast<bf16*>(d_z_bf16),
                                       static_cast<cudaStream_t>(stream)));
 }
@@ -581,6 +661,7 @@ extern "C" mf_status mf_flow_loss(const mf_plan* p, int32_t C, const float* d_z,
       !aligned(d_count, 8) || !aligned(d_mean, 8) || !aligned(d_ws, 256))
     return MF_ERR_ALIGNMENT;
   if (ws_bytes < mf_flow_loss_workspace_bytes(p)) return MF_ERR_WORKSPACE;
+  Trace tr(MF_K_LOSS, static_cast<cudaStream_t>(stream), 0, (double)p->Ni * C * 12.0, 3);
   return cuda_status(mf::launch_flow_loss(p->d_cui, p->d_img_target, p->S, p->Ni, C, d_z, d_eps, d_v,
                                           static_cast<double*>(d_ws), d_loss_sum,
                                           reinterpret_cast<long long*>(d_count), d_mean,
@@ -615,6 +696,7 @@ extern "C" mf_status mf_attention(const mf_plan* p, int32_t heads, int32_t head_
   ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
   ap.status = di->status;
   ap.wait_limit_ns = wait_limit_ns();
+  Trace tr(MF_K_ATTN, static_cast<cudaStream_t>(stream), 4.0 * p->sum_L2 * H, 0, 1);
   return cuda_status(mf::launch_attention(ap, head_dim, static_cast<cudaStream_t>(stream)));
 }
 
@@ -630,7 +712,7 @@ extern "C" mf_status mf_gemm(int32_t M, int32_t N, int32_t K, const void* d_a, c
   mf::GemmParams gp{};
   GemmSpec sp[1] = {{M, N, K, d_a, d_b, d_bias, d_c, N, 0, 0}};
   return run_gemm(sp, 1, out_f32 ? mf::kEpiBiasF32 : mf::kEpiBiasBf16, N <= 128 ? 128 : 256, gp, di,
-                  static_cast<cudaStream_t>(stream));
+                  static_cast<cudaStream_t>(stream), MF_K_GEMM_PLAIN);
 }
 
 // ====================================================================== status
@@ -654,8 +736,47 @@ extern "C" mf_status mf_selftest_timeout(int32_t limit_us, void* stream) {
   MF_TRY(device_info(&di));
   if (limit_us < 1 || limit_us > 1000000) return MF_ERR_INVALID_ARG;
   MF_TRY(mf_check(stream));  // start from a clean status word
+  Trace tr(MF_K_COND, static_cast<cudaStream_t>(stream), 0, 0, 1);
   if (mf::launch_timeout_selftest(di->status, (unsigned long long)limit_us * 1000ull,
                                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MF_ERR_CUDA;
   return mf_check(stream);
 }
+
+// ====================================================================== tracing
+extern "C" mf_status mf_trace_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace.on = on != 0;
+  if (g_trace.on) {
+    for (auto& r : g_trace.recs) {
+      g_trace.pool.push_back(r.a);
+      g_trace.pool.push_back(r.b);
+    }
+    g_trace.recs.clear();
+  }
+  return MF_OK;
+}
+
+extern "C" mf_status mf_trace_read(mf_trace_entry* e, int32_t n) {
+  if (e == nullptr || n < MF_K_COUNT) return MF_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  for (int i = 0; i < n; ++i) e[i] = mf_trace_entry{0, 0.0, 0.0, 0.0};
+  mf_status st = MF_OK;
+  for (auto& r : g_trace.recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+      st = MF_ERR_CUDA;
+    if (r.kind >= 0 && r.kind < n) {
+      e[r.kind].launches += r.nk;
+      e[r.kind].ms += ms;
+      e[r.kind].flops += r.flops;
+      e[r.kind].bytes += r.bytes;
+    }
+    g_trace.pool.push_back(r.a);
+    g_trace.pool.push_back(r.b);
+  }
+  g_trace.recs.clear();
+  return st;
+}
+
+extern "C" int64_t mf_launch_count(void) { return g_launches.load(); }

@@ -12,6 +12,7 @@
 struct mf_plan {
   int32_t budget = 0;
   int32_t S = 0, N = 0, Nt = 0, Ni = 0, n_items = 0;
+  double sum_L2 = 0.0;  // sum over samples of (sample length)^2: attention work
 
   std::vector<int32_t> order;       // [S]    candidate index per packed sample
   std::vector<int32_t> cu;          // [S+1]  joint offsets (cu_seqlens)

@@ -144,6 +144,7 @@ extern "C" mf_status mf_pack(const mf_sample* samples, int32_t n, int32_t budget
   });
   for (int32_t k : seqs) {
     int32_t L = p->cu[k + 1] - p->cu[k];
+    p->sum_L2 += (double)L * (double)L;
     int32_t nq = (L + mf::kQTile - 1) / mf::kQTile;
     for (int32_t q = 0; q < nq; ++q) {
       p->items.push_back(k);

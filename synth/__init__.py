@@ -243,6 +243,18 @@ def batch_inputs(samples, dims: Dims, seed: int, bf16: bool = True) -> Batch:
     return Batch(list(samples), xs, zs, es)
 
 
+def pack_inputs(samples, order, dims: Dims, seed: int):
+    """Inputs of the packed candidates only, concatenated in stream order (pack order):
+    x_txt [N_txt][H], z and eps [N_img][C], all bf16-exact float32.  Candidate c draws the same
+    values as batch_inputs() gives it (the streams are keyed by candidate index)."""
+    H, C = dims.hidden, dims.channels
+    xs = [round_bf16(normal(seed, f"x_txt.{c}", (samples[c].txt_len, H))) for c in order]
+    zs = [round_bf16(normal(seed, f"z.{c}", (samples[c].img_len, C))) for c in order]
+    es = [round_bf16(normal(seed, f"eps.{c}", (samples[c].img_len, C))) for c in order]
+    cat = lambda a, w: np.concatenate(a) if a else np.zeros((0, w), np.float32)   # noqa: E731
+    return cat(xs, H), cat(zs, C), cat(es, C)
+
+
 def cfg_batch(samples, dims: Dims, seed: int) -> Batch:
     """Packed-CFG inputs: each uncond branch shares its cond partner's starting noise z0
     (stored in `z`) and takes no text."""

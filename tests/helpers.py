@@ -29,6 +29,26 @@ def assert_close(got, ref, name, rel=TOL_REL, cos=TOL_COS):
     return s
 
 
+def bf16_ulp(x):
+    """Spacing of bf16 numbers at |x| (8 significand bits)."""
+    a = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def assert_update_close(got, ref, x_in, name, frac=3e-2):
+    """Checks a residual update out = x_in + delta stored in bf16: each element may differ
+    from the exact result by one bf16 rounding of the output plus `frac` of the largest exact
+    update.  (Comparing raw deltas would measure only the output rounding when the update is
+    smaller than one bf16 step of the residual.)"""
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    delta = ref - np.asarray(x_in, np.float64)
+    bound = bf16_ulp(ref) + frac * np.abs(delta).max()
+    err = np.abs(got - ref)
+    worst = float((err / bound).max()) if err.size else 0.0
+    assert worst <= 1.0, f"{name}: worst error / bound = {worst:.3f}, stats {stats(got - x_in, delta)}"
+    return stats(got - np.asarray(x_in, np.float64), delta)
+
+
 def stream_concat(parts, order, width):
     arrs = [parts[c] for c in order]
     if not arrs:

@@ -6,7 +6,7 @@ import pytest
 import synth
 from oracle import model as M
 from oracle import pack as opack
-from tests.helpers import assert_close, oracle_stack, stream_concat
+from tests.helpers import assert_close, assert_update_close, oracle_stack, stream_concat
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -107,8 +107,8 @@ def test_tiny_block_and_intermediates():
     got_t, got_i = _f(x_txt), _f(x_img)
     assert_close(got_t, xt_ref, "block x_txt")
     assert_close(got_i, xi_ref, "block x_img")
-    assert_close(got_t - x_txt0, xt_ref - x_txt0, "block delta txt", rel=3e-2, cos=0.999)
-    assert_close(got_i - emb, xi_ref - emb, "block delta img", rel=3e-2, cos=0.999)
+    assert_update_close(got_t, xt_ref, x_txt0, "block update txt")
+    assert_update_close(got_i, xi_ref, emb, "block update img")
 
 
 def _stack_and_loss(case, n_blocks):
