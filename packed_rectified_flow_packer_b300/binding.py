@@ -4,7 +4,7 @@ runs in the library's kernels.  Function names are the C entry points' names.
 Device memory is whatever the caller passes: torch tensors (their data_ptr() is used), raw
 integer addresses, or None for NULL.  Streams default to torch's current CUDA stream.
 A non-OK status raises MageflowError.  Importing this module fails loudly when the library has
-not been built (python -m packed_rectified_flow_packer_b300.build).
+not been built (python packed_rectified_flow_packer_b300/build.py).
 """
 from __future__ import annotations
 
@@ -32,7 +32,7 @@ class MageflowError(RuntimeError):
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with "
-                      "`python -m packed_rectified_flow_packer_b300.build`")
+                      "`python packed_rectified_flow_packer_b300/build.py`")
 lib = C.CDLL(LIB_PATH)
 
 

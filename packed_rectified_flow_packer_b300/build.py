@@ -1,6 +1,6 @@
 """Builds libmageflow.so in-tree for sm_103a with nvcc (no JIT cache, no torch extension).
 
-    python -m packed_rectified_flow_packer_b300.build [--force]
+    python packed_rectified_flow_packer_b300/build.py [--force]
 
 Objects go to packed_rectified_flow_packer_b300/_build/ and the library to
 packed_rectified_flow_packer_b300/libmageflow.so.  Rebuilds only what changed.
