@@ -274,6 +274,27 @@ mf_status mf_flow_loss(const mf_plan* plan, int32_t channels, const float* d_z, 
                        const float* d_v, double* d_loss_sum, int64_t* d_count, double* d_mean,
                        void* d_ws, size_t ws_bytes, void* stream);
 
+/* Image rows the scratch of mf_flow_loss_noalloc holds (8 bytes each, per device). */
+#define MF_NOALLOC_MAX_IMG_ROWS 65536
+
+/* mf_flow_loss without a workspace argument, for callers that cannot allocate device memory
+ * where they compute the loss (an allocator owned by another framework that forbids side
+ * allocations, a fixed pre-reserved memory budget, or a point where an allocation would
+ * synchronise the device).  The paper has no counterpart: this is a library convenience.
+ * Same inputs, outputs and result as mf_flow_loss; the per-row scratch lives in one
+ * library-owned device array per device (MF_NOALLOC_MAX_IMG_ROWS doubles, held until the
+ * library is unloaded).  The call allocates nothing.
+ *   - The first call on a device looks up that array's device address (with the device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - All calls on a device share the array: calls that overlap on the GPU (unordered
+ *     streams) race; order them on one stream.  Each call writes every scratch row before it
+ *     reads it, so nothing left by an earlier call reaches the result.
+ * Errors: as mf_flow_loss, and MF_ERR_WORKSPACE when the plan has more than
+ * MF_NOALLOC_MAX_IMG_ROWS image rows (checked before any launch). */
+mf_status mf_flow_loss_noalloc(const mf_plan* plan, int32_t channels, const float* d_z,
+                               const float* d_eps, const float* d_v, double* d_loss_sum,
+                               int64_t* d_count, double* d_mean, void* stream);
+
 /* ------------------------------------------------------------------------------------ */
 /* Building blocks, exposed for testing and reuse                                        */
 /* ------------------------------------------------------------------------------------ */
