@@ -108,8 +108,8 @@ typedef struct mf_plan mf_plan; /* opaque; owned by the library, freed with mf_p
 mf_status mf_pack(const mf_sample* samples, int32_t n, int32_t budget, mf_plan** out);
 
 /* Copies the plan's index buffers to the current device (library-owned device memory,
- * allocated on the first upload, freed by mf_plan_free).  Asynchronous on `stream`; the
- * host copy must not be modified meanwhile (it never is: plans are immutable).
+ * allocated on the first upload, freed by mf_plan_free).  The copy is enqueued on `stream`
+ * and synchronised before the call returns; a second upload on the same device is a no-op.
  * Errors: MF_ERR_INVALID_ARG, MF_ERR_CUDA. */
 mf_status mf_plan_upload(mf_plan* plan, void* stream);
 
