@@ -122,7 +122,7 @@ typedef struct {
   int32_t n_tok;      /* N: packed tokens (<= budget) */
   int32_t n_txt;      /* text-stream rows */
   int32_t n_img;      /* image-stream rows */
-  int32_t n_items;    /* attention work items (sequence, 128-row query tile) */
+  int32_t n_items;    /* attention work items (sequence, 256-row query block) */
   int32_t budget;
   int32_t uploaded;   /* 1 after mf_plan_upload */
   int32_t reserved;
@@ -142,7 +142,8 @@ mf_status mf_plan_get_info(const mf_plan* plan, mf_plan_info* info);
  *   9 img_pair[N_img] CFG partner image row, -1 if none
  *  10 img_target[N_img] 1 for target-frame rows, 0 for an edit's source frame
  *  11 seq_role[S]     cfg_role of each packed sample
- *  12 items[n_items*2] attention work list (sequence, query tile), longest sequences first
+ *  12 items[n_items*2] attention work list (sequence, 256-row query block), longest sequences
+ *                     first
  * Errors: MF_ERR_INVALID_ARG for an unknown `which` or null pointers. */
 mf_status mf_plan_array(const mf_plan* plan, int32_t which, const int32_t** data, int64_t* len);
 

@@ -24,7 +24,7 @@ struct mf_plan {
   std::vector<int32_t> img_pair;    // [Ni]  CFG partner row or -1
   std::vector<int32_t> img_target;  // [Ni]  1 = target frame
   std::vector<int32_t> seq_role;    // [S]   cfg_role
-  std::vector<int32_t> items;       // [n_items*2] (sequence, query tile), longest first
+  std::vector<int32_t> items;       // [n_items*2] (sequence, query block), longest first
   std::vector<float> t;             // [S]   flow time per packed sample
 
   // stream-sorted rows: text rows 0..Nt-1, then image rows Nt..Nt+Ni-1
@@ -52,5 +52,5 @@ struct mf_plan {
 
 namespace mf {
 
-constexpr int kQTile = 128;  // attention query / key tile rows
+constexpr int kQBlock = 256;  // query rows of one attention work item (two 128-row tiles)
 }  // namespace mf

@@ -136,7 +136,7 @@ extern "C" mf_status mf_pack(const mf_sample* samples, int32_t n, int32_t budget
   }
   for (int32_t r = 0; r < Nt + Ni; ++r) p->joint_srow[p->srow_joint[r]] = r;
 
-  // attention work list: (sequence, query tile), longest sequences first (stable)
+  // attention work list: (sequence, 256-row query block), longest sequences first (stable)
   std::vector<int32_t> seqs(S);
   for (int32_t k = 0; k < S; ++k) seqs[k] = k;
   std::stable_sort(seqs.begin(), seqs.end(), [&](int32_t a, int32_t b) {
@@ -145,7 +145,7 @@ extern "C" mf_status mf_pack(const mf_sample* samples, int32_t n, int32_t budget
   for (int32_t k : seqs) {
     int32_t L = p->cu[k + 1] - p->cu[k];
     p->sum_L2 += (double)L * (double)L;
-    int32_t nq = (L + mf::kQTile - 1) / mf::kQTile;
+    int32_t nq = (L + mf::kQBlock - 1) / mf::kQBlock;
     for (int32_t q = 0; q < nq; ++q) {
       p->items.push_back(k);
       p->items.push_back(q);

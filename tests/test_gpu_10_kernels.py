@@ -62,13 +62,13 @@ def _attn_plan(samples):
 ATTN_SAMPLES = [synth.Sample(3, 1, 1, 2, 0.5), synth.Sample(0, 1, 1, 1, 0.5),
                 synth.Sample(27, 1, 10, 10, 0.5), synth.Sample(28, 1, 10, 10, 0.5),
                 synth.Sample(29, 1, 10, 10, 0.5), synth.Sample(44, 1, 16, 16, 0.5),
-                synth.Sample(100, 2, 16, 16, 0.5)]
+                synth.Sample(100, 2, 16, 16, 0.5), synth.Sample(17, 1, 30, 40, 0.5)]
 
 
 @pytest.mark.parametrize("heads,D", [(2, 128), (4, 64)])
 @pytest.mark.parametrize("growth", [0.0, 6.0])
 def test_attention_ragged(heads, D, growth):
-    """Ragged samples (1 .. 612 tokens, tile tails on both sides of 128).  `growth` scales the
+    """Ragged samples (1 .. 1217 tokens, tile tails on both sides of 128 and 256).  `growth` scales the
     keys up along each sample so later key tiles raise the running max by large steps (the
     rescaling path)."""
     ref, plan = _attn_plan(ATTN_SAMPLES)

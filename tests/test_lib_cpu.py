@@ -52,10 +52,10 @@ def _same_plan(samples, budget):
     np.testing.assert_array_equal(got.array("seq_role"), roles)
     i = got.info()
     assert (i.n_seq, i.n_tok, i.n_txt, i.n_img) == (ref.n_seq, ref.n_tok, ref.n_txt, ref.n_img)
-    # attention work list: every (sample, query tile) once, longest samples first
+    # attention work list: every (sample, 256-row query block) once, longest samples first
     items = got.array("items").reshape(-1, 2)
     lens = np.diff(ref.cu_seqlens)
-    want = sorted((s, q) for s in range(ref.n_seq) for q in range(-(-lens[s] // 128)))
+    want = sorted((s, q) for s in range(ref.n_seq) for q in range(-(-lens[s] // 256)))
     assert sorted(map(tuple, items.tolist())) == want
     assert np.all(np.diff(lens[items[:, 0]]) <= 0) if len(items) else True
     return got
