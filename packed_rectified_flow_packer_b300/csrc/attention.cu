@@ -26,8 +26,9 @@
 // and P_t's columns may be overwritten (the PV that read them has completed).
 // The running max is only moved (and O rescaled in TMEM) when a tile's max exceeds it by
 // more than 8 in log2 units; the result is unchanged because numerator and denominator use
-// the same stale max, and P stays <= 2^8.  A quarter of the exponentials of full key tiles
-// run on the FMA pipe (exp2_fma) to relieve the special-function unit.
+// the same stale max, and P stays <= 2^8.  Per score the softmax spends half a three-input
+// max, half a packed f32x2 FMA (scale and shift), one ex2.approx, half a packed add (row sum)
+// and half a bf16x2 conversion.
 #include "attention.cuh"
 
 namespace mf {
@@ -38,27 +39,36 @@ constexpr uint32_t kAtom = 16384;   // 128 rows x 128 bytes
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kThreads = 320;
 
-// 2^x on the FMA pipe: x = n + f with n = floor(x), f in [0, 1); 2^f from a degree-3
-// polynomial fitted by us (iteratively reweighted least squares on relative error over
-// [0, 1]); n is then added to the result's exponent field.  Max relative error 7.6e-5, far
-// inside the bf16 rounding P gets next.  Inputs below -125 give (near) zero.
-__device__ __forceinline__ float exp2_fma(float x) {
-  x = fmaxf(x, -125.0f);
-  const float n = floorf(x);
-  const float f = x - n;
-  float p = fmaf(0.07802354544401169f, f, 0.22606661915779114f);
-  p = fmaf(p, f, 0.6958348155021667f);
-  p = fmaf(p, f, 0.9999249577522278f);
-  return __int_as_float(__float_as_int(p) + (static_cast<int>(n) << 23));
+// Three-input f32 maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
-// 16 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+// (x0, x1) = (x0 * c + d, x1 * c + d) as one packed f32x2 FMA.
+__device__ __forceinline__ void fma2(float& x0, float& x1, float c, float d) {
+  asm("{\n\t.reg .b64 x, c, d;\n\t"
+      "mov.b64 x, {%0, %1};\n\tmov.b64 c, {%2, %2};\n\tmov.b64 d, {%3, %3};\n\t"
+      "fma.rn.f32x2 x, x, c, d;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(x0), "+f"(x1)
+      : "f"(c), "f"(d));
+}
+
+// (a0, a1) += (x0, x1) as one packed f32x2 add.
+__device__ __forceinline__ void add2(float& a0, float& a1, float x0, float x1) {
+  asm("{\n\t.reg .b64 a, x;\n\t"
+      "mov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\t"
+      "add.rn.f32x2 a, a, x;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1));
+}
+
+// 8 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
       : "memory");
 }
 
@@ -262,47 +272,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           for (int i = 0; i < kT; ++i)
             if (i >= valid) sr[i >> 5][i & 31] = __float_as_uint(-INFINITY);
         }
-        float mx[8];
+#define MF_S(i) __uint_as_float(sr[(i) >> 5][(i) & 31])
+        float mx[4] = {MF_S(0), MF_S(1), MF_S(2), MF_S(3)};
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(sr[0][u]);
-#pragma unroll
-        for (int i = 8; i < kT; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sr[i >> 5][i & 31]));
-        const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
+        for (int i = 4; i < kT; i += 2) mx[(i >> 1) & 3] = max3f(mx[(i >> 1) & 3], MF_S(i), MF_S(i + 1));
+        const float m_tile = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c;
         const bool need = (j == 0) || (m_tile > m + kRescaleLog2);
         const float alpha = (j > 0 && need) ? ex2_approx(m - m_tile) : 1.0f;
         if (need) m = m_tile;
 
         // P_j = exp2(S c - m) in bf16, two keys per 32-bit TMEM column, written over the
-        // first 64 columns of S_t, 32 keys at a time
+        // first 64 columns of S_t, 16 keys at a time
         const float neg_m = -m;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t pk[16];
-          if (valid >= kT) {
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t pk[8];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float a0 = fmaf(__uint_as_float(sr[cc][i]), c, neg_m);
-              const float a1 = fmaf(__uint_as_float(sr[cc][i + 1]), c, neg_m);
-              const float e0 = ex2_approx(a0);
-              const float e1 = (i & 2) ? exp2_fma(a1) : ex2_approx(a1);
-              ls[i & 3] += e0;
-              ls[(i & 3) + 1] += e1;
-              pk[i >> 1] = pack_bf16x2(e0, e1);
-            }
-          } else {  // last key tile: masked columns hold -inf, and ex2(-inf) is exactly 0
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float e0 = ex2_approx(fmaf(__uint_as_float(sr[cc][i]), c, neg_m));
-              const float e1 = ex2_approx(fmaf(__uint_as_float(sr[cc][i + 1]), c, neg_m));
-              ls[i & 3] += e0;
-              ls[(i & 3) + 1] += e1;
-              pk[i >> 1] = pack_bf16x2(e0, e1);
-            }
+          for (int i = 0; i < 16; i += 2) {
+            float e0 = MF_S(cc * 16 + i), e1 = MF_S(cc * 16 + i + 1);
+            fma2(e0, e1, c, neg_m);
+            e0 = ex2_approx(e0);  // masked columns: ex2(-inf) is exactly 0
+            e1 = ex2_approx(e1);
+            add2(ls[i & 2], ls[(i & 2) + 1], e0, e1);
+            pk[i >> 1] = pack_bf16x2(e0, e1);
           }
-          tmem_st16(lane_base + s_col + cc * 16, pk);
+          tmem_st8(lane_base + s_col + cc * 8, pk);
         }
+#undef MF_S
         l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         // O_t is quiescent here (see the header): rescale it in place when a row's max moved
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
