@@ -250,6 +250,8 @@ struct GemmSpec {
 
 mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmParams& p,
                    const DevInfo* di, cudaStream_t st, int kind) {
+  // 256-wide tiles run on CTA pairs (256 x 256 per pair), 128-wide ones on single CTAs
+  const bool pair = BN == 256;
   p.n_prob = 0;
   p.tile_begin[0] = 0;
   int begin = 0;
@@ -258,7 +260,7 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
     if (g.M <= 0) continue;
     const int i = p.n_prob;
     if (!make_tmap(&p.tmA[i], g.A, g.K, g.M, 128)) return MF_ERR_CUDA;
-    if (!make_tmap(&p.tmB[i], g.B, g.K, g.N, BN)) return MF_ERR_CUDA;
+    if (!make_tmap(&p.tmB[i], g.B, g.K, g.N, pair ? BN / 2 : BN)) return MF_ERR_CUDA;
     p.prob[i].M = g.M;
     p.prob[i].N = g.N;
     p.prob[i].K = g.K;
@@ -267,7 +269,7 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
     p.prob[i].ldo = g.ldo;
     p.prob[i].bias = static_cast<const bf16*>(g.bias);
     p.prob[i].out = g.out;
-    p.tiles_m[i] = (g.M + 127) / 128;
+    p.tiles_m[i] = pair ? (g.M + 255) / 256 : (g.M + 127) / 128;
     p.tiles_n[i] = (g.N + BN - 1) / BN;
     begin += p.tiles_m[i] * p.tiles_n[i];
     p.tile_begin[i + 1] = begin;
@@ -280,7 +282,8 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
   double flops = 0;
   for (int i = 0; i < p.n_prob; ++i) flops += 2.0 * p.prob[i].M * (double)p.prob[i].N * p.prob[i].K;
   Trace tr(kind, st, flops, 0, 1);
-  return cuda_status(mf::launch_gemm(p, BN, epi, di->sms, st));
+  return cuda_status(pair ? mf::launch_gemm_pair(p, epi, di->sms, st)
+                          : mf::launch_gemm(p, BN, epi, di->sms, st));
 }
 
 mf_status conditioning(const mf_plan* p, const mf_dims* d, const mf_temb_weights* tw,

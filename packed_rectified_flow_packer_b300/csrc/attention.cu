@@ -64,12 +64,13 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float x0, float x1) {
       : "f"(x0), "f"(x1));
 }
 
-// 8 consecutive 32-bit columns of this thread's TMEM lane.
+// 8 consecutive 32-bit columns of this thread's TMEM lane.  No memory clobber, so the
+// compiler may interleave the arithmetic of neighbouring chunks with the stores; the stores
+// stay ordered before tcgen05.wait::st (both are volatile asm).
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-      : "memory");
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
 }
 
 // O_t += P_t V: A operand (P, 128 x 16 bf16 per instruction) read from TMEM.
@@ -186,47 +187,49 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
+    // Waits are ordered by criticality: P_t first, then the ring slot (whose copy normally
+    // landed long ago).  Shared-memory descriptors are built once and advanced by constants.
     if (lane == 0) {
-      const uint32_t qa = smem_u32(smem + L::off_q);
-      auto issue_s = [&](int t, uint32_t ka) {
+      const uint64_t qd = sdesc_sw128(smem_u32(smem + L::off_q), 16, 1024);
+      const uint64_t kv0d = sdesc_sw128(smem_u32(smem + L::off_kv), 16, 1024);
+      const uint64_t vv0d = sdesc_sw128(smem_u32(smem + L::off_kv), kAtom, 1024);
+      auto issue_s = [&](int t, int slot) {
+        const uint64_t kd = kv0d + ((slot * L::KV) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * kAtom + (kk & 3) * 32;
-          mma_bf16(tmem_base + t * kT, sdesc_sw128(qa + t * L::Q + o, 16, 1024),
-                   sdesc_sw128(ka + o, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          const uint32_t o = ((kk >> 2) * kAtom + (kk & 3) * 32) >> 4;
+          mma_bf16(tmem_base + t * kT, qd + ((t * L::Q) >> 4) + o, kd + o, IDESC_S, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[t]);
       };
-      auto slot_wait = [&](int idx) -> bool {
-        return mbar_wait(&kv_full[idx % NS], (idx / NS) & 1, lim) && !*(volatile int*)&abort_flag;
-      };
+      auto slot_wait = [&](int idx) -> bool { return mbar_wait(&kv_full[idx % NS], (idx / NS) & 1, lim); };
       bool ok = mbar_wait(&q_full, 0, lim) && slot_wait(0);
       if (ok) {
         tc_fence_after();
-        const uint32_t ka = smem_u32(smem + L::off_kv);
-        for (int t = 0; t < n_t; ++t) issue_s(t, ka);
+        for (int t = 0; t < n_t; ++t) issue_s(t, 0);
         mma_commit(&kv_empty[0]);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         const int iv = 2 * j + 1, ik = 2 * j + 2;
         const bool next = j + 1 < n_kv;
-        if (!slot_wait(iv) || (next && !slot_wait(ik))) {
-          ok = false;
-          break;
-        }
-        const uint32_t va = smem_u32(smem + L::off_kv + (iv % NS) * L::KV);
-        const uint32_t ka = smem_u32(smem + L::off_kv + (ik % NS) * L::KV);
+        const uint64_t vd = vv0d + (((iv % NS) * L::KV) >> 4);
         for (int t = 0; t < n_t; ++t) {
-          if (!mbar_wait(&p_full[t], j & 1, lim)) {
+          if (!mbar_wait(&p_full[t], j & 1, lim) || (t == 0 && !slot_wait(iv))) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_bf16_ts(tmem_base + O_COL + t * D, tmem_base + t * kT + kk * 8,
-                        sdesc_sw128(va + kk * 2048, kAtom, 1024), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-          if (next) issue_s(t, ka);
+            mma_bf16_ts(tmem_base + O_COL + t * D, tmem_base + t * kT + kk * 8, vd + ((kk * 2048) >> 4),
+                        IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          if (next) {
+            if (t == 0 && !slot_wait(ik)) {
+              ok = false;
+              break;
+            }
+            issue_s(t, ik % NS);
+          }
         }
         if (!ok) break;
         mma_commit(&kv_empty[iv % NS]);
@@ -255,8 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     bool ok = true;
     if (t < n_t) {
       for (int j = 0; j < n_kv; ++j) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, lim)) &&
-             !__any_sync(0xffffffffu, *(volatile int*)&abort_flag);
+        // one lane polls (eight warps spinning with all lanes would crowd the barrier unit the
+        // MMA issuer needs); the warp then synchronises before reading TMEM
+        uint32_t okw = 1;
+        if (lane == 0) okw = mbar_wait(&s_full[t], j & 1, lim) ? 1u : 0u;
+        ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
+        __syncwarp();
         if (!ok) break;
         tc_fence_after();
         uint32_t sr[4][32];

@@ -110,11 +110,12 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const GemmPr
     bf16* dst = (which == 0 ? p.q : (which == 1 ? p.k : p.v)) + (size_t)joint * p.H + cc;
     if (which < 2) {
       const int* ps = p.pos + (size_t)joint * 3;
-      const float pa[3] = {(float)__ldg(ps), (float)__ldg(ps + 1), (float)__ldg(ps + 2)};
+      const float pf = (float)__ldg(ps), pr_ = (float)__ldg(ps + 1), pc = (float)__ldg(ps + 2);
       const int g0 = (cc % p.head_dim) >> 1;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float th = pa[rope_axis[g0 + i]] * rope_inv[g0 + i];
+        const int ax = rope_axis[g0 + i];
+        const float th = (ax == 0 ? pf : (ax == 1 ? pr_ : pc)) * rope_inv[g0 + i];
         float s, c;
         sincosf(th, &s, &c);
         const float x0 = v[2 * i], x1 = v[2 * i + 1];
@@ -320,7 +321,243 @@ cudaError_t launch_t(const GemmParams& p, int num_sms, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------------------------------
+// CTA-pair variant: a cluster of two CTAs computes one 256 x 256 tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).  Each CTA stages its own 128 rows of
+// A and its own 128 rows of B (half of the tile's N) per 64-wide K block, so a CTA moves
+// 32 KB per K block instead of the 48 KB of the single-CTA 128 x 256 tile for the same MMA
+// work per SM.  Both CTAs' copies complete on the even CTA's full barrier; the even CTA's
+// MMA thread issues for the pair and its commits arrive on the barriers of both CTAs
+// (multicast), so each CTA's producer sees its own stage freed and each CTA's epilogue sees
+// its own 128 accumulator rows (TMEM lanes) ready.  Epilogue warps of both CTAs release an
+// accumulator buffer by arriving on the even CTA's barrier.
+template <int EPI>
+__global__ void __launch_bounds__(192, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int STAGES = 6;
+  constexpr int BN = 256;
+  constexpr uint32_t A_BYTES = kBM * kBK * 2;         // this CTA's 128 rows of A
+  constexpr uint32_t B_BYTES = (BN / 2) * kBK * 2;    // this CTA's 128 rows of B
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr uint32_t IDESC = idesc_bf16_f32(2 * kBM, BN, false);
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  __shared__ float rope_inv[64];
+  __shared__ int rope_axis[64];
+
+  uint8_t* smem = align1024(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const int total = p.tile_begin[p.n_prob];
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 8);  // lane 0 of the 4 epilogue warps of both CTAs
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if constexpr (EPI == kEpiQkvRope) {
+    const int D = p.head_dim;
+    if ((int)threadIdx.x < D / 2) {
+      const int g = threadIdx.x, d = 2 * g;
+      const int wf = D / 8, wr = 7 * D / 16;
+      int axis, j, width;
+      if (d < wf) { axis = 0; j = d / 2; width = wf; }
+      else if (d < wf + wr) { axis = 1; j = (d - wf) / 2; width = wr; }
+      else { axis = 2; j = (d - wf - wr) / 2; width = wr; }
+      rope_axis[g] = axis;
+      rope_inv[g] = (float)exp(-(2.0 * j / width) * 9.210340371976184);  // ln(10000)
+    }
+  }
+  if (warp == 1) tmem_alloc_pair(&tmem_base_sh, TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.n_prob; ++i) {
+      tma_prefetch_desc(&p.tmA[i]);
+      tma_prefetch_desc(&p.tmB[i]);
+    }
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised before any remote signal
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer (both CTAs)
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total; tile += n_pairs) {
+        int pi, m, n;
+        decode_tile(p, tile, pi, m, n);
+        const int nkb = p.prob[pi].K / kBK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, lim) || *(volatile int*)&abort_flag) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * STAGE_BYTES);
+          const uint32_t fb = mapa_shared(&full_bar[stage], 0);
+          tma_load_2d_pair(sa, &p.tmA[pi], kb * kBK, m * 2 * kBM + rank * kBM, fb);
+          tma_load_2d_pair(sa + A_BYTES, &p.tmB[pi], kb * kBK, n * BN + rank * (BN / 2), fb);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        *(volatile int*)&abort_flag = 1;
+        report_status(p.status, kStatusTimeout);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total; tile += n_pairs) {
+        int pi, m, n;
+        decode_tile(p, tile, pi, m, n);
+        const int nkb = p.prob[pi].K / kBK;
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, lim) || *(volatile int*)&abort_flag) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_pair(d_tmem, sdesc_sw128(a0 + k * 32, 16, 1024), sdesc_sw128(b0 + k * 32, 16, 1024),
+                          IDESC, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair_mc(&empty_bar[stage], 0x3);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(&tfull_bar[acc], 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (!ok) {
+        *(volatile int*)&abort_flag = 1;
+        report_status(p.status, kStatusTimeout);
+        mma_commit_pair_mc(&drain_bar, 0x1);  // wait for this thread's MMAs before TMEM is freed
+        mbar_wait(&drain_bar, 0, lim);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue warps (both CTAs)
+    const int q = warp & 3;
+    const uint32_t tempty0 = mapa_shared(&tempty_bar[0], 0), tempty1 = mapa_shared(&tempty_bar[1], 0);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = pair; tile < total; tile += n_pairs) {
+      int pi, m, n;
+      decode_tile(p, tile, pi, m, n);
+      const bool ok = mbar_wait(&tfull_bar[acc], acc_phase, lim);
+      if (!__all_sync(0xffffffffu, ok) || __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
+        if (lane == 0) {
+          *(volatile int*)&abort_flag = 1;
+          report_status(p.status, kStatusTimeout);
+        }
+        break;
+      }
+      tc_fence_after();
+      const GemmProblem& pr = p.prob[pi];
+      const int row = m * 2 * kBM + rank * kBM + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tmem_base, q * 32, acc * BN + c), r);
+        tmem_ld_wait();
+        tmem_reg_fence(r);
+        epilogue_chunk<EPI>(p, pr, row, n * BN + c, r, rope_inv, rope_axis);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc ? tempty1 : tempty0);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // the pair's MMAs and TMEM reads are done, no remote signal is pending
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int EPI>
+cudaError_t launch_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
+  constexpr int STAGES = 6;
+  const int smem = STAGES * (kBM * kBK * 2 + 128 * kBK * 2) + 1024;
+  auto kern = gemm_pair_kernel<EPI>;
+  static int max_pairs = 0;  // clusters of two that fit on the device at once (per instantiation)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_pairs == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_pairs = n < num_sms / 2 ? n : num_sms / 2;
+  }
+  const int total = p.tile_begin[p.n_prob];
+  if (total <= 0) return cudaSuccess;
+  const int pairs = total < max_pairs ? total : max_pairs;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 }  // namespace
+
+cudaError_t launch_gemm_pair(const GemmParams& p, int epi, int num_sms, cudaStream_t stream) {
+  switch (epi) {
+    case kEpiBiasBf16: return launch_pair<kEpiBiasBf16>(p, num_sms, stream);
+    case kEpiBiasF32: return launch_pair<kEpiBiasF32>(p, num_sms, stream);
+    case kEpiQkvRope: return launch_pair<kEpiQkvRope>(p, num_sms, stream);
+    case kEpiGateResid: return launch_pair<kEpiGateResid>(p, num_sms, stream);
+    case kEpiGelu: return launch_pair<kEpiGelu>(p, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_gemm(const GemmParams& p, int BN, int epi, int num_sms, cudaStream_t stream) {
 #define MF_GEMM_CASE(bn, ep) \

@@ -50,4 +50,9 @@ struct GemmParams {
 // Launches the persistent kernel for tile width BN in {128, 256}.
 cudaError_t launch_gemm(const GemmParams& p, int BN, int epi, int num_sms, cudaStream_t stream);
 
+// Launches the persistent CTA-pair kernel: 256 x 256 tiles, tmA boxes of 128 rows (each CTA's
+// half of the tile's rows), tmB boxes of 128 rows (each CTA's half of the tile's columns),
+// tiles_m counted in 256-row tiles.
+cudaError_t launch_gemm_pair(const GemmParams& p, int epi, int num_sms, cudaStream_t stream);
+
 }  // namespace mf

@@ -45,65 +45,100 @@ __global__ void sinusoid_kernel(const float* __restrict__ t, int S, int F, float
   out[(size_t)s * F + half + j] = (float)sin(a);
 }
 
+// Streaming 16-byte load of read-once data (weights, activations): not kept in L1.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 u;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+               : "l"(p));
+  return u;
+}
+
+// y[s][o] = act(W[o] . x[s] + b[o]) for every sample s.  One warp per kGemvRows consecutive
+// output features; each lane owns 8-element chunks k = 8*lane + 256*i.  Per chunk the lane
+// loads the kGemvRows weight chunks (read once, streamed past L1) and then each sample's x
+// chunk once ([S][K] f32, kept in L1), so x is re-read per kGemvRows rows, not per row.
+constexpr int kGemvRows = 4;
+
 template <int ACT>
-__global__ void gemv_kernel(const bf16* __restrict__ W, const bf16* __restrict__ b,
-                            const float* __restrict__ x, int S, int K, int O, float* __restrict__ y,
-                            int y_stride, int y_off) {
-  const int o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+__global__ void __launch_bounds__(256) gemv_kernel(const bf16* __restrict__ W, const bf16* __restrict__ b,
+                                                   const float* __restrict__ x, int S, int K, int O,
+                                                   float* __restrict__ y, int y_stride, int y_off) {
+  const int o0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kGemvRows;
   const int lane = threadIdx.x & 31;
-  if (o >= O) return;
-  const bf16* w = W + (size_t)o * K;
-  const float bias = b ? __bfloat162float(b[o]) : 0.0f;
+  if (o0 >= O) return;
+  const int nr = min(kGemvRows, O - o0);
   for (int s0 = 0; s0 < S; s0 += 4) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[kGemvRows][4] = {};
     for (int k = lane * 8; k < K; k += 256) {
-      float wf[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(w + k)), wf);
+      uint4 wv[kGemvRows];
+#pragma unroll
+      for (int r = 0; r < kGemvRows; ++r)
+        wv[r] = r < nr ? ld_stream16(W + (size_t)(o0 + r) * K + k) : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int si = 0; si < 4; ++si) {
         if (s0 + si < S) {
           const float4* xv = reinterpret_cast<const float4*>(x + (size_t)(s0 + si) * K + k);
           const float4 a = __ldg(xv), c = __ldg(xv + 1);
-          acc[si] += wf[0] * a.x + wf[1] * a.y + wf[2] * a.z + wf[3] * a.w + wf[4] * c.x +
-                     wf[5] * c.y + wf[6] * c.z + wf[7] * c.w;
+#pragma unroll
+          for (int r = 0; r < kGemvRows; ++r) {
+            float wf[8];
+            unpack8(wv[r], wf);
+            acc[r][si] += wf[0] * a.x + wf[1] * a.y + wf[2] * a.z + wf[3] * a.w + wf[4] * c.x +
+                          wf[5] * c.y + wf[6] * c.z + wf[7] * c.w;
+          }
         }
       }
     }
 #pragma unroll
-    for (int si = 0; si < 4; ++si) {
-      const float r = warp_sum(acc[si]) + bias;
-      if (lane == 0 && s0 + si < S)
-        y[(size_t)(s0 + si) * y_stride + y_off + o] = ACT == 1 ? silu_f(r) : r;
+    for (int r = 0; r < kGemvRows; ++r) {
+#pragma unroll
+      for (int si = 0; si < 4; ++si) {
+        const float v = warp_sum(acc[r][si]);
+        if (lane == 0 && r < nr && s0 + si < S) {
+          const float t = v + (b ? __bfloat162float(b[o0 + r]) : 0.0f);
+          y[(size_t)(s0 + si) * y_stride + y_off + o0 + r] = ACT == 1 ? silu_f(t) : t;
+        }
+      }
     }
   }
 }
 
 // ------------------------------------------------------------------ LN + modulate
+// One warp per row; the row stays in registers as packed bf16 (NV 16-byte chunks per lane),
+// is unpacked once per pass (mean, variance, output), and all NV loads are issued before the
+// first use.  shift / scale rows (f32, shared by every row of a sample) come through L1.
 template <int NV>
-__global__ void ln_modulate_kernel(const LnModArgs a) {
+__global__ void __launch_bounds__(128) ln_modulate_kernel(const LnModArgs a) {
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= a.rows) return;
   const int H = a.H;
   const bool second = r >= a.n_first;
   const bf16* x = second ? a.x_second + (size_t)(r - a.n_first) * H : a.x_first + (size_t)r * H;
-  float v[NV][8];
+  uint4 raw[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) raw[i] = ld_stream16(reinterpret_cast<const uint4*>(x) + lane + 32 * i);
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
-    unpack8(__ldg(reinterpret_cast<const uint4*>(x) + lane + 32 * i), v[i]);
+    float v[8];
+    unpack8(raw[i], v);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) s += v[i][u];
+    for (int u = 0; u < 8; ++u) s += v[u];
   }
   const float mean = warp_sum(s) / (float)H;
   float q = 0.f;
 #pragma unroll
-  for (int i = 0; i < NV; ++i)
+  for (int i = 0; i < NV; ++i) {
+    float v[8];
+    unpack8(raw[i], v);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const float d = v[i][u] - mean;
+      const float d = v[u] - mean;
       q += d * d;
     }
+  }
   const float rstd = rsqrtf(warp_sum(q) / (float)H + 1e-6f);
   const int seq = __ldg(a.row_seq + r);
   const float* mrow = a.mod + (size_t)seq * a.seq_stride + (second ? a.stream_stride : 0);
@@ -117,9 +152,10 @@ __global__ void ln_modulate_kernel(const LnModArgs a) {
     const float4 k0 = __ldg(sc + c4), k1 = __ldg(sc + c4 + 1);
     const float shv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
     const float scv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-    float o[8];
+    float v[8], o[8];
+    unpack8(raw[i], v);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) o[u] = (v[i][u] - mean) * rstd * (1.0f + scv[u]) + shv[u];
+    for (int u = 0; u < 8; ++u) o[u] = (v[u] - mean) * rstd * (1.0f + scv[u]) + shv[u];
     uint4 w;
     w.x = pack_bf16x2(o[0], o[1]);
     w.y = pack_bf16x2(o[2], o[3]);
@@ -299,7 +335,8 @@ cudaError_t launch_sinusoid(const float* t, int S, int F, float* out, cudaStream
 cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int K, int O, float* y,
                         int y_stride, int y_off, int act, cudaStream_t st) {
   if (S <= 0 || O <= 0) return cudaSuccess;
-  const int blocks = (O + 7) / 8;
+  const int warps = (O + kGemvRows - 1) / kGemvRows;
+  const int blocks = (warps + 7) / 8;
   if (act == 1)
     gemv_kernel<1><<<blocks, 256, 0, st>>>(W, b, x, S, K, O, y, y_stride, y_off);
   else
@@ -309,10 +346,10 @@ cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int
 
 cudaError_t launch_ln_modulate(const LnModArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
-  const int blocks = (a.rows + 7) / 8;
+  const int blocks = (a.rows + 3) / 4;
   switch (a.H / 256) {
 #define MF_LN_CASE(nv) \
-  case nv: ln_modulate_kernel<nv><<<blocks, 256, 0, st>>>(a); break;
+  case nv: ln_modulate_kernel<nv><<<blocks, 128, 0, st>>>(a); break;
     MF_LN_CASE(1) MF_LN_CASE(2) MF_LN_CASE(3) MF_LN_CASE(4) MF_LN_CASE(5) MF_LN_CASE(6)
     MF_LN_CASE(7) MF_LN_CASE(8) MF_LN_CASE(9) MF_LN_CASE(10) MF_LN_CASE(11) MF_LN_CASE(12)
     MF_LN_CASE(13) MF_LN_CASE(14) MF_LN_CASE(15) MF_LN_CASE(16)
