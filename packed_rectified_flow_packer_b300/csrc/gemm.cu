@@ -116,8 +116,12 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const GemmPr
       for (int i = 0; i < 16; ++i) {
         const int ax = rope_axis[g0 + i];
         const float th = (ax == 0 ? pf : (ax == 1 ? pr_ : pc)) * rope_inv[g0 + i];
+        // |th| <= max position (< 2^10): reduce modulo 2 pi with a two-constant Cody-Waite
+        // step (2 pi = kHi + kLo), then the hardware sine / cosine on [-pi, pi]
+        const float kq = rintf(th * 0.15915494309189535f);
+        const float rr = fmaf(-kq, -1.7484555314695172e-07f, fmaf(-kq, 6.2831854820251465f, th));
         float s, c;
-        sincosf(th, &s, &c);
+        __sincosf(rr, &s, &c);
         const float x0 = v[2 * i], x1 = v[2 * i + 1];
         v[2 * i] = x0 * c - x1 * s;
         v[2 * i + 1] = x0 * s + x1 * c;
@@ -323,6 +327,8 @@ cudaError_t launch_t(const GemmParams& p, int num_sms, cudaStream_t stream) {
 
 
 // ---------------------------------------------------------------------------------------
+constexpr int kPairThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
+
 // CTA-pair variant: a cluster of two CTAs computes one 256 x 256 tile with
 // tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).  Each CTA stages its own 128 rows of
 // A and its own 128 rows of B (half of the tile's N) per 64-wide K block, so a CTA moves
@@ -330,10 +336,11 @@ cudaError_t launch_t(const GemmParams& p, int num_sms, cudaStream_t stream) {
 // work per SM.  Both CTAs' copies complete on the even CTA's full barrier; the even CTA's
 // MMA thread issues for the pair and its commits arrive on the barriers of both CTAs
 // (multicast), so each CTA's producer sees its own stage freed and each CTA's epilogue sees
-// its own 128 accumulator rows (TMEM lanes) ready.  Epilogue warps of both CTAs release an
-// accumulator buffer by arriving on the even CTA's barrier.
+// its own 128 accumulator rows (TMEM lanes) ready.  Eight epilogue warps per CTA, two per TMEM
+// lane quarter, each take 128 of the tile's 256 columns; the epilogue warps of both CTAs
+// release an accumulator buffer by arriving on the even CTA's barrier.
 template <int EPI>
-__global__ void __launch_bounds__(192, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   constexpr int STAGES = 6;
   constexpr int BN = 256;
   constexpr uint32_t A_BYTES = kBM * kBK * 2;         // this CTA's 128 rows of A
@@ -366,7 +373,7 @@ __global__ void __launch_bounds__(192, 1) gemm_pair_kernel(const __grid_constant
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
-      mbar_init(&tempty_bar[b], 8);  // lane 0 of the 4 epilogue warps of both CTAs
+      mbar_init(&tempty_bar[b], 16);  // lane 0 of the 8 epilogue warps of both CTAs
     }
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
@@ -471,7 +478,8 @@ __global__ void __launch_bounds__(192, 1) gemm_pair_kernel(const __grid_constant
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue warps (both CTAs)
-    const int q = warp & 3;
+    const int q = warp & 3;                 // TMEM lane quarter = 32 accumulator rows
+    const int c_lo = ((warp - 2) >> 2) * (BN / 2);  // first of this warp's 128 columns
     const uint32_t tempty0 = mapa_shared(&tempty_bar[0], 0), tempty1 = mapa_shared(&tempty_bar[1], 0);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = pair; tile < total; tile += n_pairs) {
@@ -489,7 +497,7 @@ __global__ void __launch_bounds__(192, 1) gemm_pair_kernel(const __grid_constant
       const GemmProblem& pr = p.prob[pi];
       const int row = m * 2 * kBM + rank * kBM + q * 32 + lane;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
+      for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
         uint32_t r[32];
         tmem_ld32(tmem_addr(tmem_base, q * 32, acc * BN + c), r);
         tmem_ld_wait();
@@ -524,7 +532,7 @@ cudaError_t launch_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cfg.attrs = attr;
