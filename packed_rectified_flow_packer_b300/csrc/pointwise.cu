@@ -55,38 +55,47 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 }
 
 // y[s][o] = act(W[o] . x[s] + b[o]) for every sample s.  One warp per kGemvRows consecutive
-// output features; each lane owns 8-element chunks k = 8*lane + 256*i.  Per chunk the lane
-// loads the kGemvRows weight chunks (read once, streamed past L1) and then each sample's x
-// chunk once ([S][K] f32, kept in L1), so x is re-read per kGemvRows rows, not per row.
-constexpr int kGemvRows = 4;
+// output features; lane l owns the 8-element chunks k = 8 l + 256 i, i < NCH = K / 256.  All
+// kGemvRows * NCH weight chunks of the warp (read once, streamed past L1) are requested before
+// the first multiply, so every warp keeps its whole share of the weight stream in flight; x
+// ([S][K] f32, S <= 4) comes from L1, one load per chunk shared by the warp's rows.
+constexpr int kGemvRows = 2;
 
-template <int ACT>
-__global__ void __launch_bounds__(256) gemv_kernel(const bf16* __restrict__ W, const bf16* __restrict__ b,
-                                                   const float* __restrict__ x, int S, int K, int O,
+template <int ACT, int NCH>
+__global__ void __launch_bounds__(128) gemv_kernel(const bf16* __restrict__ W, const bf16* __restrict__ b,
+                                                   const float* __restrict__ x, int S, int O,
                                                    float* __restrict__ y, int y_stride, int y_off) {
+  constexpr int K = NCH * 256;
   const int o0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kGemvRows;
   const int lane = threadIdx.x & 31;
   if (o0 >= O) return;
   const int nr = min(kGemvRows, O - o0);
-  for (int s0 = 0; s0 < S; s0 += 4) {
-    float acc[kGemvRows][4] = {};
-    for (int k = lane * 8; k < K; k += 256) {
-      uint4 wv[kGemvRows];
+  uint4 wv[kGemvRows][NCH];
 #pragma unroll
-      for (int r = 0; r < kGemvRows; ++r)
-        wv[r] = r < nr ? ld_stream16(W + (size_t)(o0 + r) * K + k) : make_uint4(0, 0, 0, 0);
+  for (int r = 0; r < kGemvRows; ++r)
+#pragma unroll
+    for (int i = 0; i < NCH; ++i)
+      wv[r][i] = r < nr ? ld_stream16(W + (size_t)(o0 + r) * K + lane * 8 + 256 * i) : make_uint4(0, 0, 0, 0);
+  // at most four samples per launch (the host launches once per group of four), so each weight
+  // chunk is unpacked once, right where it is used
+  {
+    constexpr int s0 = 0;
+    float acc[kGemvRows][4] = {};
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int k = lane * 8 + 256 * i;
+      float wf[kGemvRows][8];
+#pragma unroll
+      for (int r = 0; r < kGemvRows; ++r) unpack8(wv[r][i], wf[r]);
 #pragma unroll
       for (int si = 0; si < 4; ++si) {
         if (s0 + si < S) {
           const float4* xv = reinterpret_cast<const float4*>(x + (size_t)(s0 + si) * K + k);
           const float4 a = __ldg(xv), c = __ldg(xv + 1);
 #pragma unroll
-          for (int r = 0; r < kGemvRows; ++r) {
-            float wf[8];
-            unpack8(wv[r], wf);
-            acc[r][si] += wf[0] * a.x + wf[1] * a.y + wf[2] * a.z + wf[3] * a.w + wf[4] * c.x +
-                          wf[5] * c.y + wf[6] * c.z + wf[7] * c.w;
-          }
+          for (int r = 0; r < kGemvRows; ++r)
+            acc[r][si] += wf[r][0] * a.x + wf[r][1] * a.y + wf[r][2] * a.z + wf[r][3] * a.w +
+                          wf[r][4] * c.x + wf[r][5] * c.y + wf[r][6] * c.z + wf[r][7] * c.w;
         }
       }
     }
@@ -336,11 +345,27 @@ cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int
                         int y_stride, int y_off, int act, cudaStream_t st) {
   if (S <= 0 || O <= 0) return cudaSuccess;
   const int warps = (O + kGemvRows - 1) / kGemvRows;
-  const int blocks = (warps + 7) / 8;
-  if (act == 1)
-    gemv_kernel<1><<<blocks, 256, 0, st>>>(W, b, x, S, K, O, y, y_stride, y_off);
-  else
-    gemv_kernel<0><<<blocks, 256, 0, st>>>(W, b, x, S, K, O, y, y_stride, y_off);
+  const int blocks = (warps + 3) / 4;
+  const int nch = K % 256 == 0 ? K / 256 : 0;
+  for (int s0 = 0; s0 < S; s0 += 4) {  // four samples per launch
+    const int sn = S - s0 < 4 ? S - s0 : 4;
+    const float* xs = x + (size_t)s0 * K;
+    float* ys = y + (size_t)s0 * y_stride;
+    switch (nch * 2 + (act == 1 ? 1 : 0)) {
+#define MF_GEMV_CASE(n)                                                                  \
+  case 2 * n:                                                                           \
+    gemv_kernel<0, n><<<blocks, 128, 0, st>>>(W, b, xs, sn, O, ys, y_stride, y_off);    \
+    break;                                                                              \
+  case 2 * n + 1:                                                                       \
+    gemv_kernel<1, n><<<blocks, 128, 0, st>>>(W, b, xs, sn, O, ys, y_stride, y_off);    \
+    break;
+      MF_GEMV_CASE(1) MF_GEMV_CASE(2) MF_GEMV_CASE(3) MF_GEMV_CASE(4) MF_GEMV_CASE(5) MF_GEMV_CASE(6)
+      MF_GEMV_CASE(7) MF_GEMV_CASE(8) MF_GEMV_CASE(9) MF_GEMV_CASE(10) MF_GEMV_CASE(11) MF_GEMV_CASE(12)
+      MF_GEMV_CASE(13) MF_GEMV_CASE(14) MF_GEMV_CASE(15) MF_GEMV_CASE(16)
+#undef MF_GEMV_CASE
+      default: return cudaErrorInvalidValue;  // K must be a multiple of 256, at most 4096
+    }
+  }
   return cudaGetLastError();
 }
 
