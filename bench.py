@@ -52,6 +52,24 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", 0))
 
 
+def rank_seeds(rank, n_packs=N_PACKS):
+    """Pack seeds of one rank: ranks never share a pack (weak scaling, no data exchange)."""
+    return [rank * n_packs + i for i in range(n_packs)]
+
+
+def combine_over_ranks(elapsed_s, tokens, dist=None, device="cpu"):
+    """Whole-job timing of a multi-rank run: the slowest rank's elapsed time and the tokens of
+    all ranks.  With no process group (one rank) the inputs come back unchanged."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return elapsed_s, tokens
+    import torch
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(n)
+    return float(t.item()), int(n.item())
+
+
 def config_dict(dims):
     return {"workload": "native-resolution pack, 16384-token budget, 8 seeded packs (first-fit over 64 "
                         "candidates each), 1 NR-MMDiT block + latent embed/final layer + flow loss",
@@ -175,8 +193,7 @@ def run_mageflow(args, rank, world, local_rank):
     d = model.dims
 
     packs = []
-    for i in range(N_PACKS):
-        seed = rank * N_PACKS + i
+    for seed in rank_seeds(rank):
         cands = synth.native_candidates(seed)
         plan = mf.mf_pack(cands, BUDGET)
         mf.mf_plan_upload(plan)
@@ -248,13 +265,7 @@ def run_mageflow(args, rank, world, local_rank):
     clocks = sampler.stop()
     mf.mf_check()
     elapsed = ev0.elapsed_time(ev1) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
-        n = torch.tensor([tokens], dtype=torch.float64, device=dev)
-        dist.all_reduce(n)
-        tokens = int(n.item())
+    elapsed, tokens = combine_over_ranks(elapsed, tokens, dist if world > 1 else None, dev)
 
     # ---- block-only timing (untraced): events around each block call
     block_ms, block_tok = 0.0, 0
