@@ -5,8 +5,8 @@ the packer), written from the method's description on the Mage-Flow pages:
 
 * "Mage-Flow: An Efficient Native-Resolution Foundation Model for Image Generation and
   Editing" - PaperReading review (obsidian blog), sections 2.2(2) native-resolution NR-MMDiT,
-  2.2(3) packed CFG and operator fusion, and 5 (concepts: rectified flow, MMDiT, native
-  resolution packing, CFG);
+  2.2(3) packed CFG and operator fusion, 2.2(4) the Diffusion-NFT objective, and 5 (concepts:
+  rectified flow, MMDiT, native resolution packing, CFG);
 * the hyper.ai summary of the same paper, sections 方法 (method) and 实验 (experiments).
 
 It works one sample at a time with no packing inside the math, so that the packed GPU result
@@ -15,8 +15,8 @@ bench's CPU-baseline leg may import it; the product path never does.  It shares 
 the CUDA library and does not import it.
 
 Parity status: the packer, RoPE, attention, LayerNorm, GELU, the timestep embedding, the
-block's residual structure, the interpolation, the loss, the Euler step and CFG are each
-pinned by tests against closed forms, invariants, brute force or hand-computed values.  The
+block's residual structure, the interpolation, the loss, the Diffusion-NFT loss, the Euler
+step and CFG are each pinned by tests against closed forms, invariants, brute force or hand-computed values.  The
 whole-model numbers (a full block with random weights) have no printed worked example on the
 pages: "parity unpinned" for the composed block beyond those structural pins.
 """

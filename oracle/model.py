@@ -15,6 +15,8 @@ Sources (page titles and sections):
 * [PR 5] same review, §5 concepts: MMDiT = separate projections and norms per modality with
   joint self-attention; rectified flow samples along the learned ODE from noise to data;
   CFG uses the difference of the conditional and unconditional predictions.
+* [PR 2.2(4)] same review, §2.2 (4): the Diffusion-NFT post-training objective
+  E[ r ||v+ - v||^2 + (1 - r) ||v- - v||^2 ] with a group-normalised reward r in [0, 1].
 * [HA 方法] hyper.ai summary, 方法 (method): the same loss and interpolation; a frame dimension
   added to the 2-D rotary embedding for editing.
 
@@ -231,6 +233,20 @@ def flow_loss(v, z, eps, target=None):
     if target is not None:
         d = d[target]
     return float((d * d).sum()), int(d.size)
+
+
+def nft_loss(v_pos, v_neg, z, eps, r, target=None):
+    """Diffusion-NFT objective of one sample [PR 2.2(4)]: (sum over its target elements of
+    r (v_pos - v*)^2 + (1 - r) (v_neg - v*)^2, element count), where v* = z - eps is the
+    flow-matching velocity target of [PR 2.2(2)] and r in [0, 1] is the sample's
+    group-normalised reward.  The pages do not say how the positive and negative policy
+    velocities v_pos, v_neg are formed; they are inputs here."""
+    v_star = f64(z) - f64(eps)
+    dp = f64(v_pos) - v_star
+    dn = f64(v_neg) - v_star
+    if target is not None:
+        dp, dn = dp[target], dn[target]
+    return float(r * (dp * dp).sum() + (1.0 - r) * (dn * dn).sum()), int(dp.size)
 
 
 def mean_loss(sums, counts):

@@ -336,6 +336,27 @@ def test_cfg_limits():
     np.testing.assert_array_equal(M.cfg_combine(vc, vu, 0.0), vu)
 
 
+def test_nft_loss_pins():
+    """Diffusion-NFT objective [PR 2.2(4)]: a hand-worked value, the reward limits (r = 1 is the
+    flow loss of v+, r = 0 that of v-), equal velocities reduce to the flow loss for any r,
+    linearity in r, and target-frame masking."""
+    z, e = np.array([1.0, 2.0]), np.array([0.5, -1.0])          # v* = z - eps = [0.5, 3]
+    vp, vn = np.array([1.0, 3.0]), np.array([0.0, 0.0])
+    # 0.25 * (0.5^2 + 0^2) + 0.75 * (0.5^2 + 3^2) = 0.0625 + 6.9375
+    assert M.nft_loss(vp, vn, z, e, 0.25) == (7.0, 2)
+    z, e = R.standard_normal((9, 5)), R.standard_normal((9, 5))
+    vp, vn = R.standard_normal((9, 5)), R.standard_normal((9, 5))
+    assert M.nft_loss(vp, vn, z, e, 1.0) == M.flow_loss(vp, z, e)
+    assert M.nft_loss(vp, vn, z, e, 0.0) == M.flow_loss(vn, z, e)
+    s, n = M.nft_loss(vp, vp, z, e, 0.37)
+    assert n == 45 and abs(s - M.flow_loss(vp, z, e)[0]) < 1e-12
+    s1, s0 = M.nft_loss(vp, vn, z, e, 1.0)[0], M.nft_loss(vp, vn, z, e, 0.0)[0]
+    assert abs(M.nft_loss(vp, vn, z, e, 0.6)[0] - (0.6 * s1 + 0.4 * s0)) < 1e-12
+    tgt = np.arange(9) >= 3
+    s, n = M.nft_loss(vp, vn, z, e, 0.6, tgt)
+    assert n == 30 and abs(s - M.nft_loss(vp[3:], vn[3:], z[3:], e[3:], 0.6)[0]) < 1e-12
+
+
 # ------------------------------------------------------------------ planted mistakes
 def _pins_pass():
     """A compact battery of the pins above, for the planted-mistake test."""
@@ -360,6 +381,7 @@ def _pins_pass():
         test_interpolation_endpoints_and_loss_zero()
         test_euler_straight_path()
         test_cfg_limits()
+        test_nft_loss_pins()
     except AssertionError:
         return False
     return True
@@ -367,7 +389,7 @@ def _pins_pass():
 
 ORIG = {n: getattr(M, n) for n in ("layer_norm", "gelu", "timestep_embedding", "rope_angles",
                                      "attention", "interpolate", "flow_loss", "euler_step",
-                                     "cfg_combine")}
+                                     "cfg_combine", "nft_loss")}
 
 
 def _mut_layer_norm(x, eps=M.LN_EPS):              # unbiased variance
@@ -397,6 +419,12 @@ MUTANTS = {
     "loss_sign": ("flow_loss", lambda v, z, e, target=None: ORIG["flow_loss"](v, e, z, target)),
     "euler_sign": ("euler_step", lambda z, v, dt: M.f64(z) - dt * M.f64(v)),
     "cfg_swapped": ("cfg_combine", lambda vc, vu, w: ORIG["cfg_combine"](vu, vc, w)),
+    "nft_reward_swapped": ("nft_loss", lambda vp, vn, z, e, r, target=None:
+                           ORIG["nft_loss"](vp, vn, z, e, 1.0 - r, target)),
+    "nft_target_sign": ("nft_loss", lambda vp, vn, z, e, r, target=None:
+                        ORIG["nft_loss"](vp, vn, e, z, r, target)),
+    "nft_no_negative_term": ("nft_loss", lambda vp, vn, z, e, r, target=None:
+                             ORIG["nft_loss"](vp, vp, z, e, 1.0, target)),
 }
 
 
