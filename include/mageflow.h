@@ -275,6 +275,21 @@ mf_status mf_flow_loss(const mf_plan* plan, int32_t channels, const float* d_z, 
                        const float* d_v, double* d_loss_sum, int64_t* d_count, double* d_mean,
                        void* d_ws, size_t ws_bytes, void* stream);
 
+/* Diffusion-NFT post-training objective [PR 2.2(4)]: per sample s with normalised reward
+ * r[s] in [0, 1], loss_sum[s] = sum over its target-frame image elements of
+ *   r[s] (v_pos - (z - eps))^2 + (1 - r[s]) (v_neg - (z - eps))^2        (f64),
+ * count[s] = number of those elements, mean[0] = sum_s loss_sum[s] / sum_s count[s].  The
+ * velocity target z - eps is the flow-matching target [PR 2.2(2)]; how the positive and
+ * negative policy velocities are formed is left to the caller (the pages do not say).
+ * d_z, d_eps, d_v_pos, d_v_neg: f32 [N_img][C]; d_reward: f32 [S] in pack order; outputs are
+ * device arrays; d_ws: workspace of mf_flow_loss_workspace_bytes() bytes.  Deterministic.
+ * Errors: MF_ERR_INVALID_ARG (null pointers, bad channels), MF_ERR_ALIGNMENT,
+ * MF_ERR_WORKSPACE, MF_ERR_NOT_UPLOADED, MF_ERR_CUDA. */
+mf_status mf_nft_loss(const mf_plan* plan, int32_t channels, const float* d_z, const float* d_eps,
+                      const float* d_v_pos, const float* d_v_neg, const float* d_reward,
+                      double* d_loss_sum, int64_t* d_count, double* d_mean, void* d_ws,
+                      size_t ws_bytes, void* stream);
+
 /* Image rows the scratch of mf_flow_loss_noalloc holds (8 bytes each, per device). */
 #define MF_NOALLOC_MAX_IMG_ROWS 65536
 

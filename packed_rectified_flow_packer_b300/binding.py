@@ -13,7 +13,7 @@ import os
 
 import numpy as np
 
-__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_attention", "mf_gemm", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
+__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_gemm", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmageflow.so")
 
@@ -99,6 +99,7 @@ _sigs = {
     "mf_flow_loss_workspace_bytes": (C.c_size_t, [_P]),
     "mf_flow_loss": (_S, [_P, C.c_int32, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "mf_flow_loss_noalloc": (_S, [_P, C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
+    "mf_nft_loss": (_S, [_P, C.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "mf_attention": (_S, [_P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P]),
     "mf_gemm": (_S, [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P, C.c_int32, _P]),
     "mf_check": (_S, [_P]),
@@ -292,6 +293,14 @@ def mf_flow_loss(plan: Plan, channels: int, z, eps, v, loss_sum, count, mean, ws
     nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     _ok(lib.mf_flow_loss(plan.handle, channels, _ptr(z), _ptr(eps), _ptr(v), _ptr(loss_sum),
                          _ptr(count), _ptr(mean), _ptr(ws), nbytes, _stream(stream)), "mf_flow_loss")
+
+
+def mf_nft_loss(plan: Plan, channels: int, z, eps, v_pos, v_neg, reward, loss_sum, count, mean, ws,
+                ws_bytes=None, stream=None):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _ok(lib.mf_nft_loss(plan.handle, channels, _ptr(z), _ptr(eps), _ptr(v_pos), _ptr(v_neg), _ptr(reward),
+                        _ptr(loss_sum), _ptr(count), _ptr(mean), _ptr(ws), nbytes, _stream(stream)),
+        "mf_nft_loss")
 
 
 NOALLOC_MAX_IMG_ROWS = 65536   # MF_NOALLOC_MAX_IMG_ROWS

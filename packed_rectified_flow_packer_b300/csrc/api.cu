@@ -671,6 +671,28 @@ extern "C" mf_status mf_flow_loss(const mf_plan* p, int32_t C, const float* d_z,
                                           static_cast<cudaStream_t>(stream)));
 }
 
+extern "C" mf_status mf_nft_loss(const mf_plan* p, int32_t C, const float* d_z, const float* d_eps,
+                                 const float* d_v_pos, const float* d_v_neg, const float* d_reward,
+                                 double* d_loss_sum, int64_t* d_count, double* d_mean, void* d_ws,
+                                 size_t ws_bytes, void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(check_latent_call(p, C, &di));
+  if (d_loss_sum == nullptr || d_count == nullptr || d_mean == nullptr) return MF_ERR_INVALID_ARG;
+  if (p->Ni > 0 && (d_z == nullptr || d_eps == nullptr || d_v_pos == nullptr || d_v_neg == nullptr ||
+                    d_reward == nullptr || d_ws == nullptr))
+    return MF_ERR_INVALID_ARG;
+  if (!aligned(d_z, 16) || !aligned(d_eps, 16) || !aligned(d_v_pos, 16) || !aligned(d_v_neg, 16) ||
+      !aligned(d_reward, 4) || !aligned(d_loss_sum, 8) || !aligned(d_count, 8) || !aligned(d_mean, 8) ||
+      !aligned(d_ws, 256))
+    return MF_ERR_ALIGNMENT;
+  if (ws_bytes < mf_flow_loss_workspace_bytes(p)) return MF_ERR_WORKSPACE;
+  Trace tr(MF_K_LOSS, static_cast<cudaStream_t>(stream), 0, (double)p->Ni * C * 16.0, 3);
+  return cuda_status(mf::launch_nft_loss(p->d_cui, p->d_img_seq, p->d_img_target, d_reward, p->S, p->Ni,
+                                         C, d_z, d_eps, d_v_pos, d_v_neg, static_cast<double*>(d_ws),
+                                         d_loss_sum, reinterpret_cast<long long*>(d_count), d_mean,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 // ====================================================================== building blocks
 extern "C" mf_status mf_attention(const mf_plan* p, int32_t heads, int32_t head_dim, const void* d_q,
                                   const void* d_k, const void* d_v, void* d_o, void* stream) {

@@ -273,6 +273,40 @@ __global__ void loss_row_kernel(const int* __restrict__ img_target, int Ni, int 
   if (lane == 0) ws[r] = acc;
 }
 
+// Diffusion-NFT objective, per image row: sum over channels of
+// r (v+ - (z - eps))^2 + (1 - r) (v- - (z - eps))^2 in f64 with the row's sample's reward r
+// (0 for source-frame rows).  The per-sample sums then take the flow loss's reductions.
+__global__ void nft_row_kernel(const int* __restrict__ img_seq, const int* __restrict__ img_target,
+                               const float* __restrict__ reward, int Ni, int C,
+                               const float* __restrict__ z, const float* __restrict__ eps,
+                               const float* __restrict__ vp, const float* __restrict__ vn,
+                               double* __restrict__ ws) {
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= Ni) return;
+  double acc = 0.0;
+  if (__ldg(img_target + r)) {
+    const double w = (double)__ldg(reward + __ldg(img_seq + r));
+    const size_t base = (size_t)r * C;
+    double sp = 0.0, sn = 0.0;
+    for (int c = lane * 4; c < C; c += 128) {
+      const float4 a = *reinterpret_cast<const float4*>(z + base + c);
+      const float4 e = *reinterpret_cast<const float4*>(eps + base + c);
+      const float4 p = *reinterpret_cast<const float4*>(vp + base + c);
+      const float4 n = *reinterpret_cast<const float4*>(vn + base + c);
+      const double t0 = (double)a.x - (double)e.x, t1 = (double)a.y - (double)e.y;
+      const double t2 = (double)a.z - (double)e.z, t3 = (double)a.w - (double)e.w;
+      const double p0 = (double)p.x - t0, p1 = (double)p.y - t1, p2 = (double)p.z - t2, p3 = (double)p.w - t3;
+      const double n0 = (double)n.x - t0, n1 = (double)n.y - t1, n2 = (double)n.z - t2, n3 = (double)n.w - t3;
+      sp += p0 * p0 + p1 * p1 + p2 * p2 + p3 * p3;
+      sn += n0 * n0 + n1 * n1 + n2 * n2 + n3 * n3;
+    }
+    acc = w * sp + (1.0 - w) * sn;
+  }
+  acc = warp_sum_d(acc);
+  if (lane == 0) ws[r] = acc;
+}
+
 // one block per sample, fixed reduction order
 __global__ void loss_seq_kernel(const int* __restrict__ cu_img, const int* __restrict__ img_target,
                                 int C, const double* __restrict__ ws, double* __restrict__ loss_sum,
@@ -414,6 +448,17 @@ cudaError_t launch_flow_loss(const int* cu_img, const int* img_target, int S, in
                              const float* z, const float* eps, const float* v, double* ws,
                              double* loss_sum, long long* count, double* mean, cudaStream_t st) {
   if (Ni > 0) loss_row_kernel<<<(Ni + 7) / 8, 256, 0, st>>>(img_target, Ni, C, z, eps, v, ws);
+  if (S > 0) loss_seq_kernel<<<S, 256, 0, st>>>(cu_img, img_target, C, ws, loss_sum, count);
+  loss_mean_kernel<<<1, 32, 0, st>>>(S, loss_sum, count, mean);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nft_loss(const int* cu_img, const int* img_seq, const int* img_target,
+                            const float* reward, int S, int Ni, int C, const float* z,
+                            const float* eps, const float* vp, const float* vn, double* ws,
+                            double* loss_sum, long long* count, double* mean, cudaStream_t st) {
+  if (Ni > 0)
+    nft_row_kernel<<<(Ni + 7) / 8, 256, 0, st>>>(img_seq, img_target, reward, Ni, C, z, eps, vp, vn, ws);
   if (S > 0) loss_seq_kernel<<<S, 256, 0, st>>>(cu_img, img_target, C, ws, loss_sum, count);
   loss_mean_kernel<<<1, 32, 0, st>>>(S, loss_sum, count, mean);
   return cudaGetLastError();

@@ -44,6 +44,11 @@ cudaError_t launch_euler(int Ni, int C, float dt, const float* v, float* z, bf16
 cudaError_t launch_flow_loss(const int* cu_img, const int* img_target, int S, int Ni, int C,
                              const float* z, const float* eps, const float* v, double* ws,
                              double* loss_sum, long long* count, double* mean, cudaStream_t st);
+// Diffusion-NFT loss: per-row weighted sums, then the flow loss's per-sample and mean passes.
+cudaError_t launch_nft_loss(const int* cu_img, const int* img_seq, const int* img_target,
+                            const float* reward, int S, int Ni, int C, const float* z,
+                            const float* eps, const float* vp, const float* vn, double* ws,
+                            double* loss_sum, long long* count, double* mean, cudaStream_t st);
 cudaError_t launch_timeout_selftest(unsigned* status, unsigned long long limit_ns,
                                     cudaStream_t st);
 

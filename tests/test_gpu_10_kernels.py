@@ -167,3 +167,41 @@ def test_rectified_flow_epilogues(C):
     ls2 = torch.zeros_like(ls)
     mf.mf_flow_loss(plan, C, Z, E, V, ls2, cnt, mean, ws)
     assert torch.equal(ls, ls2)
+
+
+@pytest.mark.parametrize("case", ["mixed", "native16k"])
+def test_nft_loss(case):
+    """Diffusion-NFT objective against the oracle, per sample: edit source frames excluded,
+    rewards at the endpoints 0 and 1 and inside; sums to 1e-12 relative, counts exact."""
+    if case == "mixed":
+        samples, ref, plan = _latent_case()
+        C = 64
+    else:
+        samples = synth.native_candidates(0)
+        ref = opack.build_plan(samples, 16384)
+        plan = mf.mf_pack(samples, 16384)
+        mf.mf_plan_upload(plan)
+        C = 128
+    Ni, S = ref.n_img, ref.n_seq
+    g = np.random.default_rng(11 + C)
+    z, e, vp, vn = (g.standard_normal((Ni, C)).astype(np.float32) for _ in range(4))
+    r = g.uniform(0.0, 1.0, S).astype(np.float32)
+    r[0] = 1.0
+    if S > 1:
+        r[1] = 0.0
+    ls = torch.zeros(S, dtype=torch.float64, device="cuda")
+    cnt = torch.zeros(S, dtype=torch.int64, device="cuda")
+    mean = torch.zeros(1, dtype=torch.float64, device="cuda")
+    ws = torch.empty(mf.mf_flow_loss_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
+    mf.mf_nft_loss(plan, C, to_f32(z), to_f32(e), to_f32(vp), to_f32(vn), to_f32(r), ls, cnt, mean, ws)
+    mf.mf_check()
+    sums, counts = [], []
+    for k, cidx in enumerate(ref.order):
+        a, b = ref.cu_img[k], ref.cu_img[k + 1]
+        sm, n = M.nft_loss(vp[a:b], vn[a:b], z[a:b], e[a:b], float(r[k]), M.target_mask(samples[cidx]))
+        sums.append(sm)
+        counts.append(n)
+    np.testing.assert_allclose(ls.cpu().numpy(), sums, rtol=1e-12)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), counts)
+    want = M.mean_loss(sums, counts)
+    assert abs(mean.item() - want) <= 1e-12 * abs(want)
