@@ -376,6 +376,12 @@ typedef struct {
  * concurrent library calls on other threads. */
 mf_status mf_trace_enable(int32_t on);
 
+/* Which kinds are bracketed while tracing is on: bit k of `mask` selects mf_kernel_kind k
+ * (all kinds by default).  Launches of other kinds are still counted by mf_launch_count but
+ * get no events, so a measured region can time one kernel kind without adding event records
+ * around every other launch. */
+mf_status mf_trace_kinds(uint32_t mask);
+
 /* Waits for the recorded events, writes one entry per mf_kernel_kind (n >= MF_K_COUNT) and
  * clears the records.  Errors: MF_ERR_INVALID_ARG, MF_ERR_CUDA. */
 mf_status mf_trace_read(mf_trace_entry* entries, int32_t n);

@@ -13,7 +13,7 @@ import os
 
 import numpy as np
 
-__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_gemm", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
+__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_gemm", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmageflow.so")
 
@@ -105,6 +105,7 @@ _sigs = {
     "mf_check": (_S, [_P]),
     "mf_selftest_timeout": (_S, [C.c_int32, _P]),
     "mf_trace_enable": (_S, [C.c_int32]),
+    "mf_trace_kinds": (_S, [C.c_uint32]),
     "mf_trace_read": (_S, [C.POINTER(mf_trace_entry), C.c_int32]),
     "mf_launch_count": (C.c_int64, []),
 }
@@ -344,6 +345,12 @@ def mf_version() -> int:
 # ------------------------------------------------------------------ tracing
 def mf_trace_enable(on: bool = True):
     _ok(lib.mf_trace_enable(1 if on else 0), "mf_trace_enable")
+
+
+def mf_trace_kinds(kinds=None):
+    """Restrict tracing to the given kind names (KERNEL_KINDS); None traces every kind."""
+    mask = 0xFFFFFFFF if kinds is None else sum(1 << KERNEL_KINDS.index(k) for k in kinds)
+    _ok(lib.mf_trace_kinds(mask), "mf_trace_kinds")
 
 
 def mf_trace_read() -> dict:

@@ -74,6 +74,7 @@ struct TraceRec {
 
 struct TraceState {
   bool on = false;
+  uint32_t mask = 0xffffffffu;  // kinds that are bracketed while tracing is on
   std::vector<TraceRec> recs;
   std::vector<cudaEvent_t> pool;
 };
@@ -98,7 +99,7 @@ class Trace {
   Trace(int kind, cudaStream_t st, double flops, double bytes, int nk) : st_(st) {
     g_launches += nk;
     std::lock_guard<std::mutex> lk(g_trace_mu);
-    if (!g_trace.on) return;
+    if (!g_trace.on || ((g_trace.mask >> kind) & 1u) == 0) return;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
     rec_ = TraceRec{kind, trace_event(), trace_event(), flops, bytes, nk};
@@ -769,6 +770,12 @@ extern "C" mf_status mf_selftest_timeout(int32_t limit_us, void* stream) {
 }
 
 // ====================================================================== tracing
+extern "C" mf_status mf_trace_kinds(uint32_t mask) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace.mask = mask;
+  return MF_OK;
+}
+
 extern "C" mf_status mf_trace_enable(int32_t on) {
   std::lock_guard<std::mutex> lk(g_trace_mu);
   g_trace.on = on != 0;
