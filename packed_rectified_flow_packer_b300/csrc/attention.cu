@@ -10,9 +10,10 @@
 // One CTA per work item, 320 threads.  The 256 query rows are two 128-row tiles t = 0, 1,
 // each with its own softmax warpgroup, so the tensor core works on one tile while the other
 // tile's exponentials run:
-//   warp 0 lane 0 : TMA producer: Q_0 and Q_1 once, then K_0, V_0, K_1, V_1, ... into one
+//   warp 0        : TMA producer: Q_0 and Q_1 once, then K_0, V_0, K_1, V_1, ... into one
 //                   shared-memory ring, in the order the tensor core consumes them.
-//   warp 1        : TMEM allocator; lane 0 issues tcgen05.mma in the order
+//   warp 1        : TMEM allocator and MMA issuer (the whole warp runs the loop, one elected
+//                   lane issues) of tcgen05.mma in the order
 //                   S_0 = Q_0 K_0^T, S_1 = Q_1 K_0^T, then per key tile j
 //                   O_0 += P_0 V_j, S_0 = Q_0 K_{j+1}^T, O_1 += P_1 V_j, S_1 = Q_1 K_{j+1}^T.
 //   warps 2..5    : softmax of tile 0, warps 6..9: softmax of tile 1; one thread per query
@@ -73,14 +74,15 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
 }
 
-// O_t += P_t V: A operand (P, 128 x 16 bf16 per instruction) read from TMEM.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
+// O_t += P_t V: A operand (P, 128 x 16 bf16 per instruction) read from TMEM; issued by the
+// lane whose `pred` is nonzero.
+__device__ __forceinline__ void mma_bf16_ts_if(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem,
+                                               uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
       : "memory");
 }
 
@@ -148,101 +150,116 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
+    // The whole warp runs the loop (warp-uniform state); one elected lane issues.
+    const uint32_t el = elect_one();
+    if (el) {
       tma_prefetch_desc(&p.tmK);
       tma_prefetch_desc(&p.tmV);
-      bool ok = true;
-      uint32_t armed = 0, armed_par = 0;  // bit s: ring slot s has a copy in flight; its parity
       mbar_arrive_expect_tx(&q_full, n_t * L::Q);
       for (int t = 0; t < n_t; ++t)
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
           tma_load_2d(smem + L::off_q + t * L::Q + a * kAtom, &p.tmQ, h * D + a * 64, q0 + t * kT,
                       &q_full);
-      // ring order = consumption order of the tensor core: K_0, V_0, K_1, V_1, ...
-      for (int idx = 0; ok && idx < 2 * n_kv; ++idx) {
-        const int st = idx % NS;
-        const uint32_t ph = (idx / NS) & 1;
-        if (!mbar_wait(&kv_empty[st], ph ^ 1, lim) || *(volatile int*)&abort_flag) {
-          ok = false;
-          break;
-        }
+    }
+    __syncwarp();
+    bool ok = true;
+    uint32_t armed = 0, armed_par = 0;  // bit s: ring slot s has a copy in flight; its parity
+    // ring order = consumption order of the tensor core: K_0, V_0, K_1, V_1, ...
+    for (int idx = 0; ok && idx < 2 * n_kv; ++idx) {
+      const int st = idx % NS;
+      const uint32_t ph = (idx / NS) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&kv_empty[st], ph ^ 1, lim)) ||
+          __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (el) {
         const CUtensorMap* tm = (idx & 1) ? &p.tmV : &p.tmK;
         mbar_arrive_expect_tx(&kv_full[st], L::KV);
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
           tma_load_2d(smem + L::off_kv + st * L::KV + a * kAtom, tm, h * D + a * 64,
                       kv0 + (idx >> 1) * kT, &kv_full[st]);
-        armed |= 1u << st;
-        armed_par = (armed_par & ~(1u << st)) | (ph << st);
       }
-      if (!ok) {
+      __syncwarp();
+      armed |= 1u << st;
+      armed_par = (armed_par & ~(1u << st)) | (ph << st);
+    }
+    if (!ok) {
+      if (el) {
         *(volatile int*)&abort_flag = 1;
         report_status(p.status, kStatusTimeout);
-        mbar_wait(&q_full, 0, lim);  // let this thread's copies land before exiting
-        for (int s = 0; s < NS; ++s)
-          if (armed & (1u << s)) mbar_wait(&kv_full[s], (armed_par >> s) & 1u, lim);
       }
+      mbar_wait(&q_full, 0, lim);  // let this warp's copies land before exiting
+      for (int s2 = 0; s2 < NS; ++s2)
+        if (armed & (1u << s2)) mbar_wait(&kv_full[s2], (armed_par >> s2) & 1u, lim);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    // Waits are ordered by criticality: P_t first, then the ring slot (whose copy normally
-    // landed long ago).  Shared-memory descriptors are built once and advanced by constants.
-    if (lane == 0) {
-      const uint64_t qd = sdesc_sw128(smem_u32(smem + L::off_q), 16, 1024);
-      const uint64_t kv0d = sdesc_sw128(smem_u32(smem + L::off_kv), 16, 1024);
-      const uint64_t vv0d = sdesc_sw128(smem_u32(smem + L::off_kv), kAtom, 1024);
-      auto issue_s = [&](int t, int slot) {
-        const uint64_t kd = kv0d + ((slot * L::KV) >> 4);
+    // The whole warp runs the loop (warp-uniform state and descriptors); one elected lane
+    // issues each MMA and commit.  Waits are ordered by criticality: P_t first, then the ring
+    // slot (whose copy normally landed long ago).
+    const uint32_t el = elect_one();
+    const uint64_t qd = sdesc_sw128(smem_u32(smem + L::off_q), 16, 1024);
+    const uint64_t kv0d = sdesc_sw128(smem_u32(smem + L::off_kv), 16, 1024);
+    const uint64_t vv0d = sdesc_sw128(smem_u32(smem + L::off_kv), kAtom, 1024);
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, lim));
+    };
+    auto issue_s = [&](int t, int slot) {
+      const uint64_t kd = kv0d + ((slot * L::KV) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = ((kk >> 2) * kAtom + (kk & 3) * 32) >> 4;
-          mma_bf16(tmem_base + t * kT, qd + ((t * L::Q) >> 4) + o, kd + o, IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[t]);
-      };
-      auto slot_wait = [&](int idx) -> bool { return mbar_wait(&kv_full[idx % NS], (idx / NS) & 1, lim); };
-      bool ok = mbar_wait(&q_full, 0, lim) && slot_wait(0);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < n_t; ++t) issue_s(t, 0);
-        mma_commit(&kv_empty[0]);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t o = ((kk >> 2) * kAtom + (kk & 3) * 32) >> 4;
+        mma_bf16_if(el, tmem_base + t * kT, qd + ((t * L::Q) >> 4) + o, kd + o, IDESC_S, kk > 0 ? 1u : 0u);
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int iv = 2 * j + 1, ik = 2 * j + 2;
-        const bool next = j + 1 < n_kv;
-        const uint64_t vd = vv0d + (((iv % NS) * L::KV) >> 4);
-        for (int t = 0; t < n_t; ++t) {
-          if (!mbar_wait(&p_full[t], j & 1, lim) || (t == 0 && !slot_wait(iv))) {
+      mma_commit_if(el, &s_full[t]);
+    };
+    auto slot_wait = [&](int idx) -> bool { return wait_all(&kv_full[idx % NS], (idx / NS) & 1); };
+    bool ok = wait_all(&q_full, 0) && slot_wait(0);
+    if (ok) {
+      tc_fence_after();
+      for (int t = 0; t < n_t; ++t) issue_s(t, 0);
+      mma_commit_if(el, &kv_empty[0]);
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int iv = 2 * j + 1, ik = 2 * j + 2;
+      const bool next = j + 1 < n_kv;
+      const uint64_t vd = vv0d + (((iv % NS) * L::KV) >> 4);
+      for (int t = 0; t < n_t; ++t) {
+        if (!wait_all(&p_full[t], j & 1) || (t == 0 && !slot_wait(iv))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_bf16_ts_if(el, tmem_base + O_COL + t * D, tmem_base + t * kT + kk * 8, vd + ((kk * 2048) >> 4),
+                         IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        if (next) {
+          if (t == 0 && !slot_wait(ik)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_bf16_ts(tmem_base + O_COL + t * D, tmem_base + t * kT + kk * 8, vd + ((kk * 2048) >> 4),
-                        IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-          if (next) {
-            if (t == 0 && !slot_wait(ik)) {
-              ok = false;
-              break;
-            }
-            issue_s(t, ik % NS);
-          }
+          issue_s(t, ik % NS);
         }
-        if (!ok) break;
-        mma_commit(&kv_empty[iv % NS]);
-        if (next) mma_commit(&kv_empty[ik % NS]);
       }
-      if (ok) {
-        for (int t = 0; t < n_t; ++t) mma_commit(&o_done[t]);
-      } else {
+      if (!ok) break;
+      mma_commit_if(el, &kv_empty[iv % NS]);
+      if (next) mma_commit_if(el, &kv_empty[ik % NS]);
+    }
+    if (ok) {
+      for (int t = 0; t < n_t; ++t) mma_commit_if(el, &o_done[t]);
+    } else {
+      if (el) {
         *(volatile int*)&abort_flag = 1;
         report_status(p.status, kStatusTimeout);
-        mma_commit(&drain_bar);  // wait for this thread's MMAs before TMEM is freed
-        mbar_wait(&drain_bar, 0, lim);
+        mma_commit(&drain_bar);  // wait for this warp's MMAs before TMEM is freed
       }
+      __syncwarp();
+      mbar_wait(&drain_bar, 0, lim);
     }
     __syncwarp();
   } else {

@@ -131,6 +131,115 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const GemmPr
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Staged epilogue of the CTA-pair kernel.  A warp owns 32 accumulator rows (its TMEM lane
+// quarter) and moves them 16 columns at a time.  Phase 1, one thread per row: bias, then GELU
+// or RoPE, in f32, written to the warp's staging rows in shared memory.  Phase 2, two threads
+// per row, 8 columns each: the last operation (gated residual, scatter to joint order) and the
+// global store, so each store instruction writes whole 32-byte sectors of 16 rows instead of
+// 16 bytes of 32 rows (stores of that shape held back the tensor core's issue).
+constexpr int kStageRow = 20;  // floats per staged row (16 + 4 padding: conflict-free 16-byte writes)
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_reg_fence16(uint32_t (&r)[16]) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+               "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+               "+r"(r[14]), "+r"(r[15]));
+}
+
+// Phase 1: 16 columns of one row, in place.
+template <int EPI>
+__device__ __forceinline__ void epi_row16(const GemmParams& p, const GemmProblem& pr, int row, int col0,
+                                          float (&v)[16], const float* rope_inv, const int* rope_axis) {
+  if (row >= pr.M || col0 >= pr.N) return;
+  if (pr.bias != nullptr) {
+    const uint4* b = reinterpret_cast<const uint4*>(pr.bias + col0);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 u = __ldg(b + i);
+      const float2 f0 = unpack_bf16x2(u.x), f1 = unpack_bf16x2(u.y), f2 = unpack_bf16x2(u.z),
+                   f3 = unpack_bf16x2(u.w);
+      v[8 * i + 0] += f0.x; v[8 * i + 1] += f0.y; v[8 * i + 2] += f1.x; v[8 * i + 3] += f1.y;
+      v[8 * i + 4] += f2.x; v[8 * i + 5] += f2.y; v[8 * i + 6] += f3.x; v[8 * i + 7] += f3.y;
+    }
+  }
+  if constexpr (EPI == kEpiGelu) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.7071067811865476f));
+  } else if constexpr (EPI == kEpiQkvRope) {
+    const int which = col0 / p.H;
+    if (which < 2) {
+      const int joint = __ldg(p.srow_joint + pr.row_off + row);
+      const int* ps = p.pos + (size_t)joint * 3;
+      const float pf = (float)__ldg(ps), pr_ = (float)__ldg(ps + 1), pc = (float)__ldg(ps + 2);
+      const int g0 = ((col0 - which * p.H) % p.head_dim) >> 1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int ax = rope_axis[g0 + i];
+        const float th = (ax == 0 ? pf : (ax == 1 ? pr_ : pc)) * rope_inv[g0 + i];
+        // |th| <= max position (a few hundred): reduce modulo 2 pi with a two-constant
+        // Cody-Waite step (2 pi = kHi + kLo), then the hardware sine / cosine on [-pi, pi]
+        const float kq = rintf(th * 0.15915494309189535f);
+        const float rr = fmaf(-kq, -1.7484555314695172e-07f, fmaf(-kq, 6.2831854820251465f, th));
+        float sn, cs;
+        __sincosf(rr, &sn, &cs);
+        const float x0 = v[2 * i], x1 = v[2 * i + 1];
+        v[2 * i] = x0 * cs - x1 * sn;
+        v[2 * i + 1] = x0 * sn + x1 * cs;
+      }
+    }
+  }
+}
+
+// Phase 2: 8 columns of one row to global memory.
+template <int EPI>
+__device__ __forceinline__ void epi_store8(const GemmParams& p, const GemmProblem& pr, int row, int col,
+                                           const float4& a, const float4& b) {
+  if (row >= pr.M || col >= pr.N) return;
+  if constexpr (EPI == kEpiBiasF32) {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(pr.out) + (size_t)row * pr.ldo + col);
+    o[0] = a;
+    o[1] = b;
+    return;
+  }
+  float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  bf16* dst;
+  if constexpr (EPI == kEpiQkvRope) {
+    const int joint = __ldg(p.srow_joint + pr.row_off + row);
+    const int which = col / p.H;
+    dst = (which == 0 ? p.q : (which == 1 ? p.k : p.v)) + (size_t)joint * p.H + (col - which * p.H);
+  } else {
+    dst = static_cast<bf16*>(pr.out) + (size_t)row * pr.ldo + col;
+  }
+  if constexpr (EPI == kEpiGateResid) {
+    const int seq = __ldg(p.srow_seq + pr.row_off + row);
+    const float4* g = reinterpret_cast<const float4*>(
+        p.mod + ((size_t)seq * 2 + pr.stream) * 6 * (size_t)p.H + p.gate_off + col);
+    const float4 ga = __ldg(g), gb = __ldg(g + 1);
+    const uint4 u = *reinterpret_cast<const uint4*>(dst);
+    const float2 x0 = unpack_bf16x2(u.x), x1 = unpack_bf16x2(u.y), x2 = unpack_bf16x2(u.z),
+                 x3 = unpack_bf16x2(u.w);
+    v[0] = fmaf(ga.x, v[0], x0.x); v[1] = fmaf(ga.y, v[1], x0.y);
+    v[2] = fmaf(ga.z, v[2], x1.x); v[3] = fmaf(ga.w, v[3], x1.y);
+    v[4] = fmaf(gb.x, v[4], x2.x); v[5] = fmaf(gb.y, v[5], x2.y);
+    v[6] = fmaf(gb.z, v[6], x3.x); v[7] = fmaf(gb.w, v[7], x3.y);
+  }
+  uint4 w;
+  w.x = pack_bf16x2(v[0], v[1]);
+  w.y = pack_bf16x2(v[2], v[3]);
+  w.z = pack_bf16x2(v[4], v[5]);
+  w.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(dst) = w;
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(192, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr int STAGES = (BN == 256) ? 4 : 6;
@@ -337,8 +446,9 @@ constexpr int kPairThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 // MMA thread issues for the pair and its commits arrive on the barriers of both CTAs
 // (multicast), so each CTA's producer sees its own stage freed and each CTA's epilogue sees
 // its own 128 accumulator rows (TMEM lanes) ready.  Eight epilogue warps per CTA, two per TMEM
-// lane quarter, each take 128 of the tile's 256 columns; the epilogue warps of both CTAs
-// release an accumulator buffer by arriving on the even CTA's barrier.
+// lane quarter, each take 128 of the tile's 256 columns through the staged epilogue above; the
+// epilogue warps of both CTAs release an accumulator buffer by arriving on the even CTA's
+// barrier.
 template <int EPI>
 __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   constexpr int STAGES = 6;
@@ -407,71 +517,89 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      bool ok = true;
-      for (int tile = pair; ok && tile < total; tile += n_pairs) {
-        int pi, m, n;
-        decode_tile(p, tile, pi, m, n);
-        const int nkb = p.prob[pi].K / kBK;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1, lim) || *(volatile int*)&abort_flag) {
-            ok = false;
-            break;
-          }
+    const uint32_t el = elect_one();
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int tile = pair; ok && tile < total; tile += n_pairs) {
+      int pi, m, n;
+      decode_tile(p, tile, pi, m, n);
+      const int nkb = p.prob[pi].K / kBK;
+      // the pair's next tile: its panels are prefetched into L2 one k-block per load of this
+      // tile, so a pair's first k-blocks of a new tile find their operands in L2
+      const bool has_next = tile + n_pairs < total;
+      int pi2 = 0, m2 = 0, n2 = 0;
+      if (has_next) decode_tile(p, tile + n_pairs, pi2, m2, n2);
+      const int nkb2 = has_next ? p.prob[pi2].K / kBK : 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1, lim)) ||
+            __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (el) {
           uint8_t* sa = smem + stage * STAGE_BYTES;
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * STAGE_BYTES);
           const uint32_t fb = mapa_shared(&full_bar[stage], 0);
           tma_load_2d_pair(sa, &p.tmA[pi], kb * kBK, m * 2 * kBM + rank * kBM, fb);
           tma_load_2d_pair(sa + A_BYTES, &p.tmB[pi], kb * kBK, n * BN + rank * (BN / 2), fb);
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          if (kb < nkb2) {
+            tma_prefetch_l2_2d(&p.tmA[pi2], kb * kBK, m2 * 2 * kBM + rank * kBM);
+            tma_prefetch_l2_2d(&p.tmB[pi2], kb * kBK, n2 * BN + rank * (BN / 2));
+          }
         }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
-      if (!ok) {
-        *(volatile int*)&abort_flag = 1;
-        report_status(p.status, kStatusTimeout);
-      }
+    }
+    if (!ok && el) {
+      *(volatile int*)&abort_flag = 1;
+      report_status(p.status, kStatusTimeout);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (even CTA)
-    if (leader && lane == 0) {
+    // The whole warp runs the loop; one elected lane issues each MMA and commit.
+    if (leader) {
+      const uint32_t el = elect_one();
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < total; tile += n_pairs) {
         int pi, m, n;
         decode_tile(p, tile, pi, m, n);
         const int nkb = p.prob[pi].K / kBK;
-        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, lim) || *(volatile int*)&abort_flag) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&tempty_bar[acc], acc_phase ^ 1, lim)) ||
+            __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, lim)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase, lim))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t b0 = a0 + A_BYTES;
+          const uint64_t ad = sdesc_sw128(smem_u32(smem + stage * STAGE_BYTES), 16, 1024);
+          const uint64_t bd = ad + (A_BYTES >> 4);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_pair(d_tmem, sdesc_sw128(a0 + k * 32, 16, 1024), sdesc_sw128(b0 + k * 32, 16, 1024),
-                          IDESC, (kb | k) != 0 ? 1u : 0u);
-          mma_commit_pair_mc(&empty_bar[stage], 0x3);
+            mma_bf16_pair_if(el, d_tmem, ad + k * 2, bd + k * 2, IDESC, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair_mc_if(el, &empty_bar[stage], 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        mma_commit_pair_mc(&tfull_bar[acc], 0x3);
+        mma_commit_pair_mc_if(el, &tfull_bar[acc], 0x3);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
       if (!ok) {
-        *(volatile int*)&abort_flag = 1;
-        report_status(p.status, kStatusTimeout);
-        mma_commit_pair_mc(&drain_bar, 0x1);  // wait for this thread's MMAs before TMEM is freed
+        if (el) {
+          *(volatile int*)&abort_flag = 1;
+          report_status(p.status, kStatusTimeout);
+          mma_commit_pair_mc(&drain_bar, 0x1);  // wait for this warp's MMAs before TMEM is freed
+        }
+        __syncwarp();
         mbar_wait(&drain_bar, 0, lim);
       }
     }
@@ -495,14 +623,29 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
       }
       tc_fence_after();
       const GemmProblem& pr = p.prob[pi];
-      const int row = m * 2 * kBM + rank * kBM + q * 32 + lane;
+      const int row0 = m * 2 * kBM + rank * kBM + q * 32;  // first of this warp's 32 rows
+      float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES) + (warp - 2) * 32 * kStageRow;
 #pragma unroll 1
-      for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tmem_base, q * 32, acc * BN + c), r);
+      for (int c = c_lo; c < c_lo + BN / 2; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem_addr(tmem_base, q * 32, acc * BN + c), r);
         tmem_ld_wait();
-        tmem_reg_fence(r);
-        epilogue_chunk<EPI>(p, pr, row, n * BN + c, r, rope_inv, rope_axis);
+        tmem_reg_fence16(r);
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+        epi_row16<EPI>(p, pr, row0 + lane, n * BN + c, v, rope_inv, rope_axis);
+        float4* sp = reinterpret_cast<float4*>(stg + lane * kStageRow);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sp[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {  // rows 16 it .. 16 it + 15, two threads per row
+          const int rr = 16 * it + (lane >> 1), hh = lane & 1;
+          const float4* rp = reinterpret_cast<const float4*>(stg + rr * kStageRow + hh * 8);
+          epi_store8<EPI>(p, pr, row0 + rr, n * BN + c + hh * 8, rp[0], rp[1]);
+        }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
@@ -523,7 +666,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
 template <int EPI>
 cudaError_t launch_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
   constexpr int STAGES = 6;
-  const int smem = STAGES * (kBM * kBK * 2 + 128 * kBK * 2) + 1024;
+  const int smem = STAGES * (kBM * kBK * 2 + 128 * kBK * 2) + 8 * 32 * kStageRow * 4 + 1024;
   auto kern = gemm_pair_kernel<EPI>;
   static int max_pairs = 0;  // clusters of two that fit on the device at once (per instantiation)
   cudaLaunchAttribute attr[1];
