@@ -272,6 +272,9 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
     p.prob[i].out = g.out;
     p.tiles_m[i] = pair ? (g.M + 255) / 256 : (g.M + 127) / 128;
     p.tiles_n[i] = (g.N + BN - 1) / BN;
+    // N fastest when a wave of tiles spans whole rows of N tiles (few N tiles: the weight
+    // matrix then stays in L2); otherwise sweep N over groups of 16 row tiles
+    p.group_m[i] = p.tiles_n[i] <= 16 ? 0 : 16;
     begin += p.tiles_m[i] * p.tiles_n[i];
     p.tile_begin[i + 1] = begin;
     p.n_prob++;

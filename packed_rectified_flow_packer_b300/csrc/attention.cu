@@ -346,27 +346,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], 0, lim));
         if (ok) {
           tc_fence_after();
+          // O / l in bf16 through this tile's Q buffer (free once o_done[t] fired: every MMA of
+          // tile t has completed): each warp stages its 32 rows, 16-byte chunks XOR-swizzled by
+          // row, then writes whole rows (D bf16 each) with consecutive lanes on consecutive
+          // 16-byte chunks of a row
           const float inv_l = 1.0f / l;
-          const int qrow = q0 + t * kT + row;
-          const bool valid = qrow < kv0 + len;
-          bf16* dst = valid ? p.out + (size_t)__ldg(p.joint_srow + qrow) * p.H + h * D : nullptr;
+          uint8_t* stg = smem + L::off_q + t * L::Q;   // [128 rows][D bf16]
+          constexpr int kChunks = D / 8;               // 16-byte chunks per row
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t r[32];
             tmem_ld32(lane_base + o_col + cc * 32, r);
             tmem_ld_wait();
             tmem_reg_fence(r);
-            if (valid) {
-              uint4* o = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint4 w;
-                w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
-                w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
-                w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
-                w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
-                o[i] = w;
-              }
+            for (int i = 0; i < 4; ++i) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+              const int ch = cc * 4 + i;
+              *reinterpret_cast<uint4*>(stg + row * (D * 2) + ((ch ^ (row & 7)) << 4)) = w;
+            }
+          }
+          __syncwarp();
+          constexpr int kRowsPerStore = 32 / kChunks;  // rows one warp-wide store covers
+#pragma unroll 1
+          for (int r0 = 0; r0 < 32; r0 += kRowsPerStore) {
+            const int rr = qw * 32 + r0 + lane / kChunks, ch = lane % kChunks;
+            const int qrow = q0 + t * kT + rr;
+            if (qrow < kv0 + len) {
+              const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * (D * 2) + ((ch ^ (rr & 7)) << 4));
+              bf16* dst = p.out + (size_t)__ldg(p.joint_srow + qrow) * p.H + h * D;
+              reinterpret_cast<uint4*>(dst)[ch] = w;
             }
           }
         }

@@ -17,17 +17,29 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kGroupM = 16;  // tile rasterisation: 16 row tiles share a sweep over N
 
+// Tile order, chosen per problem on the host (GemmParams::group_m):
+//  * group_m == 0, N fastest: for few N tiles (out-proj, MLP-down).  The tiles running at the
+//    same time cover every N tile of a few row panels, so each A k-slice serves all of them
+//    from L2 and the weight matrix stays resident in L2 from one row panel to the next.
+//  * group_m > 0: group_m row tiles fastest, then N (QKV, MLP-up).  With many N tiles the
+//    wide output streaming through L2 would evict a resident weight matrix; sweeping N for a
+//    fixed group of row panels keeps those A panels in L2 instead.
 __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& pi, int& m,
                                             int& n) {
   pi = (p.n_prob > 1 && tile >= p.tile_begin[1]) ? 1 : 0;
   const int t = tile - p.tile_begin[pi];
   const int tn = p.tiles_n[pi], tm = p.tiles_m[pi];
-  const int group = t / (kGroupM * tn);
-  const int first_m = group * kGroupM;
-  const int gm = min(kGroupM, tm - first_m);
-  const int local = t - group * kGroupM * tn;
+  const int gmax = p.group_m[pi];
+  if (gmax == 0) {
+    m = t / tn;
+    n = t - m * tn;
+    return;
+  }
+  const int group = t / (gmax * tn);
+  const int first_m = group * gmax;
+  const int gm = min(gmax, tm - first_m);
+  const int local = t - group * gmax * tn;
   m = first_m + local % gm;
   n = local / gm;
 }

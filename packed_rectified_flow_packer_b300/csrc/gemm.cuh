@@ -31,6 +31,7 @@ struct GemmParams {
   GemmProblem prob[2];
   int n_prob;
   int tiles_m[2], tiles_n[2];
+  int group_m[2];         // tile order: 0 = N fastest, else this many row tiles fastest
   int tile_begin[3];
   // epilogue inputs shared by the problems
   const int* srow_seq;    // [rows] sample of each stream-sorted row
