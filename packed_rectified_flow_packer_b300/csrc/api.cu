@@ -272,6 +272,12 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
     p.prob[i].out = g.out;
     p.tiles_m[i] = pair ? (g.M + 255) / 256 : (g.M + 127) / 128;
     p.tiles_n[i] = (g.N + BN - 1) / BN;
+    p.tma_store[i] = 0;
+    if (pair && (epi == mf::kEpiBiasBf16 || epi == mf::kEpiGelu) && g.ldo == g.N && g.N % 64 == 0 &&
+        aligned(g.out, 16)) {
+      if (!make_tmap(&p.tmC[i], g.out, g.N, g.M, 32)) return MF_ERR_CUDA;
+      p.tma_store[i] = 1;
+    }
     // N fastest when a wave of tiles spans whole rows of N tiles (few N tiles: the weight
     // matrix then stays in L2); otherwise sweep N over groups of 16 row tiles
     p.group_m[i] = p.tiles_n[i] <= 16 ? 0 : 16;

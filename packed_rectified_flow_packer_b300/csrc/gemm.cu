@@ -637,6 +637,54 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
       const GemmProblem& pr = p.prob[pi];
       const int row0 = m * 2 * kBM + rank * kBM + q * 32;  // first of this warp's 32 rows
       float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES) + (warp - 2) * 32 * kStageRow;
+      if constexpr (EPI == kEpiBiasBf16 || EPI == kEpiGelu) {
+        if (p.tma_store[pi]) {
+          // bf16 rows of 64 columns, 16-byte chunks swizzled as the 128-byte-swizzle tensor map
+          // expects, then one TMA store of 32 rows x 64 columns per group
+          uint8_t* tst = smem + STAGES * STAGE_BYTES + (warp - 2) * 4096;
+          const uint32_t el = elect_one();
+#pragma unroll 1
+          for (int g = 0; g < BN / 2; g += 64) {
+            if (el) tma_store_wait_read();  // the previous group's store has read the buffer
+            __syncwarp();
+#pragma unroll
+            for (int cq = 0; cq < 4; ++cq) {
+              const int c = c_lo + g + cq * 16;
+              uint32_t r[16];
+              tmem_ld16(tmem_addr(tmem_base, q * 32, acc * BN + c), r);
+              tmem_ld_wait();
+              tmem_reg_fence16(r);
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+              epi_row16<EPI>(p, pr, row0 + lane, n * BN + c, v, rope_inv, rope_axis);
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                uint4 w;
+                w.x = pack_bf16x2(v[8 * h2 + 0], v[8 * h2 + 1]);
+                w.y = pack_bf16x2(v[8 * h2 + 2], v[8 * h2 + 3]);
+                w.z = pack_bf16x2(v[8 * h2 + 4], v[8 * h2 + 5]);
+                w.w = pack_bf16x2(v[8 * h2 + 6], v[8 * h2 + 7]);
+                const int ch = cq * 2 + h2;
+                *reinterpret_cast<uint4*>(tst + lane * 128 + ((ch ^ (lane & 7)) << 4)) = w;
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (el) {
+              tma_store_2d(&p.tmC[pi], n * BN + c_lo + g, row0, tst);
+              tma_store_commit();
+            }
+            __syncwarp();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc ? tempty1 : tempty0);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+          continue;
+        }
+      }
 #pragma unroll 1
       for (int c = c_lo; c < c_lo + BN / 2; c += 16) {
         uint32_t r[16];
@@ -667,6 +715,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     }
   }
 
+  if (warp >= 2) tma_store_wait_all();  // this thread's bulk stores (if any) have completed
   tc_fence_before();
   cluster_sync();  // the pair's MMAs and TMEM reads are done, no remote signal is pending
   if (warp == 1) {
@@ -678,7 +727,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
 template <int EPI>
 cudaError_t launch_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
   constexpr int STAGES = 6;
-  const int smem = STAGES * (kBM * kBK * 2 + 128 * kBK * 2) + 8 * 32 * kStageRow * 4 + 1024;
+  // epilogue staging: 8 warps x max(32 rows of kStageRow floats, a 32 x 64 bf16 store box)
+  constexpr int kStaging = 8 * (32 * kStageRow * 4 > 4096 ? 32 * kStageRow * 4 : 4096);
+  const int smem = STAGES * (kBM * kBK * 2 + 128 * kBK * 2) + kStaging + 1024;
   auto kern = gemm_pair_kernel<EPI>;
   static int max_pairs = 0;  // clusters of two that fit on the device at once (per instantiation)
   cudaLaunchAttribute attr[1];

@@ -28,6 +28,8 @@ struct GemmProblem {
 struct GemmParams {
   CUtensorMap tmA[2];     // A [M][K], box {64, 128}, 128-byte swizzle
   CUtensorMap tmB[2];     // B [N][K], box {64, BN}, 128-byte swizzle
+  CUtensorMap tmC[2];     // bf16 output [M][N] for TMA stores, box {64, 32}, 128-byte swizzle
+  int tma_store[2];       // 1: the problem's epilogue stores through tmC (bias / GELU, bf16, ldo == N)
   GemmProblem prob[2];
   int n_prob;
   int tiles_m[2], tiles_n[2];
