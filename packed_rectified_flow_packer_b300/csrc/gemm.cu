@@ -536,12 +536,6 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
       int pi, m, n;
       decode_tile(p, tile, pi, m, n);
       const int nkb = p.prob[pi].K / kBK;
-      // the pair's next tile: its panels are prefetched into L2 one k-block per load of this
-      // tile, so a pair's first k-blocks of a new tile find their operands in L2
-      const bool has_next = tile + n_pairs < total;
-      int pi2 = 0, m2 = 0, n2 = 0;
-      if (has_next) decode_tile(p, tile + n_pairs, pi2, m2, n2);
-      const int nkb2 = has_next ? p.prob[pi2].K / kBK : 0;
       for (int kb = 0; kb < nkb; ++kb) {
         if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1, lim)) ||
             __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
@@ -554,10 +548,6 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
           const uint32_t fb = mapa_shared(&full_bar[stage], 0);
           tma_load_2d_pair(sa, &p.tmA[pi], kb * kBK, m * 2 * kBM + rank * kBM, fb);
           tma_load_2d_pair(sa + A_BYTES, &p.tmB[pi], kb * kBK, n * BN + rank * (BN / 2), fb);
-          if (kb < nkb2) {
-            tma_prefetch_l2_2d(&p.tmA[pi2], kb * kBK, m2 * 2 * kBM + rank * kBM);
-            tma_prefetch_l2_2d(&p.tmB[pi2], kb * kBK, n2 * BN + rank * (BN / 2));
-          }
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
