@@ -299,7 +299,9 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
 mf_status conditioning(const mf_plan* p, const mf_dims* d, const mf_temb_weights* tw,
                        const float* t, float* sinus, float* h1, float* c, cudaStream_t st) {
   const int S = p->S, H = d->hidden, F = d->freq_dim;
-  Trace tr(MF_K_COND, st, 2.0 * S * ((double)F * H + (double)H * H), 2.0 * ((double)F * H + (double)H * H), 3);
+  const int groups = (S + 3) / 4;  // one GEMV launch per group of four samples
+  Trace tr(MF_K_COND, st, 2.0 * S * ((double)F * H + (double)H * H), 2.0 * ((double)F * H + (double)H * H),
+           1 + 2 * groups);
   MF_CUDA(mf::launch_sinusoid(t, S, F, sinus, st));
   MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(tw->w_t1), static_cast<const bf16*>(tw->b_t1),
                           sinus, S, F, H, h1, H, 0, 1, st));
@@ -448,11 +450,11 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
   // 1. timestep condition c = SiLU(temb(t)) and the per-sample adaLN modulation of both streams
   MF_TRY(conditioning(p, d, &w->temb, t, sinus, h1, c, st));
   {
-    Trace tr(MF_K_COND, st, 2.0 * 2 * S * 6.0 * H * H, 2.0 * 2 * 6.0 * H * H, 2);
-    MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w->txt.w_mod), static_cast<const bf16*>(w->txt.b_mod),
-                            c, S, H, 6 * H, mod, 12 * H, 0, 0, st));
-    MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w->img.w_mod), static_cast<const bf16*>(w->img.b_mod),
-                            c, S, H, 6 * H, mod, 12 * H, 6 * H, 0, st));
+    // both streams' modulation GEMVs share c and run as one launch per group of four samples
+    Trace tr(MF_K_COND, st, 2.0 * 2 * S * 6.0 * H * H, 2.0 * 2 * 6.0 * H * H, (S + 3) / 4);
+    MF_CUDA(mf::launch_gemv2(static_cast<const bf16*>(w->txt.w_mod), static_cast<const bf16*>(w->txt.b_mod), 0,
+                             static_cast<const bf16*>(w->img.w_mod), static_cast<const bf16*>(w->img.b_mod),
+                             6 * H, c, S, H, 6 * H, mod, 12 * H, st));
   }
 
   // 2. a = LN(x)(1 + scale1) + shift1, stream-sorted
@@ -585,7 +587,7 @@ extern "C" mf_status mf_final(const mf_plan* p, const mf_dims* d, const mf_temb_
   MF_TRY(conditioning(p, d, temb, t, reinterpret_cast<float*>(ws + L.sinus),
                       reinterpret_cast<float*>(ws + L.h1), c, st));
   {
-    Trace tr(MF_K_COND, st, 2.0 * S * 2.0 * H * H, 2.0 * 2.0 * H * H, 1);
+    Trace tr(MF_K_COND, st, 2.0 * S * 2.0 * H * H, 2.0 * 2.0 * H * H, (S + 3) / 4);
     MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w_fmod), static_cast<const bf16*>(b_fmod), c, S, H,
                             2 * H, fmod, 2 * H, 0, 0, st));
   }

@@ -54,60 +54,92 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return u;
 }
 
-// y[s][o] = act(W[o] . x[s] + b[o]) for every sample s.  One warp per kGemvRows consecutive
-// output features; lane l owns the 8-element chunks k = 8 l + 256 i, i < NCH = K / 256.  All
-// kGemvRows * NCH weight chunks of the warp (read once, streamed past L1) are requested before
-// the first multiply, so every warp keeps its whole share of the weight stream in flight; x
-// ([S][K] f32, S <= 4) comes from L1, one load per chunk shared by the warp's rows.
-constexpr int kGemvRows = 2;
+// (a0, a1) += (w0 * x0, w1 * x1) as one packed f32x2 FMA.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float w0, float w1, float x0, float x1) {
+  asm("{\n\t.reg .b64 a, w, x;\n\t"
+      "mov.b64 a, {%0, %1};\n\tmov.b64 w, {%2, %3};\n\tmov.b64 x, {%4, %5};\n\t"
+      "fma.rn.f32x2 a, w, x, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
+}
+
+// y[s][y_off[p] + o] = act(W_p[o] . x[s] + b_p[o]) for the samples s < S <= 4 of one launch and
+// the problem p = blockIdx.y.  One warp per kGemvRows consecutive output features; lane l owns
+// the 8-element chunks k = 8 l + 256 i, i < NCH = K / 256.  The weights (read once, streamed past
+// L1) pass through a register ring: the loads of chunk i + kGemvDepth are issued before chunk i
+// is used.  Every chunk of x (f32, from L1) is loaded once for all rows of the warp; with two
+// rows per warp the L1 traffic for x was four times the weight bytes and bounded the kernel.
+// Products accumulate as packed f32x2 FMAs into even / odd partial sums that meet before the
+// warp reduction.  Samples beyond S reuse the last sample's x (valid addresses; their sums are
+// not stored), which keeps the x loads free of branches.
+constexpr int kGemvRows = 4;
+constexpr int kGemvDepth = 1;
+
+struct GemvArgs {
+  const bf16* W[2];
+  const bf16* b[2];
+  int y_off[2];
+  const float* x;
+  int S, O;
+  float* y;
+  int y_stride;
+};
 
 template <int ACT, int NCH>
-__global__ void __launch_bounds__(128) gemv_kernel(const bf16* __restrict__ W, const bf16* __restrict__ b,
-                                                   const float* __restrict__ x, int S, int O,
-                                                   float* __restrict__ y, int y_stride, int y_off) {
+__global__ void __launch_bounds__(128) gemv_kernel(const GemvArgs g) {
   constexpr int K = NCH * 256;
-  const int o0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kGemvRows;
+  constexpr int R = kGemvRows, D = kGemvDepth;
+  const int pb = blockIdx.y;
+  const int o0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * R;
   const int lane = threadIdx.x & 31;
-  if (o0 >= O) return;
-  const int nr = min(kGemvRows, O - o0);
-  uint4 wv[kGemvRows][NCH];
+  if (o0 >= g.O) return;
+  const int nr = min(R, g.O - o0);
+  const int S = g.S;
+  const bf16* wrow = (pb ? g.W[1] : g.W[0]) + (size_t)o0 * K + lane * 8;
+  uint4 wv[D + 1][R];
 #pragma unroll
-  for (int r = 0; r < kGemvRows; ++r)
+  for (int i = 0; i < D && i < NCH; ++i)
 #pragma unroll
-    for (int i = 0; i < NCH; ++i)
-      wv[r][i] = r < nr ? ld_stream16(W + (size_t)(o0 + r) * K + lane * 8 + 256 * i) : make_uint4(0, 0, 0, 0);
-  // at most four samples per launch (the host launches once per group of four), so each weight
-  // chunk is unpacked once, right where it is used
-  {
-    constexpr int s0 = 0;
-    float acc[kGemvRows][4] = {};
+    for (int r = 0; r < R; ++r)
+      wv[i][r] = r < nr ? ld_stream16(wrow + (size_t)r * K + 256 * i) : make_uint4(0, 0, 0, 0);
+  float acc[R][4][2] = {};
 #pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-      const int k = lane * 8 + 256 * i;
-      float wf[kGemvRows][8];
+  for (int i = 0; i < NCH; ++i) {
+    if (i + D < NCH) {
 #pragma unroll
-      for (int r = 0; r < kGemvRows; ++r) unpack8(wv[r][i], wf[r]);
+      for (int r = 0; r < R; ++r)
+        wv[(i + D) % (D + 1)][r] = r < nr ? ld_stream16(wrow + (size_t)r * K + 256 * (i + D)) : make_uint4(0, 0, 0, 0);
+    }
+    const int k = lane * 8 + 256 * i;
+    float xv[4][8];
 #pragma unroll
-      for (int si = 0; si < 4; ++si) {
-        if (s0 + si < S) {
-          const float4* xv = reinterpret_cast<const float4*>(x + (size_t)(s0 + si) * K + k);
-          const float4 a = __ldg(xv), c = __ldg(xv + 1);
-#pragma unroll
-          for (int r = 0; r < kGemvRows; ++r)
-            acc[r][si] += wf[r][0] * a.x + wf[r][1] * a.y + wf[r][2] * a.z + wf[r][3] * a.w +
-                          wf[r][4] * c.x + wf[r][5] * c.y + wf[r][6] * c.z + wf[r][7] * c.w;
-        }
-      }
+    for (int si = 0; si < 4; ++si) {
+      const float4* xp = reinterpret_cast<const float4*>(g.x + (size_t)min(si, S - 1) * K + k);
+      const float4 a = __ldg(xp), c = __ldg(xp + 1);
+      xv[si][0] = a.x; xv[si][1] = a.y; xv[si][2] = a.z; xv[si][3] = a.w;
+      xv[si][4] = c.x; xv[si][5] = c.y; xv[si][6] = c.z; xv[si][7] = c.w;
     }
 #pragma unroll
-    for (int r = 0; r < kGemvRows; ++r) {
+    for (int r = 0; r < R; ++r) {
+      float wf[8];
+      unpack8(wv[i % (D + 1)][r], wf);
 #pragma unroll
-      for (int si = 0; si < 4; ++si) {
-        const float v = warp_sum(acc[r][si]);
-        if (lane == 0 && r < nr && s0 + si < S) {
-          const float t = v + (b ? __bfloat162float(b[o0 + r]) : 0.0f);
-          y[(size_t)(s0 + si) * y_stride + y_off + o0 + r] = ACT == 1 ? silu_f(t) : t;
-        }
+      for (int si = 0; si < 4; ++si)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          ffma2(acc[r][si][0], acc[r][si][1], wf[2 * j], wf[2 * j + 1], xv[si][2 * j], xv[si][2 * j + 1]);
+    }
+  }
+  const bf16* bias = pb ? g.b[1] : g.b[0];
+  float* y = g.y + (pb ? g.y_off[1] : g.y_off[0]) + o0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+#pragma unroll
+    for (int si = 0; si < 4; ++si) {
+      const float v = warp_sum(acc[r][si][0] + acc[r][si][1]);
+      if (lane == 0 && r < nr && si < S) {
+        const float t = v + (bias ? __bfloat162float(bias[o0 + r]) : 0.0f);
+        y[(size_t)si * g.y_stride + r] = ACT == 1 ? silu_f(t) : t;
       }
     }
   }
@@ -375,23 +407,26 @@ cudaError_t launch_sinusoid(const float* t, int S, int F, float* out, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int K, int O, float* y,
-                        int y_stride, int y_off, int act, cudaStream_t st) {
-  if (S <= 0 || O <= 0) return cudaSuccess;
-  const int warps = (O + kGemvRows - 1) / kGemvRows;
-  const int blocks = (warps + 3) / 4;
+namespace {
+// One launch per group of four samples; gridDim.y = number of problems.
+cudaError_t gemv_groups(GemvArgs g, int np, int K, int act, const float* x, float* y, int S,
+                        cudaStream_t st, int* launches) {
+  if (launches) *launches = 0;
+  if (S <= 0 || g.O <= 0) return cudaSuccess;
+  const int warps = (g.O + kGemvRows - 1) / kGemvRows;
+  const dim3 grid((warps + 3) / 4, np);
   const int nch = K % 256 == 0 ? K / 256 : 0;
-  for (int s0 = 0; s0 < S; s0 += 4) {  // four samples per launch
-    const int sn = S - s0 < 4 ? S - s0 : 4;
-    const float* xs = x + (size_t)s0 * K;
-    float* ys = y + (size_t)s0 * y_stride;
+  for (int s0 = 0; s0 < S; s0 += 4) {
+    g.S = S - s0 < 4 ? S - s0 : 4;
+    g.x = x + (size_t)s0 * K;
+    g.y = y + (size_t)s0 * g.y_stride;
     switch (nch * 2 + (act == 1 ? 1 : 0)) {
-#define MF_GEMV_CASE(n)                                                                  \
-  case 2 * n:                                                                           \
-    gemv_kernel<0, n><<<blocks, 128, 0, st>>>(W, b, xs, sn, O, ys, y_stride, y_off);    \
-    break;                                                                              \
-  case 2 * n + 1:                                                                       \
-    gemv_kernel<1, n><<<blocks, 128, 0, st>>>(W, b, xs, sn, O, ys, y_stride, y_off);    \
+#define MF_GEMV_CASE(n)                                 \
+  case 2 * n:                                          \
+    gemv_kernel<0, n><<<grid, 128, 0, st>>>(g);        \
+    break;                                             \
+  case 2 * n + 1:                                      \
+    gemv_kernel<1, n><<<grid, 128, 0, st>>>(g);        \
     break;
       MF_GEMV_CASE(1) MF_GEMV_CASE(2) MF_GEMV_CASE(3) MF_GEMV_CASE(4) MF_GEMV_CASE(5) MF_GEMV_CASE(6)
       MF_GEMV_CASE(7) MF_GEMV_CASE(8) MF_GEMV_CASE(9) MF_GEMV_CASE(10) MF_GEMV_CASE(11) MF_GEMV_CASE(12)
@@ -399,8 +434,23 @@ cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int
 #undef MF_GEMV_CASE
       default: return cudaErrorInvalidValue;  // K must be a multiple of 256, at most 4096
     }
+    if (launches) ++*launches;
   }
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int K, int O, float* y,
+                        int y_stride, int y_off, int act, cudaStream_t st, int* launches) {
+  GemvArgs g{{W, W}, {b, b}, {y_off, y_off}, x, 0, O, y, y_stride};
+  return gemv_groups(g, 1, K, act, x, y, S, st, launches);
+}
+
+cudaError_t launch_gemv2(const bf16* W0, const bf16* b0, int y_off0, const bf16* W1, const bf16* b1,
+                         int y_off1, const float* x, int S, int K, int O, float* y, int y_stride,
+                         cudaStream_t st, int* launches) {
+  GemvArgs g{{W0, W1}, {b0, b1}, {y_off0, y_off1}, x, 0, O, y, y_stride};
+  return gemv_groups(g, 2, K, 0, x, y, S, st, launches);
 }
 
 cudaError_t launch_ln_modulate(const LnModArgs& a, cudaStream_t st) {

@@ -9,9 +9,17 @@ namespace mf {
 cudaError_t launch_sinusoid(const float* t, int S, int F, float* out, cudaStream_t st);
 
 // y[s][y_off + o] = act(W[o] . x[s] + b[o]) for o < O, W bf16 [O][K], x f32 [S][K];
-// act 0 = identity, 1 = SiLU.  K multiple of 256.
+// act 0 = identity, 1 = SiLU.  K multiple of 256, at most 4096.  *launches (if not null)
+// receives the number of kernels launched (one per group of four samples).
 cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int K, int O,
-                        float* y, int y_stride, int y_off, int act, cudaStream_t st);
+                        float* y, int y_stride, int y_off, int act, cudaStream_t st,
+                        int* launches = nullptr);
+
+// Two GEMVs with the same x, K and O in one launch per group of four samples:
+// y[s][y_off_p + o] = W_p[o] . x[s] + b_p[o] for p = 0, 1 (no activation).
+cudaError_t launch_gemv2(const bf16* W0, const bf16* b0, int y_off0, const bf16* W1, const bf16* b1,
+                         int y_off1, const float* x, int S, int K, int O, float* y, int y_stride,
+                         cudaStream_t st, int* launches = nullptr);
 
 // out[r] = LN(x[r]) (1 + scale) + shift for stream-sorted rows r in [0, rows), where rows
 // below n_first come from x_first and the rest from x_second; (shift, scale) of row r are
