@@ -108,13 +108,16 @@ typedef struct mf_plan mf_plan; /* opaque; owned by the library, freed with mf_p
 mf_status mf_pack(const mf_sample* samples, int32_t n, int32_t budget, mf_plan** out);
 
 /* Copies the plan's index buffers to the current device (library-owned device memory,
- * allocated on the first upload, freed by mf_plan_free).  The copy is enqueued on `stream`
- * and synchronised before the call returns; a second upload on the same device is a no-op.
+ * allocated on the first upload in stream order on `stream`, freed by mf_plan_free).  The copy
+ * is enqueued on `stream` and `stream` is synchronised before the call returns (work on other
+ * streams is not waited for); a second upload on the same device is a no-op.
  * Errors: MF_ERR_INVALID_ARG, MF_ERR_CUDA. */
 mf_status mf_plan_upload(mf_plan* plan, void* stream);
 
-/* Frees host and device memory of the plan.  The caller must make sure no stream still
- * uses it.  NULL is a no-op. */
+/* Frees host and device memory of the plan without waiting for the device: the device copy
+ * is released in stream order on the legacy default stream.  The caller must make sure no
+ * work still in flight uses it (synchronise the stream that last used the plan, or wait on an
+ * event recorded after that use).  NULL is a no-op. */
 void mf_plan_free(mf_plan* plan);
 
 typedef struct {

@@ -351,20 +351,21 @@ extern "C" mf_status mf_plan_upload(mf_plan* p, void* stream) {
   o = (o + p->t.size() * 4 + 63) & ~size_t(63);
   p->blob_bytes = o > 0 ? o : 64;
 
+  // stream-ordered allocation: neither this nor mf_plan_free waits for work on other streams
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* blob = nullptr;
-  if (cudaMalloc(&blob, p->blob_bytes) != cudaSuccess) return MF_ERR_CUDA;
+  if (cudaMallocAsync(&blob, p->blob_bytes, st) != cudaSuccess) return MF_ERR_CUDA;
   // staged in one host buffer; the upload is synchronised before the buffer is released
   char* host = static_cast<char*>(std::malloc(p->blob_bytes));
-  if (host == nullptr) { cudaFree(blob); return MF_ERR_CUDA; }
+  if (host == nullptr) { cudaFreeAsync(blob, st); return MF_ERR_CUDA; }
   std::memset(host, 0, p->blob_bytes);
   for (int i = 0; i < np; ++i)
     if (counts[i]) std::memcpy(host + off[i], srcs[i], counts[i] * 4);
   if (!p->t.empty()) std::memcpy(host + off[np], p->t.data(), p->t.size() * 4);
-  cudaError_t e = cudaMemcpyAsync(blob, host, p->blob_bytes, cudaMemcpyHostToDevice,
-                                  static_cast<cudaStream_t>(stream));
-  if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaMemcpyAsync(blob, host, p->blob_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   std::free(host);
-  if (e != cudaSuccess) { cudaFree(blob); return MF_ERR_CUDA; }
+  if (e != cudaSuccess) { cudaFreeAsync(blob, st); return MF_ERR_CUDA; }
 
   char* b = static_cast<char*>(blob);
   p->d_cu = reinterpret_cast<const int32_t*>(b + off[0]);
@@ -390,7 +391,8 @@ extern "C" void mf_plan_free(mf_plan* p) {
     int cur = -1;
     cudaGetDevice(&cur);
     if (cur != p->device) cudaSetDevice(p->device);
-    cudaFree(p->d_blob);
+    // released in stream order on the legacy default stream, without a device-wide wait
+    cudaFreeAsync(p->d_blob, nullptr);
     if (cur != p->device && cur >= 0) cudaSetDevice(cur);
   }
   delete p;
