@@ -32,6 +32,10 @@ Readings where the pages are silent (each is a named constant below):
 * edit: every token of a sample shares t; the source frame stays clean;
 * Euler: v ~ z - eps = -dz_t/dt, so stepping t_k -> t_{k+1} < t_k is z += (t_k - t_{k+1}) v;
 * loss: per-sample sums over target-frame image elements, and the element-weighted mean.
+* QK-RMSNorm (a variant, off unless a stream's weights carry w_qnorm / w_knorm): each head's
+  query and key vector after the QKV projection is divided by its root mean square over the
+  head dimension (eps 1e-6) and multiplied by a learned per-dimension scale of that stream,
+  before RoPE.
 """
 from __future__ import annotations
 
@@ -39,6 +43,7 @@ import numpy as np
 from scipy.special import erf
 
 LN_EPS = 1e-6
+RMS_EPS = 1e-6
 ROPE_BASE = 10000.0
 T_SCALE = 1000.0
 MAX_PERIOD = 10000.0
@@ -73,6 +78,13 @@ def layer_norm(x, eps: float = LN_EPS):
     mu = x.mean(axis=-1, keepdims=True)
     var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
     return (x - mu) / np.sqrt(var + eps)
+
+
+def rms_norm_heads(x, g, eps: float = RMS_EPS):
+    """x [L][heads][D] -> x / sqrt(mean over D of x^2 + eps) * g, g [D] (one scale per head
+    dimension, shared by the heads)."""
+    x = f64(x)
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps) * f64(g)
 
 
 def modulate(x, shift, scale):
@@ -169,6 +181,12 @@ def block_forward(x_txt, x_img, pos_img, c, bw: dict, heads: int, rows=None):
     a = {s: modulate(x[s], mod[s]["shift1"], mod[s]["scale1"]) for s in STREAMS}
     qkv = np.concatenate([linear(a[s], bw[s]["w_qkv"], bw[s]["b_qkv"]) for s in STREAMS])
     q, k, v = (qkv[:, i * H:(i + 1) * H].reshape(L, heads, D) for i in range(3))
+    if any("w_qnorm" in bw[s] for s in STREAMS):
+        # QK-RMSNorm variant: each stream's rows with that stream's scales (text rows first)
+        q, k = q.copy(), k.copy()
+        for s, seg in (("txt", slice(0, Lt)), ("img", slice(Lt, L))):
+            q[seg] = rms_norm_heads(q[seg], bw[s]["w_qnorm"])
+            k[seg] = rms_norm_heads(k[seg], bw[s]["w_knorm"])
     pos = np.concatenate([np.zeros((Lt, 3), np.int64), np.asarray(pos_img, np.int64)])
     sel = np.arange(L) if rows is None else np.asarray(rows)
     q = apply_rope(q[sel], pos[sel])

@@ -203,7 +203,9 @@ class ModelWeights:
 
 
 def model_weights(dims: Dims, n_blocks: int, seed: int, std: float = 0.02,
-                  bf16: bool = True) -> ModelWeights:
+                  bf16: bool = True, qk_norm: bool = False) -> ModelWeights:
+    """Seeded weights of an n-block stack.  qk_norm adds the QK-RMSNorm scales of each stream
+    (w_qnorm, w_knorm [head_dim], 1 + N(0, 0.1^2))."""
     d = dims
     H, C, F = d.hidden, d.channels, d.freq_dim
     nm = lambda name, shape: normal(seed, name, shape, std)            # noqa: E731
@@ -214,6 +216,10 @@ def model_weights(dims: Dims, n_blocks: int, seed: int, std: float = 0.02,
     for i in range(n_blocks):
         m.blocks.append({s: {k: nm(f"block{i}.{s}.{k}", shp) for k, shp in BLOCK_SHAPES(d).items()}
                          for s in STREAMS})
+        if qk_norm:
+            for s in STREAMS:
+                for k in ("w_qnorm", "w_knorm"):
+                    m.blocks[-1][s][k] = 1.0 + normal(seed, f"block{i}.{s}.{k}", (d.head_dim,), 0.1)
     m.final = {"w_fmod": nm("final.w_fmod", (2 * H, H)), "b_fmod": nm("final.b_fmod", (2 * H,)),
                "w_out": nm("final.w_out", (C, H)), "b_out": nm("final.b_out", (C,))}
     return m.rounded() if bf16 else m

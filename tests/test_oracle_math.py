@@ -358,6 +358,71 @@ def test_nft_loss_pins():
 
 
 # ------------------------------------------------------------------ planted mistakes
+def test_rms_norm_heads_pins():
+    """QK-RMSNorm: a hand-worked vector, unit RMS per head whatever the heads' scales (a norm
+    over the whole row, or over the heads, fails this), per-head scale invariance, and the
+    scale applied per dimension."""
+    y = M.rms_norm_heads(np.array([[[3.0, 4.0]]]), np.array([2.0, 0.5]), eps=0.0)
+    r = np.sqrt(12.5)                                                   # sqrt((9 + 16) / 2)
+    np.testing.assert_allclose(y[0, 0], [6.0 / r, 2.0 / r], rtol=1e-15)
+    x = R.standard_normal((6, 4, 32)) * np.array([1e-2, 1.0, 30.0, 3.0])[None, :, None]
+    y = M.rms_norm_heads(x, np.ones(32), eps=0.0)
+    np.testing.assert_allclose(np.sqrt((y ** 2).mean(-1)), 1.0, rtol=1e-12)
+    a = np.array([0.5, 7.0, 0.01, 2.0])[None, :, None]
+    np.testing.assert_allclose(M.rms_norm_heads(x * a, np.ones(32), eps=0.0), y, rtol=1e-12)
+    g = 1.0 + R.standard_normal(32)
+    np.testing.assert_allclose(M.rms_norm_heads(x, g, eps=0.0), y * g, rtol=1e-12)
+    # eps enters under the root: a zero head stays zero, a tiny one is damped
+    z = M.rms_norm_heads(np.zeros((1, 1, 4)), np.ones(4))
+    np.testing.assert_array_equal(z, 0.0)
+    t = M.rms_norm_heads(np.full((1, 1, 4), 1e-3), np.ones(4), eps=1e-6)
+    np.testing.assert_allclose(t, 1e-3 / np.sqrt(1e-6 + 1e-6), rtol=1e-12)
+
+
+def test_block_qk_norm_invariance():
+    """With QK-RMSNorm on, scaling a stream's query (or key) projection by a positive factor
+    leaves the block output unchanged up to the eps term, while without it the output moves;
+    with unit scales the queries and keys that reach attention have unit RMS per head (the
+    norm comes before RoPE, which keeps it)."""
+    d = synth.Dims(hidden=64, heads=2, channels=16)
+    w = synth.model_weights(d, 1, 5, bf16=False, qk_norm=True)
+    H = d.hidden
+    xt, xi = R.standard_normal((5, H)), R.standard_normal((12, H))
+    pos = M.image_positions(1, 3, 4)
+    c = R.standard_normal(H)
+    ref = np.concatenate(M.block_forward(xt, xi, pos, c, w.blocks[0], d.heads))
+    for s in M.STREAMS:
+        for part in (0, 1):                                              # q rows, k rows of W_qkv
+            bw = copy.deepcopy(w.blocks[0])
+            bw[s]["w_qkv"][part * H:(part + 1) * H] *= 20.0
+            bw[s]["b_qkv"][part * H:(part + 1) * H] *= 20.0
+            got = np.concatenate(M.block_forward(xt, xi, pos, c, bw, d.heads))
+            np.testing.assert_allclose(got, ref, rtol=0, atol=1e-5 * np.abs(ref).max())
+            off = {st: {k: v for k, v in bw[st].items() if k not in ("w_qnorm", "w_knorm")} for st in M.STREAMS}
+            base = {st: {k: v for k, v in w.blocks[0][st].items() if k not in ("w_qnorm", "w_knorm")}
+                    for st in M.STREAMS}
+            moved = np.concatenate(M.block_forward(xt, xi, pos, c, off, d.heads)) - \
+                np.concatenate(M.block_forward(xt, xi, pos, c, base, d.heads))
+            assert np.abs(moved).max() > 10 * 1e-5 * np.abs(ref).max()
+    bw = copy.deepcopy(w.blocks[0])
+    calls = []
+    orig = M.attention
+
+    def spy(q, k, v, rows=None):
+        calls.append((M.f64(q), M.f64(k)))
+        return orig(q, k, v, rows)
+
+    import unittest.mock as um
+    for st in M.STREAMS:
+        bw[st]["w_qnorm"] = np.ones(d.head_dim)
+        bw[st]["w_knorm"] = np.ones(d.head_dim)
+    with um.patch.object(M, "attention", spy):
+        M.block_forward(xt, xi, pos, c, bw, d.heads)
+    q, k = calls[-1]
+    np.testing.assert_allclose(np.sqrt((q ** 2).mean(-1)), 1.0, rtol=1e-3)   # RoPE keeps the RMS (eps: 1e-4)
+    np.testing.assert_allclose(np.sqrt((k ** 2).mean(-1)), 1.0, rtol=1e-3)
+
+
 def _pins_pass():
     """A compact battery of the pins above, for the planted-mistake test."""
     from tests.conftest import load_golden
@@ -382,12 +447,15 @@ def _pins_pass():
         test_euler_straight_path()
         test_cfg_limits()
         test_nft_loss_pins()
+        test_rms_norm_heads_pins()
+        test_block_qk_norm_invariance()
     except AssertionError:
         return False
     return True
 
 
 ORIG = {n: getattr(M, n) for n in ("layer_norm", "gelu", "timestep_embedding", "rope_angles",
+                                     "rms_norm_heads",
                                      "attention", "interpolate", "flow_loss", "euler_step",
                                      "cfg_combine", "nft_loss")}
 
@@ -425,6 +493,11 @@ MUTANTS = {
                         ORIG["nft_loss"](vp, vn, e, z, r, target)),
     "nft_no_negative_term": ("nft_loss", lambda vp, vn, z, e, r, target=None:
                              ORIG["nft_loss"](vp, vp, z, e, 1.0, target)),
+    "rms_over_whole_row": ("rms_norm_heads", lambda x, g, eps=M.RMS_EPS:
+                           M.f64(x) / np.sqrt((M.f64(x) ** 2).mean(axis=(-2, -1), keepdims=True) + eps) * M.f64(g)),
+    "rms_eps_outside_root": ("rms_norm_heads", lambda x, g, eps=M.RMS_EPS:
+                             M.f64(x) / (np.sqrt((M.f64(x) ** 2).mean(-1, keepdims=True)) + eps) * M.f64(g)),
+    "rms_no_scale": ("rms_norm_heads", lambda x, g, eps=M.RMS_EPS: ORIG["rms_norm_heads"](x, np.ones_like(M.f64(g)), eps)),
 }
 
 
