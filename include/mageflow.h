@@ -172,13 +172,18 @@ typedef struct {
 
 /* One stream (text or image) of one block [PR 5]: the adaLN modulation (6 chunks of H in
  * the order shift1, scale1, gate1, shift2, scale2, gate2), the fused QKV projection
- * (q | k | v, each H wide), the attention output projection and the MLP. */
+ * (q | k | v, each H wide), the attention output projection and the MLP.
+ * w_qnorm / w_knorm (optional, both or neither; NULL = off): the QK-RMSNorm variant, one
+ * scale per head dimension [D]: each head's q (k) vector after the QKV projection becomes
+ * q / sqrt(mean_d q_d^2 + 1e-6) * w_qnorm before RoPE.  The pages do not name a QK norm; the
+ * plain block has none. */
 typedef struct {
   const void* w_mod; const void* b_mod;   /* [6H][H], [6H] */
   const void* w_qkv; const void* b_qkv;   /* [3H][H], [3H] */
   const void* w_o;   const void* b_o;     /* [H][H],  [H]  */
   const void* w_1;   const void* b_1;     /* [rH][H], [rH] */
   const void* w_2;   const void* b_2;     /* [H][rH], [H]  */
+  const void* w_qnorm; const void* w_knorm; /* [D], [D] or NULL */
 } mf_stream_weights;
 
 typedef struct {
@@ -206,7 +211,8 @@ mf_status mf_block_workspace_layout(const mf_plan* plan, const mf_dims* dims, si
 /* One NR-MMDiT block over the whole pack, in place on x:
  *   per sample s and stream m: (shift1, scale1, gate1, shift2, scale2, gate2) = W_mod c_s + b
  *   a  = LN(x) (1 + scale1) + shift1                      (LN without affine, eps 1e-6)
- *   q, k, v = a W_qkv^T + b_qkv, RoPE on q and k over (frame, row, col)
+ *   q, k, v = a W_qkv^T + b_qkv, [QK-RMSNorm per head if the stream has its scales],
+ *             RoPE on q and k over (frame, row, col)
  *   o  = softmax(q k^T / sqrt(D)) v, jointly over each sample's own tokens only
  *   x += gate1 (o W_o^T + b_o)
  *   x += gate2 (GELU(LN(x)(1 + scale2) + shift2) W_1^T + b_1) W_2^T + b_2)

@@ -57,10 +57,11 @@ class mf_temb_weights(C.Structure):
 
 
 STREAM_FIELDS = ("w_mod", "b_mod", "w_qkv", "b_qkv", "w_o", "b_o", "w_1", "b_1", "w_2", "b_2")
+STREAM_OPTIONAL = ("w_qnorm", "w_knorm")   # QK-RMSNorm scales; NULL when absent
 
 
 class mf_stream_weights(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in STREAM_FIELDS]
+    _fields_ = [(n, C.c_void_p) for n in STREAM_FIELDS + STREAM_OPTIONAL]
 
 
 class mf_block_weights(C.Structure):
@@ -152,8 +153,10 @@ def temb_struct(w) -> mf_temb_weights:
 
 def block_struct(temb, txt, img) -> mf_block_weights:
     """temb, txt, img: dicts name -> device tensor (bf16)."""
-    return mf_block_weights(temb_struct(temb), mf_stream_weights(*[_ptr(txt[k]) for k in STREAM_FIELDS]),
-                            mf_stream_weights(*[_ptr(img[k]) for k in STREAM_FIELDS]))
+    def stream(d):
+        return mf_stream_weights(*[_ptr(d[k]) for k in STREAM_FIELDS],
+                                 *[_ptr(d.get(k)) for k in STREAM_OPTIONAL])
+    return mf_block_weights(temb_struct(temb), stream(txt), stream(img))
 
 
 # ------------------------------------------------------------------ plan

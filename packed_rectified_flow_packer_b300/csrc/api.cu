@@ -319,6 +319,9 @@ bool stream_ok(const mf_stream_weights& s) {
   const void* ptrs[] = {s.w_mod, s.b_mod, s.w_qkv, s.b_qkv, s.w_o, s.b_o, s.w_1, s.b_1, s.w_2, s.b_2};
   for (const void* q : ptrs)
     if (q == nullptr || !aligned(q, 16)) return false;
+  // QK-RMSNorm scales: both or neither
+  if ((s.w_qnorm == nullptr) != (s.w_knorm == nullptr)) return false;
+  if (s.w_qnorm != nullptr && (!aligned(s.w_qnorm, 16) || !aligned(s.w_knorm, 16))) return false;
   return true;
 }
 
@@ -477,6 +480,10 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
   gp.q = q;
   gp.k = k;
   gp.v = v;
+  gp.qk_norm[0][0] = static_cast<const bf16*>(w->txt.w_qnorm);
+  gp.qk_norm[0][1] = static_cast<const bf16*>(w->txt.w_knorm);
+  gp.qk_norm[1][0] = static_cast<const bf16*>(w->img.w_qnorm);
+  gp.qk_norm[1][1] = static_cast<const bf16*>(w->img.w_knorm);
   {
     GemmSpec sp[2] = {{Nt, 3 * H, H, a, w->txt.w_qkv, w->txt.b_qkv, nullptr, 0, 0, 0},
                       {Ni, 3 * H, H, a + (size_t)Nt * H, w->img.w_qkv, w->img.b_qkv, nullptr, 0, Nt, 1}};

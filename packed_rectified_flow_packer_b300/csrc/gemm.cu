@@ -150,6 +150,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const GemmPr
 // per row, 8 columns each: the last operation (gated residual, scatter to joint order) and the
 // global store, so each store instruction writes whole 32-byte sectors of 16 rows instead of
 // 16 bytes of 32 rows (stores of that shape held back the tensor core's issue).
+constexpr float kQkNormEps = 1e-6f;  // QK-RMSNorm epsilon (inside the root)
 constexpr int kStageRow = 20;  // floats per staged row (16 + 4 padding: conflict-free 16-byte writes)
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -167,27 +168,47 @@ __device__ __forceinline__ void tmem_reg_fence16(uint32_t (&r)[16]) {
                "+r"(r[14]), "+r"(r[15]));
 }
 
-// Phase 1: 16 columns of one row, in place.
+// v[i] += bias[col0 + i], i < 16 (no-op without a bias).
+__device__ __forceinline__ void add_bias16(const GemmProblem& pr, int col0, float (&v)[16]) {
+  if (pr.bias == nullptr) return;
+  const uint4* b = reinterpret_cast<const uint4*>(pr.bias + col0);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 u = __ldg(b + i);
+    const float2 f0 = unpack_bf16x2(u.x), f1 = unpack_bf16x2(u.y), f2 = unpack_bf16x2(u.z),
+                 f3 = unpack_bf16x2(u.w);
+    v[8 * i + 0] += f0.x; v[8 * i + 1] += f0.y; v[8 * i + 2] += f1.x; v[8 * i + 3] += f1.y;
+    v[8 * i + 4] += f2.x; v[8 * i + 5] += f2.y; v[8 * i + 6] += f3.x; v[8 * i + 7] += f3.y;
+  }
+}
+
+// Phase 1: 16 columns of one row, in place.  For the QKV epilogue with QK-RMSNorm, qk_g is the
+// stream's scale vector of this part (q or k) and qk_rstd the row's 1 / RMS over the head of
+// these columns; the norm is applied after the bias and before RoPE.
 template <int EPI>
 __device__ __forceinline__ void epi_row16(const GemmParams& p, const GemmProblem& pr, int row, int col0,
-                                          float (&v)[16], const float* rope_inv, const int* rope_axis) {
+                                          float (&v)[16], const float* rope_inv, const int* rope_axis,
+                                          const bf16* qk_g = nullptr, float qk_rstd = 0.0f) {
   if (row >= pr.M || col0 >= pr.N) return;
-  if (pr.bias != nullptr) {
-    const uint4* b = reinterpret_cast<const uint4*>(pr.bias + col0);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint4 u = __ldg(b + i);
-      const float2 f0 = unpack_bf16x2(u.x), f1 = unpack_bf16x2(u.y), f2 = unpack_bf16x2(u.z),
-                   f3 = unpack_bf16x2(u.w);
-      v[8 * i + 0] += f0.x; v[8 * i + 1] += f0.y; v[8 * i + 2] += f1.x; v[8 * i + 3] += f1.y;
-      v[8 * i + 4] += f2.x; v[8 * i + 5] += f2.y; v[8 * i + 6] += f3.x; v[8 * i + 7] += f3.y;
-    }
-  }
+  add_bias16(pr, col0, v);
   if constexpr (EPI == kEpiGelu) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.7071067811865476f));
   } else if constexpr (EPI == kEpiQkvRope) {
     const int which = col0 / p.H;
+    if (qk_g != nullptr) {
+      const uint4* gp = reinterpret_cast<const uint4*>(qk_g + (col0 - which * p.H) % p.head_dim);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint4 u = __ldg(gp + i);
+        const float2 g0 = unpack_bf16x2(u.x), g1 = unpack_bf16x2(u.y), g2 = unpack_bf16x2(u.z),
+                     g3 = unpack_bf16x2(u.w);
+        v[8 * i + 0] *= qk_rstd * g0.x; v[8 * i + 1] *= qk_rstd * g0.y;
+        v[8 * i + 2] *= qk_rstd * g1.x; v[8 * i + 3] *= qk_rstd * g1.y;
+        v[8 * i + 4] *= qk_rstd * g2.x; v[8 * i + 5] *= qk_rstd * g2.y;
+        v[8 * i + 6] *= qk_rstd * g3.x; v[8 * i + 7] *= qk_rstd * g3.y;
+      }
+    }
     if (which < 2) {
       const int joint = __ldg(p.srow_joint + pr.row_off + row);
       const int* ps = p.pos + (size_t)joint * 3;
@@ -675,6 +696,37 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
           continue;
         }
       }
+      // QK-RMSNorm: a first pass over this warp's 128 columns (one head, or two when D = 64)
+      // gives each row's 1 / RMS per head, from the same bias-added values the second uses
+      const bf16* qk_g = nullptr;
+      float qk_rstd0 = 0.0f, qk_rstd1 = 0.0f;
+      if constexpr (EPI == kEpiQkvRope) {
+        const int col_lo = n * BN + c_lo, which = col_lo / p.H;
+        const bf16* g = pi ? (which ? p.qk_norm[1][1] : p.qk_norm[1][0])
+                           : (which ? p.qk_norm[0][1] : p.qk_norm[0][0]);
+        if (which < 2 && col_lo < pr.N && g != nullptr) {
+          qk_g = g;
+          float ss0 = 0.0f, ss1 = 0.0f;
+#pragma unroll 1
+          for (int c = c_lo; c < c_lo + BN / 2; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(tmem_addr(tmem_base, q * 32, acc * BN + c), r);
+            tmem_ld_wait();
+            tmem_reg_fence16(r);
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+            add_bias16(pr, n * BN + c, v);
+            float part = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) part = fmaf(v[i], v[i], part);
+            if ((c - c_lo) >= p.head_dim) ss1 += part;
+            else ss0 += part;
+          }
+          qk_rstd0 = rsqrtf(ss0 / (float)p.head_dim + kQkNormEps);
+          qk_rstd1 = rsqrtf(ss1 / (float)p.head_dim + kQkNormEps);
+        }
+      }
 #pragma unroll 1
       for (int c = c_lo; c < c_lo + BN / 2; c += 16) {
         uint32_t r[16];
@@ -684,7 +736,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-        epi_row16<EPI>(p, pr, row0 + lane, n * BN + c, v, rope_inv, rope_axis);
+        epi_row16<EPI>(p, pr, row0 + lane, n * BN + c, v, rope_inv, rope_axis, qk_g,
+                       (c - c_lo) >= p.head_dim ? qk_rstd1 : qk_rstd0);
         float4* sp = reinterpret_cast<float4*>(stg + lane * kStageRow);
 #pragma unroll
         for (int i = 0; i < 4; ++i) sp[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);

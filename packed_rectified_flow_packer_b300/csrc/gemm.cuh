@@ -43,6 +43,7 @@ struct GemmParams {
   int H;
   int head_dim;
   int gate_off;           // float offset of the gate chunk inside a (sample, stream) mod row
+  const bf16* qk_norm[2][2];  // [problem][q, k]: QK-RMSNorm scales [head_dim], or null (off)
   bf16* q;                // [N_tok][H] joint order
   bf16* k;
   bf16* v;

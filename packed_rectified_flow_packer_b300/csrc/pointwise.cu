@@ -10,6 +10,8 @@
 // the conditional and unconditional predictions); hyper.ai summary, 方法.
 #include "pointwise.cuh"
 
+#include <algorithm>
+
 namespace mf {
 namespace {
 
@@ -146,20 +148,21 @@ __global__ void __launch_bounds__(128) gemv_kernel(const GemvArgs g) {
 }
 
 // ------------------------------------------------------------------ LN + modulate
-// One warp per row; the row stays in registers as packed bf16 (NV 16-byte chunks per lane),
-// is unpacked once per pass (mean, variance, output), and all NV loads are issued before the
-// first use.  shift / scale rows (f32, shared by every row of a sample) come through L1.
+// Persistent: warp w normalises rows w, w + W, w + 2W, ... (W = warps in the grid, two 128-thread
+// blocks per SM).  A row stays in registers as packed bf16 (NV 16-byte chunks per lane) and is
+// unpacked once per pass (mean, centred variance, output); the NV loads of the warp's next row
+// are issued before the current row is processed, so each warp keeps a row in flight while it
+// computes.  shift / scale rows (f32, shared by every row of a sample) come through L1.
 template <int NV>
-__global__ void __launch_bounds__(128) ln_modulate_kernel(const LnModArgs a) {
-  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= a.rows) return;
-  const int H = a.H;
-  const bool second = r >= a.n_first;
-  const bf16* x = second ? a.x_second + (size_t)(r - a.n_first) * H : a.x_first + (size_t)r * H;
-  uint4 raw[NV];
+__device__ __forceinline__ void ln_load_row(const LnModArgs& a, int r, int lane, uint4 (&raw)[NV]) {
+  const bf16* x = r >= a.n_first ? a.x_second + (size_t)(r - a.n_first) * a.H : a.x_first + (size_t)r * a.H;
 #pragma unroll
   for (int i = 0; i < NV; ++i) raw[i] = ld_stream16(reinterpret_cast<const uint4*>(x) + lane + 32 * i);
+}
+
+template <int NV>
+__device__ __forceinline__ void ln_row(const LnModArgs& a, int r, int lane, const uint4 (&raw)[NV]) {
+  const int H = a.H;
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
@@ -182,7 +185,7 @@ __global__ void __launch_bounds__(128) ln_modulate_kernel(const LnModArgs a) {
   }
   const float rstd = rsqrtf(warp_sum(q) / (float)H + 1e-6f);
   const int seq = __ldg(a.row_seq + r);
-  const float* mrow = a.mod + (size_t)seq * a.seq_stride + (second ? a.stream_stride : 0);
+  const float* mrow = a.mod + (size_t)seq * a.seq_stride + (r >= a.n_first ? a.stream_stride : 0);
   const float4* sh = reinterpret_cast<const float4*>(mrow + a.shift_off);
   const float4* sc = reinterpret_cast<const float4*>(mrow + a.scale_off);
   uint4* out = reinterpret_cast<uint4*>(a.out + (size_t)r * H);
@@ -203,6 +206,26 @@ __global__ void __launch_bounds__(128) ln_modulate_kernel(const LnModArgs a) {
     w.z = pack_bf16x2(o[4], o[5]);
     w.w = pack_bf16x2(o[6], o[7]);
     out[lane + 32 * i] = w;
+  }
+}
+
+template <int NV>
+__global__ void __launch_bounds__(128) ln_modulate_kernel(const LnModArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (r >= a.rows) return;
+  uint4 cur[NV];
+  ln_load_row<NV>(a, r, lane, cur);
+  for (;;) {
+    const int rn = r + nw;
+    uint4 nxt[NV];
+    if (rn < a.rows) ln_load_row<NV>(a, rn, lane, nxt);
+    ln_row<NV>(a, r, lane, cur);
+    if (rn >= a.rows) break;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) cur[i] = nxt[i];
+    r = rn;
   }
 }
 
@@ -455,7 +478,11 @@ cudaError_t launch_gemv2(const bf16* W0, const bf16* b0, int y_off0, const bf16*
 
 cudaError_t launch_ln_modulate(const LnModArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
-  const int blocks = (a.rows + 3) / 4;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int blocks = std::min((a.rows + 3) / 4, 2 * sms);  // two resident blocks per SM
   switch (a.H / 256) {
 #define MF_LN_CASE(nv) \
   case nv: ln_modulate_kernel<nv><<<blocks, 128, 0, st>>>(a); break;

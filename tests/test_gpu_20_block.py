@@ -22,10 +22,10 @@ def _f(t):
 
 
 class Case:
-    def __init__(self, samples, dims, n_blocks, seed, budget=None):
+    def __init__(self, samples, dims, n_blocks, seed, budget=None, qk_norm=False):
         self.samples, self.dims = samples, dims
         self.budget = budget or sum(s.length for s in samples)
-        self.w = synth.model_weights(dims, n_blocks, seed)
+        self.w = synth.model_weights(dims, n_blocks, seed, qk_norm=qk_norm)
         self.batch = synth.batch_inputs(samples, dims, seed)
         self.ref = opack.build_plan(samples, self.budget)
         self.plan = mf.mf_pack(samples, self.budget)
@@ -168,6 +168,22 @@ def test_mid_pack_block(seed):
     samples = _mid_samples(seed)
     case = Case(samples, MID, 1, seed=seed + 10)
     _stack_and_loss(case, 1)
+
+
+def test_tiny_stack_qk_norm():
+    """QK-RMSNorm variant at the tiny size (D = 64: each epilogue warp's 128 columns hold two
+    heads, each normalised on its own)."""
+    case = Case(synth.tiny_samples(), synth.TINY, 1, seed=11, qk_norm=True)
+    _stack_and_loss(case, 1)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_mid_pack_qk_norm(seed):
+    """QK-RMSNorm variant on a ragged H=512 pack (D = 128, one head per epilogue warp), two
+    blocks, text lengths from 0 up."""
+    samples = _mid_samples(seed + 20)
+    case = Case(samples, MID, 2, seed=seed + 30, qk_norm=True)
+    _stack_and_loss(case, 2)
 
 
 def test_mid_edit_stack():
