@@ -186,6 +186,44 @@ def test_mid_pack_qk_norm(seed):
     _stack_and_loss(case, 2)
 
 
+def test_degenerate_samples_stack():
+    """Degenerate samples in one pack: a single image token and no text, one text token and
+    one image token, a 1x3 latent behind 37 text tokens, and flow times at both ends (t = 0:
+    z_t = z; t = 1: z_t = eps)."""
+    samples = [synth.Sample(0, 1, 1, 1, 0.5), synth.Sample(1, 1, 1, 1, 0.2), synth.Sample(37, 1, 1, 3, 0.9),
+               synth.Sample(0, 1, 2, 1, 0.0), synth.Sample(5, 1, 1, 1, 1.0)]
+    case = Case(samples, synth.TINY, 1, seed=13)
+    _stack_and_loss(case, 1)
+
+
+def test_single_sample_full_budget():
+    """One sample that fills the 16384-token budget exactly (no text, 128 x 128 latents) at
+    H=512: attention over a single 16K-token sequence, the largest the budget allows.  Sampled
+    rows of the block output (the oracle computes keys and values of the whole sample and the
+    queried rows only)."""
+    d = MID
+    samples = [synth.Sample(0, 1, 128, 128, 0.35)]
+    case = Case(samples, d, 1, seed=17, budget=16384)
+    ref, H, C = case.ref, d.hidden, d.channels
+    assert ref.n_tok == 16384
+    Z, E = to_f32(case.z_np), to_f32(case.eps_np)
+    ztb = torch.empty((ref.n_img, C), dtype=torch.bfloat16, device="cuda")
+    mf.mf_interpolate(case.plan, C, None, Z, E, None, ztb)
+    x_img = torch.empty((ref.n_img, H), dtype=torch.bfloat16, device="cuda")
+    mf.mf_embed(case.plan, case.model.dims, case.model.embed["w_in"], case.model.embed["b_in"], ztb, x_img)
+    mf.mf_check()
+    emb = _f(x_img)
+    mf.mf_block_forward(case.plan, case.model.dims, case.model.block_structs[0], None, None, x_img,
+                        case.ws.block)
+    mf.mf_check()
+    s = samples[0]
+    c = M.condition(np.float32(s.t), case.w.temb, d.freq_dim)
+    rows = np.array([0, 1, 127, 128, 4095, 8191, 8192, 12345, 16255, 16256, 16383])
+    got = M.block_forward(np.zeros((0, H)), emb, M.image_positions(1, 128, 128), c, case.w.blocks[0],
+                          d.heads, rows=rows)
+    assert_close(_f(x_img)[rows], got, "block output rows of the 16K sample")
+
+
 def test_mid_edit_stack():
     """Editing structure at H=512: 2 frames (clean source, noisy target), 3-axis RoPE, loss on
     target frames only, 2 blocks."""
