@@ -279,19 +279,6 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                : "memory");
 }
 
-// D[tmem of both CTAs] (+)= A[smem of both CTAs] * B[smem of both CTAs]^T, issued by one
-// thread of the even CTA: rows 0..M/2-1 of A and D live in the even CTA, the rest in the odd
-// one; B's rows (N) are split the same way.
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Arrives once on the mbarrier at the same offset in every CTA of `cta_mask` when all
 // tcgen05 operations issued so far by this thread are done.
 __device__ __forceinline__ void mma_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
@@ -334,6 +321,9 @@ __device__ __forceinline__ void mma_commit_if(uint32_t pred, uint64_t* bar) {
       : "memory");
 }
 
+// D[tmem of both CTAs] (+)= A[smem of both CTAs] * B[smem of both CTAs]^T for the lane whose
+// pred is non-zero (the elected lane of the even CTA's MMA warp): rows 0..M/2-1 of A and D live
+// in the even CTA, the rest in the odd one; B's rows (N) are split the same way.
 __device__ __forceinline__ void mma_bf16_pair_if(uint32_t pred, uint32_t d_tmem, uint64_t a_desc,
                                                  uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
