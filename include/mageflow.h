@@ -331,6 +331,26 @@ mf_status mf_flow_loss_noalloc(const mf_plan* plan, int32_t channels, const floa
 mf_status mf_attention(const mf_plan* plan, int32_t heads, int32_t head_dim, const void* d_q,
                        const void* d_k, const void* d_v, void* d_o, void* stream);
 
+/* fp8 variant (a knob of the block's projections; the pages name no fp8 arithmetic).
+ * Per-row E4M3 quantisation: for each row r of d_x (bf16 [M][K], K a multiple of 16),
+ * d_scale[r] = max_k |x[r][k]| / 448 (1 for an all-zero row) and d_q[r][k] =
+ * E4M3(x[r][k] / d_scale[r]) (f32 division, round to nearest even, saturating to +-448;
+ * E4M3: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest finite value 448).
+ * d_q: device uint8 [M][K]; d_scale: device f32 [M].  16-byte aligned pointers.
+ * Errors: MF_ERR_INVALID_ARG, MF_ERR_ALIGNMENT, MF_ERR_CUDA. */
+mf_status mf_quantize_fp8_rows(int32_t M, int32_t K, const void* d_x, void* d_q, float* d_scale,
+                               void* stream);
+
+/* E4M3 GEMM on the tensor cores (tcgen05 kind::f8f6f4, f32 accumulation):
+ * C[m][n] = (sum_k A[m][k] B[n][k]) * a_scale[m] * b_scale[n] + bias[n], C bf16 [M][N].
+ * d_a: uint8 E4M3 codes [M][K], d_b: [N][K] (both K-major, as mf_quantize_fp8_rows writes
+ * them); d_a_scale f32 [M], d_b_scale f32 [N] (16-byte aligned); d_bias bf16 [N] or NULL.
+ * K a multiple of 128, N a multiple of 16.  Errors: MF_ERR_INVALID_ARG, MF_ERR_ALIGNMENT,
+ * MF_ERR_CUDA. */
+mf_status mf_gemm_fp8(int32_t M, int32_t N, int32_t K, const void* d_a, const float* d_a_scale,
+                      const void* d_b, const float* d_b_scale, const void* d_bias, void* d_c,
+                      void* stream);
+
 /* Plain bf16 GEMM on the tensor cores: C[M][N] = A[M][K] B[N][K]^T (+ bias[N]).
  * out_f32 = 0: C bf16, 1: C f32.  K must be a multiple of 64.  bias may be NULL. */
 mf_status mf_gemm(int32_t M, int32_t N, int32_t K, const void* d_a, const void* d_b,
@@ -369,7 +389,8 @@ typedef enum {
   MF_K_GEMM_PLAIN = 9,  /* mf_gemm */
   MF_K_LATENT = 10,     /* interpolate, packed CFG, Euler step */
   MF_K_LOSS = 11,       /* flow-matching loss reduction */
-  MF_K_COUNT = 12
+  MF_K_FP8 = 12,        /* fp8 variant: row quantisation and the E4M3 GEMM */
+  MF_K_COUNT = 13
 } mf_kernel_kind;
 
 typedef struct {

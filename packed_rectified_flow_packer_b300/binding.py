@@ -13,7 +13,7 @@ import os
 
 import numpy as np
 
-__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_gemm", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
+__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmageflow.so")
 
@@ -74,7 +74,7 @@ class mf_trace_entry(C.Structure):
 
 
 KERNEL_KINDS = ("cond", "ln", "gemm_qkv", "attn", "gemm_oproj", "gemm_up", "gemm_down", "gemm_embed",
-                "gemm_final", "gemm_plain", "latent", "loss")
+                "gemm_final", "gemm_plain", "latent", "loss", "fp8")
 
 _P = C.c_void_p
 _S = C.c_int   # mf_status
@@ -103,6 +103,8 @@ _sigs = {
     "mf_nft_loss": (_S, [_P, C.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "mf_attention": (_S, [_P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P]),
     "mf_gemm": (_S, [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P, C.c_int32, _P]),
+    "mf_quantize_fp8_rows": (_S, [C.c_int32, C.c_int32, _P, _P, _P, _P]),
+    "mf_gemm_fp8": (_S, [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "mf_check": (_S, [_P]),
     "mf_selftest_timeout": (_S, [C.c_int32, _P]),
     "mf_trace_enable": (_S, [C.c_int32]),
@@ -320,6 +322,20 @@ def mf_flow_loss_noalloc(plan: Plan, channels: int, z, eps, v, loss_sum, count, 
 def mf_attention(plan: Plan, heads: int, head_dim: int, q, k, v, o, stream=None):
     _ok(lib.mf_attention(plan.handle, heads, head_dim, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                          _stream(stream)), "mf_attention")
+
+
+def mf_quantize_fp8_rows(x, q, scale, stream=None):
+    """x bf16 [M][K] -> q uint8 E4M3 codes [M][K], scale f32 [M]."""
+    M, K = x.shape
+    _ok(lib.mf_quantize_fp8_rows(M, K, _ptr(x), _ptr(q), _ptr(scale), _stream(stream)), "mf_quantize_fp8_rows")
+
+
+def mf_gemm_fp8(a, a_scale, b, b_scale, c, bias=None, stream=None):
+    """c bf16 [M][N] = (a b^T) * a_scale[:, None] * b_scale[None, :] + bias, a / b uint8 E4M3 codes."""
+    M, K = a.shape
+    N = b.shape[0]
+    _ok(lib.mf_gemm_fp8(M, N, K, _ptr(a), _ptr(a_scale), _ptr(b), _ptr(b_scale), _ptr(bias), _ptr(c),
+                        _stream(stream)), "mf_gemm_fp8")
 
 
 def mf_gemm(a, b, c, bias=None, out_f32=False, stream=None):

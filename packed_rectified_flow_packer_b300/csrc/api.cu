@@ -155,6 +155,20 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E4M3 codes [rows][cols] (bytes, row-major, contiguous), boxes of box_rows x 128 columns
+// (128 bytes), 128-byte swizzle, zero fill outside the matrix.
+bool make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ validation helpers
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -260,8 +274,13 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
     const GemmSpec& g = specs[s];
     if (g.M <= 0) continue;
     const int i = p.n_prob;
-    if (!make_tmap(&p.tmA[i], g.A, g.K, g.M, 128)) return MF_ERR_CUDA;
-    if (!make_tmap(&p.tmB[i], g.B, g.K, g.N, pair ? BN / 2 : BN)) return MF_ERR_CUDA;
+    if (epi == mf::kEpiF8Scale) {  // E4M3 operands: byte tensor maps
+      if (!pair || !make_tmap_u8(&p.tmA[i], g.A, g.K, g.M, 128) || !make_tmap_u8(&p.tmB[i], g.B, g.K, g.N, BN / 2))
+        return MF_ERR_CUDA;
+    } else {
+      if (!make_tmap(&p.tmA[i], g.A, g.K, g.M, 128)) return MF_ERR_CUDA;
+      if (!make_tmap(&p.tmB[i], g.B, g.K, g.N, pair ? BN / 2 : BN)) return MF_ERR_CUDA;
+    }
     p.prob[i].M = g.M;
     p.prob[i].N = g.N;
     p.prob[i].K = g.K;
@@ -273,8 +292,8 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
     p.tiles_m[i] = pair ? (g.M + 255) / 256 : (g.M + 127) / 128;
     p.tiles_n[i] = (g.N + BN - 1) / BN;
     p.tma_store[i] = 0;
-    if (pair && (epi == mf::kEpiBiasBf16 || epi == mf::kEpiGelu) && g.ldo == g.N && g.N % 64 == 0 &&
-        aligned(g.out, 16)) {
+    if (pair && (epi == mf::kEpiBiasBf16 || epi == mf::kEpiGelu || epi == mf::kEpiF8Scale) && g.ldo == g.N &&
+        g.N % 64 == 0 && aligned(g.out, 16)) {
       if (!make_tmap(&p.tmC[i], g.out, g.N, g.M, 32)) return MF_ERR_CUDA;
       p.tma_store[i] = 1;
     }
@@ -744,6 +763,39 @@ extern "C" mf_status mf_attention(const mf_plan* p, int32_t heads, int32_t head_
   ap.wait_limit_ns = wait_limit_ns();
   Trace tr(MF_K_ATTN, static_cast<cudaStream_t>(stream), 4.0 * p->sum_L2 * H, 0, 1);
   return cuda_status(mf::launch_attention(ap, head_dim, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" mf_status mf_quantize_fp8_rows(int32_t M, int32_t K, const void* d_x, void* d_q, float* d_scale,
+                                          void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(device_info(&di));
+  if (M < 0 || K <= 0 || K % 16 != 0) return MF_ERR_INVALID_ARG;
+  if (M == 0) return MF_OK;
+  if (d_x == nullptr || d_q == nullptr || d_scale == nullptr) return MF_ERR_INVALID_ARG;
+  if (!aligned(d_x, 16) || !aligned(d_q, 16) || !aligned(d_scale, 4)) return MF_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Trace tr(MF_K_FP8, st, 0, 3.0 * M * (double)K + 4.0 * M, 1);
+  return cuda_status(mf::launch_quantize_e4m3_rows(static_cast<const bf16*>(d_x), M, K,
+                                                   static_cast<uint8_t*>(d_q), d_scale, st));
+}
+
+extern "C" mf_status mf_gemm_fp8(int32_t M, int32_t N, int32_t K, const void* d_a, const float* d_a_scale,
+                                 const void* d_b, const float* d_b_scale, const void* d_bias, void* d_c,
+                                 void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(device_info(&di));
+  if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 16 != 0) return MF_ERR_INVALID_ARG;
+  if (M == 0) return MF_OK;
+  if (d_a == nullptr || d_b == nullptr || d_c == nullptr || d_a_scale == nullptr || d_b_scale == nullptr)
+    return MF_ERR_INVALID_ARG;
+  if (!aligned(d_a, 16) || !aligned(d_b, 16) || !aligned(d_c, 16) || !aligned(d_bias, 16) ||
+      !aligned(d_a_scale, 4) || !aligned(d_b_scale, 16))
+    return MF_ERR_ALIGNMENT;
+  mf::GemmParams gp{};
+  gp.row_scale = d_a_scale;
+  gp.col_scale = d_b_scale;
+  GemmSpec sp[1] = {{M, N, K, d_a, d_b, d_bias, d_c, N, 0, 0}};
+  return run_gemm(sp, 1, mf::kEpiF8Scale, 256, gp, di, static_cast<cudaStream_t>(stream), MF_K_FP8);
 }
 
 extern "C" mf_status mf_gemm(int32_t M, int32_t N, int32_t K, const void* d_a, const void* d_b,

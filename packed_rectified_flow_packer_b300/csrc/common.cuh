@@ -167,6 +167,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
          | ((uint32_t)(M >> 4) << 24);        // M / 16
 }
 
+// Instruction descriptor, kind::f8f6f4: D f32, A and B E4M3 (format code 0), both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                            // D format: f32
+         | (0u << 7)                          // A format: E4M3
+         | (0u << 10)                         // B format: E4M3
+         | ((uint32_t)(N >> 3) << 17)         // N / 8
+         | ((uint32_t)(M >> 4) << 24);        // M / 16
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand (tiles 1024-byte aligned).
 // K-major: rows of 128 B (64 bf16 of K), 8-row groups `sbo` bytes apart; lbo unused.
 // MN-major: 64 contiguous MN elements per 128 B row, K rows at 128 B, 8-row K groups `sbo`
@@ -334,6 +343,19 @@ __device__ __forceinline__ void mma_bf16_pair_if(uint32_t pred, uint32_t d_tmem,
       : "memory");
 }
 
+// As mma_bf16_pair_if with E4M3 operands (kind::f8f6f4, K = 32 per instruction: the same
+// 32 bytes of each 128-byte swizzled row as one bf16 K = 16 step).
+__device__ __forceinline__ void mma_f8_pair_if(uint32_t pred, uint32_t d_tmem, uint64_t a_desc,
+                                               uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_pair_mc_if(uint32_t pred, uint64_t* bar, uint16_t cta_mask) {
   asm volatile(
       "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
@@ -348,6 +370,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Two f32 values to E4M3 codes, round to nearest even, saturating to +-448 (the hardware
+// conversion): lo in bits 7..0, hi in bits 15..8.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  unsigned short d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -190,6 +190,18 @@ __device__ __forceinline__ void epi_row16(const GemmParams& p, const GemmProblem
                                           float (&v)[16], const float* rope_inv, const int* rope_axis,
                                           const bf16* qk_g = nullptr, float qk_rstd = 0.0f) {
   if (row >= pr.M || col0 >= pr.N) return;
+  if constexpr (EPI == kEpiF8Scale) {
+    const float rs = __ldg(p.row_scale + row);
+    const float4* cs = reinterpret_cast<const float4*>(p.col_scale + col0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 c = __ldg(cs + i);
+      v[4 * i + 0] = v[4 * i + 0] * rs * c.x;
+      v[4 * i + 1] = v[4 * i + 1] * rs * c.y;
+      v[4 * i + 2] = v[4 * i + 2] * rs * c.z;
+      v[4 * i + 3] = v[4 * i + 3] * rs * c.w;
+    }
+  }
   add_bias16(pr, col0, v);
   if constexpr (EPI == kEpiGelu) {
 #pragma unroll
@@ -490,7 +502,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
   constexpr uint32_t B_BYTES = (BN / 2) * kBK * 2;    // this CTA's 128 rows of B
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN;
-  constexpr uint32_t IDESC = idesc_bf16_f32(2 * kBM, BN, false);
+  // E4M3 operands (kEpiF8Scale): a 128-byte row of a K block holds 128 elements instead of 64,
+  // and each MMA consumes K = 32 instead of 16; the byte layout of the stages is the same
+  constexpr bool F8 = EPI == kEpiF8Scale;
+  constexpr int KE = F8 ? 2 * kBK : kBK;  // K elements per stage
+  constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(2 * kBM, BN) : idesc_bf16_f32(2 * kBM, BN, false);
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
@@ -556,7 +572,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     for (int tile = pair; ok && tile < total; tile += n_pairs) {
       int pi, m, n;
       decode_tile(p, tile, pi, m, n);
-      const int nkb = p.prob[pi].K / kBK;
+      const int nkb = p.prob[pi].K / KE;
       for (int kb = 0; kb < nkb; ++kb) {
         if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1, lim)) ||
             __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
@@ -567,8 +583,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
           uint8_t* sa = smem + stage * STAGE_BYTES;
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * STAGE_BYTES);
           const uint32_t fb = mapa_shared(&full_bar[stage], 0);
-          tma_load_2d_pair(sa, &p.tmA[pi], kb * kBK, m * 2 * kBM + rank * kBM, fb);
-          tma_load_2d_pair(sa + A_BYTES, &p.tmB[pi], kb * kBK, n * BN + rank * (BN / 2), fb);
+          tma_load_2d_pair(sa, &p.tmA[pi], kb * KE, m * 2 * kBM + rank * kBM, fb);
+          tma_load_2d_pair(sa + A_BYTES, &p.tmB[pi], kb * KE, n * BN + rank * (BN / 2), fb);
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -589,7 +605,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
       for (int tile = pair; ok && tile < total; tile += n_pairs) {
         int pi, m, n;
         decode_tile(p, tile, pi, m, n);
-        const int nkb = p.prob[pi].K / kBK;
+        const int nkb = p.prob[pi].K / KE;
         if (!__all_sync(0xffffffffu, mbar_wait(&tempty_bar[acc], acc_phase ^ 1, lim)) ||
             __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
           ok = false;
@@ -607,7 +623,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
           const uint64_t bd = ad + (A_BYTES >> 4);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_pair_if(el, d_tmem, ad + k * 2, bd + k * 2, IDESC, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (F8)
+              mma_f8_pair_if(el, d_tmem, ad + k * 2, bd + k * 2, IDESC, (kb | k) != 0 ? 1u : 0u);
+            else
+              mma_bf16_pair_if(el, d_tmem, ad + k * 2, bd + k * 2, IDESC, (kb | k) != 0 ? 1u : 0u);
           mma_commit_pair_mc_if(el, &empty_bar[stage], 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -648,7 +667,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
       const GemmProblem& pr = p.prob[pi];
       const int row0 = m * 2 * kBM + rank * kBM + q * 32;  // first of this warp's 32 rows
       float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES) + (warp - 2) * 32 * kStageRow;
-      if constexpr (EPI == kEpiBiasBf16 || EPI == kEpiGelu) {
+      if constexpr (EPI == kEpiBiasBf16 || EPI == kEpiGelu || EPI == kEpiF8Scale) {
         if (p.tma_store[pi]) {
           // bf16 rows of 64 columns, 16-byte chunks swizzled as the 128-byte-swizzle tensor map
           // expects, then one TMA store of 32 rows x 64 columns per group
@@ -812,6 +831,7 @@ cudaError_t launch_gemm_pair(const GemmParams& p, int epi, int num_sms, cudaStre
     case kEpiQkvRope: return launch_pair<kEpiQkvRope>(p, num_sms, stream);
     case kEpiGateResid: return launch_pair<kEpiGateResid>(p, num_sms, stream);
     case kEpiGelu: return launch_pair<kEpiGelu>(p, num_sms, stream);
+    case kEpiF8Scale: return launch_pair<kEpiF8Scale>(p, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }

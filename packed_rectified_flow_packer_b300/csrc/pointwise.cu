@@ -229,6 +229,47 @@ __global__ void __launch_bounds__(128) ln_modulate_kernel(const LnModArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ fp8 quantisation
+// One warp per row; lane l takes the 16-element chunks l, l + 32, ...  Pass 1 finds the row's
+// largest magnitude, pass 2 (the row again, now from L1 / L2) divides and converts.
+__global__ void __launch_bounds__(128) quantize_e4m3_rows_kernel(const bf16* __restrict__ x, int M, int K,
+                                                                 uint8_t* __restrict__ q,
+                                                                 float* __restrict__ s) {
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= M) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)r * K);
+  const int nch = K / 16;
+  float amax = 0.0f;
+  for (int c = lane; c < nch; c += 32) {
+    const uint4 a = __ldg(xr + 2 * c), b = __ldg(xr + 2 * c + 1);
+    float v[16];
+    unpack8(a, *reinterpret_cast<float(*)[8]>(v));
+    unpack8(b, *reinterpret_cast<float(*)[8]>(v + 8));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  uint4* qr = reinterpret_cast<uint4*>(q + (size_t)r * K);
+  for (int c = lane; c < nch; c += 32) {
+    const uint4 a = __ldg(xr + 2 * c), b = __ldg(xr + 2 * c + 1);
+    float v[16];
+    unpack8(a, *reinterpret_cast<float(*)[8]>(v));
+    unpack8(b, *reinterpret_cast<float(*)[8]>(v + 8));
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = pack_e4m3x2(__fdiv_rn(v[4 * i], sc), __fdiv_rn(v[4 * i + 1], sc));
+      const uint32_t hi = pack_e4m3x2(__fdiv_rn(v[4 * i + 2], sc), __fdiv_rn(v[4 * i + 3], sc));
+      w[i] = lo | (hi << 16);
+    }
+    qr[c] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (lane == 0) s[r] = sc;
+}
+
 // ------------------------------------------------------------------ rectified-flow epilogues
 __global__ void interpolate_kernel(const int* __restrict__ img_seq, const int* __restrict__ img_target,
                                    const float* __restrict__ t, int Ni, int C,
@@ -474,6 +515,13 @@ cudaError_t launch_gemv2(const bf16* W0, const bf16* b0, int y_off0, const bf16*
                          cudaStream_t st, int* launches) {
   GemvArgs g{{W0, W1}, {b0, b1}, {y_off0, y_off1}, x, 0, O, y, y_stride};
   return gemv_groups(g, 2, K, 0, x, y, S, st, launches);
+}
+
+cudaError_t launch_quantize_e4m3_rows(const bf16* x, int M, int K, uint8_t* q, float* s, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  if (K <= 0 || K % 16 != 0) return cudaErrorInvalidValue;
+  quantize_e4m3_rows_kernel<<<(M + 3) / 4, 128, 0, st>>>(x, M, K, q, s);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_ln_modulate(const LnModArgs& a, cudaStream_t st) {

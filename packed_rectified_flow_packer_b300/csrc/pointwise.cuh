@@ -21,6 +21,11 @@ cudaError_t launch_gemv2(const bf16* W0, const bf16* b0, int y_off0, const bf16*
                          int y_off1, const float* x, int S, int K, int O, float* y, int y_stride,
                          cudaStream_t st, int* launches = nullptr);
 
+// Per-row E4M3 quantisation of x bf16 [M][K] (K multiple of 16): s[r] = amax(|x[r]|) / 448
+// (1 for an all-zero row), q[r][k] = E4M3(x[r][k] / s[r]) with the division correctly rounded
+// in f32 and the conversion rounding to nearest even, saturating to +-448.
+cudaError_t launch_quantize_e4m3_rows(const bf16* x, int M, int K, uint8_t* q, float* s, cudaStream_t st);
+
 // out[r] = LN(x[r]) (1 + scale) + shift for stream-sorted rows r in [0, rows), where rows
 // below n_first come from x_first and the rest from x_second; (shift, scale) of row r are
 // read at mod + seq(r) * seq_stride + stream(r) * stream_stride + {shift_off, scale_off},

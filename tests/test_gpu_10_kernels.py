@@ -205,3 +205,48 @@ def test_nft_loss(case):
     np.testing.assert_array_equal(cnt.cpu().numpy(), counts)
     want = M.mean_loss(sums, counts)
     assert abs(mean.item() - want) <= 1e-12 * abs(want)
+
+
+# ------------------------------------------------------------------ fp8 variant
+@pytest.mark.parametrize("M_,K_", [(1, 16), (300, 1024), (77, 3072)])
+def test_quantize_fp8_rows(M_, K_):
+    """Per-row E4M3 quantisation: scales and codes equal the oracle's exactly (codes compared
+    as values, so -0 and +0 agree), with an all-zero row, a row of huge and a row of tiny
+    values."""
+    from oracle import fp8 as F
+    g = np.random.default_rng(M_ + K_)
+    x = synth.round_bf16(g.normal(0, 2, (M_, K_)).astype(np.float32))
+    if M_ > 3:
+        x[1] = 0.0
+        x[2] = synth.round_bf16(x[2] * 1e3)
+        x[3] = synth.round_bf16(x[3] * 1e-4)
+    xd = to_bf16(x)
+    q = torch.empty((M_, K_), dtype=torch.uint8, device="cuda")
+    s = torch.empty(M_, dtype=torch.float32, device="cuda")
+    mf.mf_quantize_fp8_rows(xd, q, s)
+    mf.mf_check()
+    codes, scale = F.quantize_rows(x)
+    np.testing.assert_array_equal(s.cpu().numpy(), scale)
+    np.testing.assert_array_equal(F.e4m3_decode(q.cpu().numpy()), F.e4m3_decode(codes))
+
+
+@pytest.mark.parametrize("M_,N_,K_,with_bias", [(1, 256, 128, False), (257, 384, 512, True),
+                                                (1000, 512, 1024, True), (300, 3072, 3072, True)])
+def test_gemm_fp8(M_, N_, K_, with_bias):
+    """E4M3 GEMM (kind::f8f6f4 on CTA pairs) against the oracle's fp64 product of the same codes
+    and scales.  N = 384 takes the staged epilogue (no 64-column TMA store boxes), the others the
+    TMA-store one; M = 1 and 257 leave ragged row tiles."""
+    from oracle import fp8 as F
+    g = np.random.default_rng(M_ * 7 + N_)
+    a, sa = F.quantize_rows(synth.round_bf16(g.normal(0, 1, (M_, K_)).astype(np.float32)))
+    b, sb = F.quantize_rows(synth.round_bf16(g.normal(0, 0.02, (N_, K_)).astype(np.float32)))
+    bias = synth.round_bf16(g.normal(0, 0.1, N_).astype(np.float32)) if with_bias else None
+    c = torch.empty((M_, N_), dtype=torch.bfloat16, device="cuda")
+    mf.mf_gemm_fp8(torch.from_numpy(a).cuda(), torch.from_numpy(sa).cuda(), torch.from_numpy(b).cuda(),
+                   torch.from_numpy(sb).cuda(), c, None if bias is None else to_bf16(bias))
+    mf.mf_check()
+    ref = F.linear_fp8(a, sa, b, sb, bias)
+    got = _bf16_np(c).astype(np.float64)
+    assert_close(got, ref, "fp8 gemm")
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max()   # one bf16 rounding + f32 sums
+    assert np.all(np.abs(got - ref) <= bound)
