@@ -44,8 +44,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=120)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["native16k", "cfg"], default="native16k",
-                    help="native16k: the headline block-forward pack; cfg: packed vs unpacked CFG sampler")
+    ap.add_argument("--workload", choices=["native16k", "cfg", "gemm"], default="native16k",
+                    help="native16k: the headline block-forward pack; cfg: packed vs unpacked CFG sampler; "
+                         "gemm: bf16 and fp8 GEMMs alone at the block's shapes")
     return ap.parse_args()
 
 
@@ -460,6 +461,63 @@ def run_mageflow(args, rank, world, local_rank):
 
 
 # ---------------------------------------------------------------- packed vs unpacked CFG sampler
+def run_gemm_shapes(args, rank, world, local_rank):
+    """The block's four projections as plain GEMMs at the 16K pack's row count (M = 15744, the
+    mean of the seeded packs), bf16 (`mf_gemm`) and fp8 (`mf_gemm_fp8` on operands the library
+    quantised per row), CUDA events around K launches after W warm-up launches each; the
+    quantiser is timed on its own.  Random N(0, 0.5) activations and N(0, 0.02) weights."""
+    import torch
+    import packed_rectified_flow_packer_b300 as mf
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    H, M = synth.FULL.hidden, 15744
+    g = torch.Generator(device=dev).manual_seed(0)
+    peaks = read_peaks()
+    shapes = {"qkv": (3 * H, H), "oproj": (H, H), "up": (4 * H, H), "down": (H, 4 * H)}
+    out = {}
+    for name, (N, K) in shapes.items():
+        a = (torch.randn((M, K), device=dev, generator=g) * 0.5).to(torch.bfloat16)
+        b = (torch.randn((N, K), device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        aq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        bq = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        sa = torch.empty(M, dtype=torch.float32, device=dev)
+        sb = torch.empty(N, dtype=torch.float32, device=dev)
+        mf.mf_quantize_fp8_rows(b, bq, sb)
+        c8 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        c16 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        mf.mf_quantize_fp8_rows(a, aq, sa)
+        row = {}
+        for tag, fn in (("fp8", lambda: mf.mf_gemm_fp8(aq, sa, bq, sb, c8)),
+                        ("bf16", lambda: mf.mf_gemm(a, b, c16)),
+                        ("quantize", lambda: mf.mf_quantize_fp8_rows(a, aq, sa))):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / args.steps
+            if tag == "quantize":
+                row["quantize_us"] = round(ms * 1e3, 2)
+                row["quantize_gbs"] = round(3.0 * M * K / ms / 1e6, 1)
+            else:
+                row[f"{tag}_ms"] = round(ms, 4)
+                row[f"{tag}_tflops"] = round(2.0 * M * N * K / ms / 1e9, 1)
+        mf.mf_check()
+        row["M"], row["N"], row["K"] = M, N, K
+        out[name] = row
+    if rank != 0:
+        return None
+    bf = peaks["bf16_tflops"]
+    return {"metric": "GEMM TFLOP/s at the block's shapes (bf16 and fp8 E4M3), 1xB300", "workload": "gemm",
+            "steps": args.steps, "warmup": args.warmup, "shapes": out,
+            "peaks": {"bf16_tflops": bf, "fp8_tflops_from_bf16x2": round(2 * bf, 1), "source": peaks["source"]},
+            "data": "synthetic (N(0,0.5) activations, N(0,0.02) weights)"}
+
+
 def run_cfg_sampler(args, rank, world, local_rank):
     """4-block stack, two prompts (1024x1024 and 768x1344, 256 text tokens when conditional),
     4 Euler steps from t = 1 to 0, guidance w = 4.  Packed: cond and uncond branches of both
@@ -615,6 +673,8 @@ def main():
         line = run_reference(args, rank, world)
     elif args.workload == "cfg":
         line = run_cfg_sampler(args, rank, world, local_rank)
+    elif args.workload == "gemm":
+        line = run_gemm_shapes(args, rank, world, local_rank)
     else:
         line = run_mageflow(args, rank, world, local_rank)
     if rank == 0 and line is not None:
