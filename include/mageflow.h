@@ -228,6 +228,37 @@ mf_status mf_block_forward(const mf_plan* plan, const mf_dims* dims, const mf_bl
                            const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
                            size_t ws_bytes, void* stream);
 
+/* fp8 variant of the block (the pages name no fp8 arithmetic; see mf_gemm_fp8): the E4M3
+ * codes of one stream's four projection matrices, as mf_quantize_fp8_rows writes them from the
+ * bf16 weights (rows = output features), and their per-row scales. */
+typedef struct {
+  const void* q_qkv; const float* s_qkv;   /* [3H][H] codes, [3H] */
+  const void* q_o;   const float* s_o;     /* [H][H],  [H]  */
+  const void* q_1;   const float* s_1;     /* [rH][H], [rH] */
+  const void* q_2;   const float* s_2;     /* [H][rH], [H]  */
+} mf_stream_weights_fp8;
+
+typedef struct {
+  mf_stream_weights_fp8 txt;
+  mf_stream_weights_fp8 img;
+} mf_block_weights_fp8;
+
+/* Workspace of mf_block_forward_fp8: the block workspace (same layout, same offsets) plus the
+ * E4M3 codes and row scales of one projection input at a time. */
+size_t mf_block_fp8_workspace_bytes(const mf_plan* plan, const mf_dims* dims);
+
+/* mf_block_forward with the four projections on E4M3 operands: each projection input (a, the
+ * attention output o, the second a, the GELU output) is quantised per row as
+ * mf_quantize_fp8_rows does, right before its GEMM, and multiplied with w8's codes
+ * (tcgen05 kind::f8f6f4, f32 accumulation); the row and column scales are applied in the
+ * epilogue before the bias, RoPE, GELU or gated residual, which are unchanged.  w supplies
+ * everything else (timestep MLP, modulation, biases, optional QK-RMSNorm scales); its bf16
+ * projection matrices are not read.  d_ws: mf_block_fp8_workspace_bytes() bytes.
+ * Errors: as mf_block_forward. */
+mf_status mf_block_forward_fp8(const mf_plan* plan, const mf_dims* dims, const mf_block_weights* w,
+                               const mf_block_weights_fp8* w8, const float* d_t, void* d_x_txt,
+                               void* d_x_img, void* d_ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------------------ */
 /* Latent embed and final layer (stack ends)  [PR 2.2(2)]                                */
 /* ------------------------------------------------------------------------------------ */

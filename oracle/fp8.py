@@ -79,3 +79,29 @@ def linear_fp8(a_codes, a_scale, b_codes, b_scale, bias=None):
     if bias is not None:
         y = y + np.asarray(bias, np.float64)[None, :]
     return y
+
+
+def bf16_round(x):
+    """float64 values rounded to the nearest bfloat16 (ties to even), as float64: the value a
+    bf16 activation buffer holds."""
+    f = np.asarray(x, dtype=np.float32)
+    b = f.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def linear_fp8_act(x, w8: dict, name: str, bias):
+    """The fp8 variant's projection of activations x (float64 [L][K]): x is stored in bf16,
+    quantised per row, and multiplied with the weight codes w8['q_' + name] and scales
+    w8['s_' + name] (quantised per output row from the bf16 weights)."""
+    codes, s = quantize_rows(bf16_round(x).astype(np.float32))
+    return linear_fp8(codes, s, w8["q_" + name], w8["s_" + name], bias)
+
+
+def quantize_weights(bw_stream: dict):
+    """E4M3 codes and row scales of one stream's four projection matrices (float32 arrays
+    exactly representable in bf16)."""
+    out = {}
+    for name, key in (("qkv", "w_qkv"), ("o", "w_o"), ("1", "w_1"), ("2", "w_2")):
+        out["q_" + name], out["s_" + name] = quantize_rows(np.asarray(bw_stream[key], np.float32))
+    return out

@@ -161,16 +161,27 @@ def attention(q, k, v, rows=None):
 
 
 # ------------------------------------------------------------------ the block
-def block_forward(x_txt, x_img, pos_img, c, bw: dict, heads: int, rows=None):
+def _proj(x, bw_s: dict, w8_s, name: str):
+    """x W^T + b of one stream's projection `name` (qkv, o, 1, 2); with w8_s (the fp8
+    variant's codes and scales of that stream) on E4M3 operands, as oracle.fp8 defines them."""
+    if w8_s is None:
+        return linear(x, bw_s["w_" + name], bw_s["b_" + name])
+    from oracle import fp8
+    return fp8.linear_fp8_act(x, w8_s, name, bw_s["b_" + name])
+
+
+def block_forward(x_txt, x_img, pos_img, c, bw: dict, heads: int, rows=None, w8=None):
     """One NR-MMDiT block over ONE sample.
 
     x_txt [Lt][H], x_img [Li][H]: the sample's text and image tokens; pos_img [Li][3];
     c [H]: SiLU(temb) of the sample; bw[stream][name]: the stream's weights.
     Text rows use the text weights and image rows the image weights; attention is joint over
     [text | image] in that order.  `rows` (joint indices) selects which output rows to
-    compute; the keys and values always cover the whole sample.
+    compute; the keys and values always cover the whole sample.  `w8` ({stream: codes and
+    scales}) selects the fp8 variant of the four projections.
     Returns (x_txt_out, x_img_out), or the selected joint rows [len(rows)][H] if `rows`.
     """
+    w8 = w8 or {s: None for s in STREAMS}
     x = {"txt": f64(x_txt), "img": f64(x_img)}
     Lt, Li = len(x["txt"]), len(x["img"])
     H = (x["txt"] if Lt else x["img"]).shape[1]
@@ -179,7 +190,7 @@ def block_forward(x_txt, x_img, pos_img, c, bw: dict, heads: int, rows=None):
     mod = {s: dict(zip(MOD_CHUNKS, modulation(c, bw[s]["w_mod"], bw[s]["b_mod"], 6)))
            for s in STREAMS}
     a = {s: modulate(x[s], mod[s]["shift1"], mod[s]["scale1"]) for s in STREAMS}
-    qkv = np.concatenate([linear(a[s], bw[s]["w_qkv"], bw[s]["b_qkv"]) for s in STREAMS])
+    qkv = np.concatenate([_proj(a[s], bw[s], w8[s], "qkv") for s in STREAMS])
     q, k, v = (qkv[:, i * H:(i + 1) * H].reshape(L, heads, D) for i in range(3))
     if any("w_qnorm" in bw[s] for s in STREAMS):
         # QK-RMSNorm variant: each stream's rows with that stream's scales (text rows first)
@@ -199,9 +210,9 @@ def block_forward(x_txt, x_img, pos_img, c, bw: dict, heads: int, rows=None):
             continue
         xs = x["txt"][sel[m]] if s == "txt" else x["img"][sel[m] - Lt]
         w = bw[s]
-        xs = xs + mod[s]["gate1"] * linear(o[m], w["w_o"], w["b_o"])
-        h = gelu(linear(modulate(xs, mod[s]["shift2"], mod[s]["scale2"]), w["w_1"], w["b_1"]))
-        out[m] = xs + mod[s]["gate2"] * linear(h, w["w_2"], w["b_2"])
+        xs = xs + mod[s]["gate1"] * _proj(o[m], w, w8[s], "o")
+        h = gelu(_proj(modulate(xs, mod[s]["shift2"], mod[s]["scale2"]), w, w8[s], "1"))
+        out[m] = xs + mod[s]["gate2"] * _proj(h, w, w8[s], "2")
     if rows is not None:
         return out
     return out[:Lt], out[Lt:]

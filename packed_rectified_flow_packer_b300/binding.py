@@ -13,7 +13,7 @@ import os
 
 import numpy as np
 
-__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
+__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_block_fp8_workspace_bytes", "mf_block_forward_fp8", "block_struct_fp8", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmageflow.so")
 
@@ -68,6 +68,17 @@ class mf_block_weights(C.Structure):
     _fields_ = [("temb", mf_temb_weights), ("txt", mf_stream_weights), ("img", mf_stream_weights)]
 
 
+STREAM_FP8_FIELDS = ("q_qkv", "s_qkv", "q_o", "s_o", "q_1", "s_1", "q_2", "s_2")
+
+
+class mf_stream_weights_fp8(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in STREAM_FP8_FIELDS]
+
+
+class mf_block_weights_fp8(C.Structure):
+    _fields_ = [("txt", mf_stream_weights_fp8), ("img", mf_stream_weights_fp8)]
+
+
 class mf_trace_entry(C.Structure):
     _fields_ = [("launches", C.c_int64), ("ms", C.c_double), ("flops", C.c_double),
                 ("bytes", C.c_double)]
@@ -105,6 +116,8 @@ _sigs = {
     "mf_gemm": (_S, [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P, C.c_int32, _P]),
     "mf_quantize_fp8_rows": (_S, [C.c_int32, C.c_int32, _P, _P, _P, _P]),
     "mf_gemm_fp8": (_S, [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
+    "mf_block_fp8_workspace_bytes": (C.c_size_t, [_P, _P]),
+    "mf_block_forward_fp8": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "mf_check": (_S, [_P]),
     "mf_selftest_timeout": (_S, [C.c_int32, _P]),
     "mf_trace_enable": (_S, [C.c_int32]),
@@ -255,6 +268,24 @@ def mf_block_forward(plan: Plan, dims, weights: mf_block_weights, t, x_txt, x_im
     nbytes = ws_bytes if ws_bytes is not None else (ws.numel() * ws.element_size() if ws is not None else 0)
     _ok(lib.mf_block_forward(plan.handle, C.byref(_dims(dims)), C.byref(weights), _ptr(t), _ptr(x_txt),
                              _ptr(x_img), _ptr(ws), nbytes, _stream(stream)), "mf_block_forward")
+
+
+def block_struct_fp8(txt8, img8) -> mf_block_weights_fp8:
+    """txt8, img8: dicts q_* (uint8 codes) / s_* (f32 scales) -> device tensors."""
+    return mf_block_weights_fp8(mf_stream_weights_fp8(*[_ptr(txt8[k]) for k in STREAM_FP8_FIELDS]),
+                                mf_stream_weights_fp8(*[_ptr(img8[k]) for k in STREAM_FP8_FIELDS]))
+
+
+def mf_block_fp8_workspace_bytes(plan: Plan, dims) -> int:
+    return lib.mf_block_fp8_workspace_bytes(plan.handle, C.byref(_dims(dims)))
+
+
+def mf_block_forward_fp8(plan: Plan, dims, weights: mf_block_weights, weights8: mf_block_weights_fp8, t,
+                         x_txt, x_img, ws, ws_bytes=None, stream=None):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _ok(lib.mf_block_forward_fp8(plan.handle, C.byref(_dims(dims)), C.byref(weights), C.byref(weights8), _ptr(t),
+                                 _ptr(x_txt), _ptr(x_img), _ptr(ws), nbytes, _stream(stream)),
+        "mf_block_forward_fp8")
 
 
 def mf_embed(plan: Plan, dims, w_in, b_in, zt, x_img, stream=None):

@@ -233,6 +233,13 @@ BlockLayout block_layout(const mf_plan* p, const mf_dims* d) {
   return L;
 }
 
+// fp8 block forward: E4M3 codes of one projection input at a time ([N][mlp_ratio H] bytes at
+// most) and their row scales ([N] f32), after the bf16 workspace.
+size_t fp8_region_bytes(const mf_plan* p, const mf_dims* d) {
+  const size_t N = p->N, R = (size_t)d->mlp_ratio * d->hidden;
+  return al256(N * R) + al256(N * 4);
+}
+
 struct FinalLayout {
   size_t c, fmod, a, sinus, h1, total;
 };
@@ -261,6 +268,7 @@ struct GemmSpec {
   int ldo;
   int row_off;
   int stream;
+  const float* col_scale;  // E4M3 operands (kEpiF8): per-column dequantisation scale of B
 };
 
 mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmParams& p,
@@ -274,7 +282,7 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
     const GemmSpec& g = specs[s];
     if (g.M <= 0) continue;
     const int i = p.n_prob;
-    if (epi == mf::kEpiF8Scale) {  // E4M3 operands: byte tensor maps
+    if (epi & mf::kEpiF8) {  // E4M3 operands: byte tensor maps
       if (!pair || !make_tmap_u8(&p.tmA[i], g.A, g.K, g.M, 128) || !make_tmap_u8(&p.tmB[i], g.B, g.K, g.N, BN / 2))
         return MF_ERR_CUDA;
     } else {
@@ -288,12 +296,14 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
     p.prob[i].stream = g.stream;
     p.prob[i].ldo = g.ldo;
     p.prob[i].bias = static_cast<const bf16*>(g.bias);
+    p.prob[i].col_scale = g.col_scale;
     p.prob[i].out = g.out;
     p.tiles_m[i] = pair ? (g.M + 255) / 256 : (g.M + 127) / 128;
     p.tiles_n[i] = (g.N + BN - 1) / BN;
     p.tma_store[i] = 0;
-    if (pair && (epi == mf::kEpiBiasBf16 || epi == mf::kEpiGelu || epi == mf::kEpiF8Scale) && g.ldo == g.N &&
-        g.N % 64 == 0 && aligned(g.out, 16)) {
+    const int base = epi & ~mf::kEpiF8;
+    if (pair && (base == mf::kEpiBiasBf16 || base == mf::kEpiGelu) && g.ldo == g.N && g.N % 64 == 0 &&
+        aligned(g.out, 16)) {
       if (!make_tmap(&p.tmC[i], g.out, g.N, g.M, 32)) return MF_ERR_CUDA;
       p.tma_store[i] = 1;
     }
@@ -435,9 +445,20 @@ extern "C" mf_status mf_block_workspace_layout(const mf_plan* p, const mf_dims* 
   return MF_OK;
 }
 
-extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weights* w,
-                                      const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
-                                      size_t ws_bytes, void* stream) {
+namespace {
+bool stream8_ok(const mf_stream_weights_fp8& s) {
+  const void* ptrs[] = {s.q_qkv, s.s_qkv, s.q_o, s.s_o, s.q_1, s.s_1, s.q_2, s.s_2};
+  for (const void* q : ptrs)
+    if (q == nullptr || !aligned(q, 16)) return false;
+  return true;
+}
+
+// The block forward; with w8 the four projections run on E4M3 operands: each input (a, o, a,
+// hidden) is quantised per row right before its GEMM, into the fp8 region after the bf16
+// workspace.
+mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weights* w,
+                        const mf_block_weights_fp8* w8, const float* d_t, void* d_x_txt, void* d_x_img,
+                        void* d_ws, size_t ws_bytes, void* stream) {
   DevInfo* di = nullptr;
   int dev = -1;
   MF_TRY(device_info(&di, &dev));
@@ -445,13 +466,15 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
   MF_TRY(check_dims(d));
   if (w == nullptr || !temb_ok(&w->temb) || !stream_ok(w->txt) || !stream_ok(w->img))
     return MF_ERR_INVALID_ARG;
+  if (w8 != nullptr && (!stream8_ok(w8->txt) || !stream8_ok(w8->img))) return MF_ERR_INVALID_ARG;
   if (p->N == 0) return MF_OK;
   if ((p->Nt > 0 && d_x_txt == nullptr) || (p->Ni > 0 && d_x_img == nullptr) || d_ws == nullptr)
     return MF_ERR_INVALID_ARG;
   if (!aligned(d_x_txt, 16) || !aligned(d_x_img, 16) || !aligned(d_ws, 256) || !aligned(d_t, 4))
     return MF_ERR_ALIGNMENT;
   const BlockLayout L = block_layout(p, d);
-  if (ws_bytes < L.total) return MF_ERR_WORKSPACE;
+  const size_t fp8_bytes = w8 ? fp8_region_bytes(p, d) : 0;
+  if (ws_bytes < L.total + fp8_bytes) return MF_ERR_WORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(d_ws);
@@ -470,6 +493,14 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
   float* h1 = reinterpret_cast<float*>(ws + L.h1);
   bf16* xt = static_cast<bf16*>(d_x_txt);
   bf16* xi = static_cast<bf16*>(d_x_img);
+  // fp8: codes of the current projection input [N][<= R] and their row scales [N]
+  uint8_t* q8 = reinterpret_cast<uint8_t*>(ws + L.total);
+  float* s8 = reinterpret_cast<float*>(ws + L.total + al256((size_t)N * R));
+  const int F8 = w8 ? mf::kEpiF8 : 0;
+  auto quantize = [&](const bf16* src, int K) -> mf_status {
+    Trace tr(MF_K_FP8, st, 0, 3.0 * N * (double)K, 1);
+    return cuda_status(mf::launch_quantize_e4m3_rows(src, N, K, q8, s8, st));
+  };
 
   // 1. timestep condition c = SiLU(temb(t)) and the per-sample adaLN modulation of both streams
   MF_TRY(conditioning(p, d, &w->temb, t, sinus, h1, c, st));
@@ -503,7 +534,14 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
   gp.qk_norm[0][1] = static_cast<const bf16*>(w->txt.w_knorm);
   gp.qk_norm[1][0] = static_cast<const bf16*>(w->img.w_qnorm);
   gp.qk_norm[1][1] = static_cast<const bf16*>(w->img.w_knorm);
-  {
+  gp.row_scale = s8;
+  if (w8) {
+    MF_TRY(quantize(a, H));
+    GemmSpec sp[2] = {{Nt, 3 * H, H, q8, w8->txt.q_qkv, w->txt.b_qkv, nullptr, 0, 0, 0, w8->txt.s_qkv},
+                      {Ni, 3 * H, H, q8 + (size_t)Nt * H, w8->img.q_qkv, w->img.b_qkv, nullptr, 0, Nt, 1,
+                       w8->img.s_qkv}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiQkvRope | F8, 256, gp, di, st, MF_K_GEMM_QKV));
+  } else {
     GemmSpec sp[2] = {{Nt, 3 * H, H, a, w->txt.w_qkv, w->txt.b_qkv, nullptr, 0, 0, 0},
                       {Ni, 3 * H, H, a + (size_t)Nt * H, w->img.w_qkv, w->img.b_qkv, nullptr, 0, Nt, 1}};
     MF_TRY(run_gemm(sp, 2, mf::kEpiQkvRope, 256, gp, di, st, MF_K_GEMM_QKV));
@@ -531,7 +569,12 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
 
   // 5. x += gate1 (o W_o^T + b_o)
   gp.gate_off = 2 * H;
-  {
+  if (w8) {
+    MF_TRY(quantize(o, H));
+    GemmSpec sp[2] = {{Nt, H, H, q8, w8->txt.q_o, w->txt.b_o, xt, H, 0, 0, w8->txt.s_o},
+                      {Ni, H, H, q8 + (size_t)Nt * H, w8->img.q_o, w->img.b_o, xi, H, Nt, 1, w8->img.s_o}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid | F8, 256, gp, di, st, MF_K_GEMM_OPROJ));
+  } else {
     GemmSpec sp[2] = {{Nt, H, H, o, w->txt.w_o, w->txt.b_o, xt, H, 0, 0},
                       {Ni, H, H, o + (size_t)Nt * H, w->img.w_o, w->img.b_o, xi, H, Nt, 1}};
     MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid, 256, gp, di, st, MF_K_GEMM_OPROJ));
@@ -546,7 +589,13 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
   }
 
   // 7. hidden = GELU(a W_1^T + b_1)
-  {
+  if (w8) {
+    MF_TRY(quantize(a, H));
+    GemmSpec sp[2] = {{Nt, R, H, q8, w8->txt.q_1, w->txt.b_1, hid, R, 0, 0, w8->txt.s_1},
+                      {Ni, R, H, q8 + (size_t)Nt * H, w8->img.q_1, w->img.b_1, hid + (size_t)Nt * R, R, Nt, 1,
+                       w8->img.s_1}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGelu | F8, 256, gp, di, st, MF_K_GEMM_UP));
+  } else {
     GemmSpec sp[2] = {{Nt, R, H, a, w->txt.w_1, w->txt.b_1, hid, R, 0, 0},
                       {Ni, R, H, a + (size_t)Nt * H, w->img.w_1, w->img.b_1, hid + (size_t)Nt * R, R, Nt, 1}};
     MF_TRY(run_gemm(sp, 2, mf::kEpiGelu, 256, gp, di, st, MF_K_GEMM_UP));
@@ -554,12 +603,36 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
 
   // 8. x += gate2 (hidden W_2^T + b_2)
   gp.gate_off = 5 * H;
-  {
+  if (w8) {
+    MF_TRY(quantize(hid, R));
+    GemmSpec sp[2] = {{Nt, H, R, q8, w8->txt.q_2, w->txt.b_2, xt, H, 0, 0, w8->txt.s_2},
+                      {Ni, H, R, q8 + (size_t)Nt * R, w8->img.q_2, w->img.b_2, xi, H, Nt, 1, w8->img.s_2}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid | F8, 256, gp, di, st, MF_K_GEMM_DOWN));
+  } else {
     GemmSpec sp[2] = {{Nt, H, R, hid, w->txt.w_2, w->txt.b_2, xt, H, 0, 0},
                       {Ni, H, R, hid + (size_t)Nt * R, w->img.w_2, w->img.b_2, xi, H, Nt, 1}};
     MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid, 256, gp, di, st, MF_K_GEMM_DOWN));
   }
   return MF_OK;
+}
+}  // namespace
+
+extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weights* w,
+                                      const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
+                                      size_t ws_bytes, void* stream) {
+  return block_forward(p, d, w, nullptr, d_t, d_x_txt, d_x_img, d_ws, ws_bytes, stream);
+}
+
+extern "C" size_t mf_block_fp8_workspace_bytes(const mf_plan* p, const mf_dims* d) {
+  if (p == nullptr || check_dims(d) != MF_OK) return 0;
+  return block_layout(p, d).total + fp8_region_bytes(p, d);
+}
+
+extern "C" mf_status mf_block_forward_fp8(const mf_plan* p, const mf_dims* d, const mf_block_weights* w,
+                                          const mf_block_weights_fp8* w8, const float* d_t, void* d_x_txt,
+                                          void* d_x_img, void* d_ws, size_t ws_bytes, void* stream) {
+  if (w8 == nullptr) return MF_ERR_INVALID_ARG;
+  return block_forward(p, d, w, w8, d_t, d_x_txt, d_x_img, d_ws, ws_bytes, stream);
 }
 
 // ====================================================================== embed / final
@@ -793,9 +866,9 @@ extern "C" mf_status mf_gemm_fp8(int32_t M, int32_t N, int32_t K, const void* d_
     return MF_ERR_ALIGNMENT;
   mf::GemmParams gp{};
   gp.row_scale = d_a_scale;
-  gp.col_scale = d_b_scale;
-  GemmSpec sp[1] = {{M, N, K, d_a, d_b, d_bias, d_c, N, 0, 0}};
-  return run_gemm(sp, 1, mf::kEpiF8Scale, 256, gp, di, static_cast<cudaStream_t>(stream), MF_K_FP8);
+  GemmSpec sp[1] = {{M, N, K, d_a, d_b, d_bias, d_c, N, 0, 0, d_b_scale}};
+  return run_gemm(sp, 1, mf::kEpiBiasBf16 | mf::kEpiF8, 256, gp, di, static_cast<cudaStream_t>(stream),
+                  MF_K_FP8);
 }
 
 extern "C" mf_status mf_gemm(int32_t M, int32_t N, int32_t K, const void* d_a, const void* d_b,

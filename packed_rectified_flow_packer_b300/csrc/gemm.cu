@@ -189,10 +189,11 @@ template <int EPI>
 __device__ __forceinline__ void epi_row16(const GemmParams& p, const GemmProblem& pr, int row, int col0,
                                           float (&v)[16], const float* rope_inv, const int* rope_axis,
                                           const bf16* qk_g = nullptr, float qk_rstd = 0.0f) {
+  constexpr int E = EPI & 7;
   if (row >= pr.M || col0 >= pr.N) return;
-  if constexpr (EPI == kEpiF8Scale) {
-    const float rs = __ldg(p.row_scale + row);
-    const float4* cs = reinterpret_cast<const float4*>(p.col_scale + col0);
+  if constexpr ((EPI & kEpiF8) != 0) {
+    const float rs = __ldg(p.row_scale + pr.row_off + row);
+    const float4* cs = reinterpret_cast<const float4*>(pr.col_scale + col0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float4 c = __ldg(cs + i);
@@ -203,10 +204,10 @@ __device__ __forceinline__ void epi_row16(const GemmParams& p, const GemmProblem
     }
   }
   add_bias16(pr, col0, v);
-  if constexpr (EPI == kEpiGelu) {
+  if constexpr (E == kEpiGelu) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.7071067811865476f));
-  } else if constexpr (EPI == kEpiQkvRope) {
+  } else if constexpr (E == kEpiQkvRope) {
     const int which = col0 / p.H;
     if (qk_g != nullptr) {
       const uint4* gp = reinterpret_cast<const uint4*>(qk_g + (col0 - which * p.H) % p.head_dim);
@@ -248,8 +249,9 @@ __device__ __forceinline__ void epi_row16(const GemmParams& p, const GemmProblem
 template <int EPI>
 __device__ __forceinline__ void epi_store8(const GemmParams& p, const GemmProblem& pr, int row, int col,
                                            const float4& a, const float4& b) {
+  constexpr int E = EPI & 7;
   if (row >= pr.M || col >= pr.N) return;
-  if constexpr (EPI == kEpiBiasF32) {
+  if constexpr (E == kEpiBiasF32) {
     float4* o = reinterpret_cast<float4*>(static_cast<float*>(pr.out) + (size_t)row * pr.ldo + col);
     o[0] = a;
     o[1] = b;
@@ -257,14 +259,14 @@ __device__ __forceinline__ void epi_store8(const GemmParams& p, const GemmProble
   }
   float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   bf16* dst;
-  if constexpr (EPI == kEpiQkvRope) {
+  if constexpr (E == kEpiQkvRope) {
     const int joint = __ldg(p.srow_joint + pr.row_off + row);
     const int which = col / p.H;
     dst = (which == 0 ? p.q : (which == 1 ? p.k : p.v)) + (size_t)joint * p.H + (col - which * p.H);
   } else {
     dst = static_cast<bf16*>(pr.out) + (size_t)row * pr.ldo + col;
   }
-  if constexpr (EPI == kEpiGateResid) {
+  if constexpr (E == kEpiGateResid) {
     const int seq = __ldg(p.srow_seq + pr.row_off + row);
     const float4* g = reinterpret_cast<const float4*>(
         p.mod + ((size_t)seq * 2 + pr.stream) * 6 * (size_t)p.H + p.gate_off + col);
@@ -502,9 +504,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
   constexpr uint32_t B_BYTES = (BN / 2) * kBK * 2;    // this CTA's 128 rows of B
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN;
-  // E4M3 operands (kEpiF8Scale): a 128-byte row of a K block holds 128 elements instead of 64,
-  // and each MMA consumes K = 32 instead of 16; the byte layout of the stages is the same
-  constexpr bool F8 = EPI == kEpiF8Scale;
+  // E4M3 operands (kEpiF8): a 128-byte row of a K block holds 128 elements instead of 64, and
+  // each MMA consumes K = 32 instead of 16; the byte layout of the stages is the same
+  constexpr bool F8 = (EPI & kEpiF8) != 0;
+  constexpr int E = EPI & 7;
   constexpr int KE = F8 ? 2 * kBK : kBK;  // K elements per stage
   constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(2 * kBM, BN) : idesc_bf16_f32(2 * kBM, BN, false);
 
@@ -539,7 +542,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if constexpr (EPI == kEpiQkvRope) {
+  if constexpr (E == kEpiQkvRope) {
     const int D = p.head_dim;
     if ((int)threadIdx.x < D / 2) {
       const int g = threadIdx.x, d = 2 * g;
@@ -667,7 +670,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
       const GemmProblem& pr = p.prob[pi];
       const int row0 = m * 2 * kBM + rank * kBM + q * 32;  // first of this warp's 32 rows
       float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES) + (warp - 2) * 32 * kStageRow;
-      if constexpr (EPI == kEpiBiasBf16 || EPI == kEpiGelu || EPI == kEpiF8Scale) {
+      if constexpr (E == kEpiBiasBf16 || E == kEpiGelu) {
         if (p.tma_store[pi]) {
           // bf16 rows of 64 columns, 16-byte chunks swizzled as the 128-byte-swizzle tensor map
           // expects, then one TMA store of 32 rows x 64 columns per group
@@ -719,7 +722,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
       // gives each row's 1 / RMS per head, from the same bias-added values the second uses
       const bf16* qk_g = nullptr;
       float qk_rstd0 = 0.0f, qk_rstd1 = 0.0f;
-      if constexpr (EPI == kEpiQkvRope) {
+      if constexpr (E == kEpiQkvRope) {
         const int col_lo = n * BN + c_lo, which = col_lo / p.H;
         const bf16* g = pi ? (which ? p.qk_norm[1][1] : p.qk_norm[1][0])
                            : (which ? p.qk_norm[0][1] : p.qk_norm[0][0]);
@@ -831,7 +834,10 @@ cudaError_t launch_gemm_pair(const GemmParams& p, int epi, int num_sms, cudaStre
     case kEpiQkvRope: return launch_pair<kEpiQkvRope>(p, num_sms, stream);
     case kEpiGateResid: return launch_pair<kEpiGateResid>(p, num_sms, stream);
     case kEpiGelu: return launch_pair<kEpiGelu>(p, num_sms, stream);
-    case kEpiF8Scale: return launch_pair<kEpiF8Scale>(p, num_sms, stream);
+    case kEpiBiasBf16 | kEpiF8: return launch_pair<kEpiBiasBf16 | kEpiF8>(p, num_sms, stream);
+    case kEpiQkvRope | kEpiF8: return launch_pair<kEpiQkvRope | kEpiF8>(p, num_sms, stream);
+    case kEpiGateResid | kEpiF8: return launch_pair<kEpiGateResid | kEpiF8>(p, num_sms, stream);
+    case kEpiGelu | kEpiF8: return launch_pair<kEpiGelu | kEpiF8>(p, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -14,7 +14,8 @@ enum GemmEpi : int {
   kEpiQkvRope = 2,    // q | k | v = acc + bias; RoPE on q, k; rows scattered to joint order
   kEpiGateResid = 3,  // x += gate[seq] * (acc + bias), x bf16 in place
   kEpiGelu = 4,       // out bf16 = GELU(acc + bias)
-  kEpiF8Scale = 5,    // E4M3 operands; out bf16 = acc * row_scale[row] * col_scale[col] + bias
+  kEpiF8 = 8,         // flag on any of the above (pair kernel): E4M3 operands, and the
+                      // accumulator is first multiplied by row_scale[row_off + row] * col_scale[col]
 };
 
 struct GemmProblem {
@@ -23,6 +24,7 @@ struct GemmProblem {
   int stream;             // modulation stream (0 text, 1 image)
   int ldo;                // output leading dimension in elements
   const bf16* bias;       // [N] or nullptr
+  const float* col_scale; // kEpiF8: [N] dequantisation scale of B's rows (output columns)
   void* out;              // output (or the residual x for kEpiGateResid)
 };
 
@@ -45,8 +47,7 @@ struct GemmParams {
   int head_dim;
   int gate_off;           // float offset of the gate chunk inside a (sample, stream) mod row
   const bf16* qk_norm[2][2];  // [problem][q, k]: QK-RMSNorm scales [head_dim], or null (off)
-  const float* row_scale;     // kEpiF8Scale: [M] dequantisation scale of A's rows
-  const float* col_scale;     // kEpiF8Scale: [N] dequantisation scale of B's rows (output columns)
+  const float* row_scale;     // kEpiF8: dequantisation scale of A's rows (indexed row_off + row)
   bf16* q;                // [N_tok][H] joint order
   bf16* k;
   bf16* v;

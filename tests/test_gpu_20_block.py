@@ -224,6 +224,47 @@ def test_single_sample_full_budget():
     assert_close(_f(x_img)[rows], got, "block output rows of the 16K sample")
 
 
+@pytest.mark.parametrize("size", ["tiny", "mid"])
+def test_block_fp8(size):
+    """fp8 variant of the block (mf_block_forward_fp8): the four projections on E4M3 operands,
+    weights quantised per output row by the oracle and uploaded, activations quantised per row
+    on the GPU; against the oracle's fp8 block on the GPU's own embed output.  Tiny: H=256,
+    D=64, K = 256 / 1024; mid: a ragged H=512 pack, K = 512 / 2048."""
+    from oracle import fp8 as F
+    d = synth.TINY if size == "tiny" else MID
+    samples = synth.tiny_samples() if size == "tiny" else _mid_samples(3)
+    case = Case(samples, d, 1, seed=31)
+    ref, H = case.ref, d.hidden
+    x_img = torch.empty((ref.n_img, H), dtype=torch.bfloat16, device="cuda")
+    mf.mf_embed(case.plan, case.model.dims, case.model.embed["w_in"], case.model.embed["b_in"],
+                to_bf16(case.z_np), x_img)
+    emb = _f(x_img)
+    x_txt = to_bf16(case.x_txt_np)
+    x_txt0 = _f(x_txt)
+    bw = case.w.blocks[0]
+    w8 = {st: F.quantize_weights(bw[st]) for st in M.STREAMS}
+    w8d = {st: {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in w8[st].items()} for st in M.STREAMS}
+    ws = torch.empty(mf.mf_block_fp8_workspace_bytes(case.plan, case.model.dims), dtype=torch.uint8, device="cuda")
+    mf.mf_block_forward_fp8(case.plan, case.model.dims, case.model.block_structs[0],
+                            mf.block_struct_fp8(w8d["txt"], w8d["img"]), None, x_txt, x_img, ws)
+    mf.mf_check()
+    xt_ref, xi_ref = [], []
+    for k, c in enumerate(ref.order):
+        s = samples[c]
+        cond = M.condition(np.float32(s.t), case.w.temb, d.freq_dim)
+        xt = x_txt0[ref.cu_txt[k]:ref.cu_txt[k + 1]]
+        xi = emb[ref.cu_img[k]:ref.cu_img[k + 1]]
+        ot, oi = M.block_forward(xt, xi, M.image_positions(s.frames, s.lat_h, s.lat_w), cond, bw, d.heads, w8=w8)
+        xt_ref.append(ot)
+        xi_ref.append(oi)
+    xt_ref, xi_ref = np.concatenate(xt_ref), np.concatenate(xi_ref)
+    got_t, got_i = _f(x_txt), _f(x_img)
+    assert_close(got_t, xt_ref, "fp8 block x_txt")
+    assert_close(got_i, xi_ref, "fp8 block x_img")
+    assert_update_close(got_t, xt_ref, x_txt0, "fp8 block update txt")
+    assert_update_close(got_i, xi_ref, emb, "fp8 block update img")
+
+
 def test_mid_edit_stack():
     """Editing structure at H=512: 2 frames (clean source, noisy target), 3-axis RoPE, loss on
     target frames only, 2 blocks."""

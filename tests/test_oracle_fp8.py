@@ -107,3 +107,36 @@ def test_planted_fp8_mistakes(name, monkeypatch):
     assert _pins_pass()
     monkeypatch.setattr(F, "e4m3_round", MUTANTS[name])
     assert not _pins_pass(), name
+
+
+def test_bf16_round_by_hand():
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: ties to the even mantissa (1.0)
+    x = np.array([1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -9, 1.0 + 3 * 2.0 ** -8, -2.0 - 2.0 ** -7, 3.0e38])
+    want = [1.0, 1.0, 1.0 + 2.0 ** -7, 1.0 + 2.0 ** -6, -2.0, 2.0 ** 127 * 1.765625]   # 3e38 = 1.7632 * 2^127
+    np.testing.assert_array_equal(F.bf16_round(x), want)
+
+
+def test_fp8_block_close_to_bf16_block():
+    """The fp8 variant of the block equals the bf16 block up to E4M3 quantisation (a few % on
+    the projections, diluted by the residual), is not the bf16 block itself, and loses its
+    accuracy if the row scales are dropped."""
+    import synth
+    from oracle import model as M
+    d = synth.Dims(hidden=128, heads=2, channels=16)
+    w = synth.model_weights(d, 1, 3, bf16=True)
+    bw = w.blocks[0]
+    w8 = {s: F.quantize_weights(bw[s]) for s in M.STREAMS}
+    rng = np.random.default_rng(2)
+    xt, xi = rng.standard_normal((6, 128)), rng.standard_normal((20, 128))
+    pos = M.image_positions(1, 4, 5)
+    c = rng.standard_normal(128)
+    ref = np.concatenate(M.block_forward(xt, xi, pos, c, bw, d.heads))
+    got = np.concatenate(M.block_forward(xt, xi, pos, c, bw, d.heads, w8=w8))
+    x0 = np.concatenate([xt, xi])
+    dr, dg = ref - x0, got - x0
+    cos = float((dr * dg).sum() / np.sqrt((dr * dr).sum() * (dg * dg).sum()))
+    assert 0.99 < cos < 1.0 - 1e-9, cos
+    bad = {s: dict(w8[s], s_qkv=np.ones_like(w8[s]["s_qkv"])) for s in M.STREAMS}
+    gb = np.concatenate(M.block_forward(xt, xi, pos, c, bw, d.heads, w8=bad)) - x0
+    cosb = float((dr * gb).sum() / np.sqrt((dr * dr).sum() * (gb * gb).sum()))
+    assert cosb < 0.99, cosb
