@@ -44,9 +44,10 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=120)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["native16k", "cfg", "gemm"], default="native16k",
+    ap.add_argument("--workload", choices=["native16k", "cfg", "gemm", "fp8block"], default="native16k",
                     help="native16k: the headline block-forward pack; cfg: packed vs unpacked CFG sampler; "
-                         "gemm: bf16 and fp8 GEMMs alone at the block's shapes")
+                         "gemm: bf16 and fp8 GEMMs alone at the block's shapes; fp8block: the block "
+                         "forward with fp8 projections against the bf16 one on the 16K packs")
     return ap.parse_args()
 
 
@@ -518,6 +519,80 @@ def run_gemm_shapes(args, rank, world, local_rank):
             "data": "synthetic (N(0,0.5) activations, N(0,0.02) weights)"}
 
 
+def run_fp8_block(args, rank, world, local_rank):
+    """The block forward on the eight seeded 16K packs, bf16 (`mf_block_forward`) and fp8
+    (`mf_block_forward_fp8`, weights quantised per row by the library at setup), block calls
+    only, K timed calls each after W warm-up calls, CUDA events around the whole run."""
+    import torch
+    import packed_rectified_flow_packer_b300 as mf
+    from packed_rectified_flow_packer_b300.device import DeviceModel, to_bf16
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dims = synth.FULL
+    H = dims.hidden
+    model = DeviceModel(synth.model_weights(dims, 1, seed=0), device=dev)
+    d = model.dims
+    w8 = {}
+    for st in ("txt", "img"):
+        w8[st] = {}
+        for name in ("qkv", "o", "1", "2"):
+            wt = model.blocks[0][st]["w_" + name]
+            q = torch.empty(wt.shape, dtype=torch.uint8, device=dev)
+            sc = torch.empty(wt.shape[0], dtype=torch.float32, device=dev)
+            mf.mf_quantize_fp8_rows(wt, q, sc)
+            w8[st]["q_" + name], w8[st]["s_" + name] = q, sc
+    s8 = mf.block_struct_fp8(w8["txt"], w8["img"])
+    packs = []
+    for seed in rank_seeds(rank):
+        cands = synth.native_candidates(seed)
+        plan = mf.mf_pack(cands, BUDGET)
+        mf.mf_plan_upload(plan)
+        x, _, _ = synth.pack_inputs(cands, plan.array("order"), dims, seed)
+        xi = torch.randn((plan.n_img, H), device=dev, generator=torch.Generator(device=dev).manual_seed(seed))
+        packs.append({"plan": plan, "x_txt": to_bf16(x, dev), "x_img": xi.to(torch.bfloat16)})
+    ws = torch.empty(max(mf.mf_block_fp8_workspace_bytes(p["plan"], d) for p in packs), dtype=torch.uint8,
+                     device=dev)
+    xt = torch.empty((BUDGET, H), dtype=torch.bfloat16, device=dev)
+    xi = torch.empty((BUDGET, H), dtype=torch.bfloat16, device=dev)
+    out = {}
+    for tag in ("bf16", "fp8"):
+        def call(p):
+            nt, ni = p["x_txt"].shape[0], p["x_img"].shape[0]
+            xt[:nt].copy_(p["x_txt"])
+            xi[:ni].copy_(p["x_img"])
+            if tag == "fp8":
+                mf.mf_block_forward_fp8(p["plan"], d, model.block_structs[0], s8, None, xt, xi, ws)
+            else:
+                mf.mf_block_forward(p["plan"], d, model.block_structs[0], None, xt, xi, ws)
+        for i in range(args.warmup):
+            call(packs[i % N_PACKS])
+        torch.cuda.synchronize(dev)
+        ms, tok = 0.0, 0
+        for i in range(args.steps):
+            p = packs[i % N_PACKS]
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            nt, ni = p["x_txt"].shape[0], p["x_img"].shape[0]
+            xt[:nt].copy_(p["x_txt"])
+            xi[:ni].copy_(p["x_img"])
+            e0.record()
+            if tag == "fp8":
+                mf.mf_block_forward_fp8(p["plan"], d, model.block_structs[0], s8, None, xt, xi, ws)
+            else:
+                mf.mf_block_forward(p["plan"], d, model.block_structs[0], None, xt, xi, ws)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms += e0.elapsed_time(e1)
+            tok += p["plan"].n_tok
+        mf.mf_check()
+        out[tag] = {"ms_per_block": round(ms / args.steps, 4), "tokens_per_s": round(tok / (ms / 1e3), 1)}
+    if rank != 0:
+        return None
+    return {"metric": "packed tokens/s per NR-MMDiT block fwd, bf16 vs fp8 projections (1xB300)",
+            "workload": "fp8block", "steps": args.steps, "warmup": args.warmup, "bf16": out["bf16"],
+            "fp8": out["fp8"], "fp8_speedup": round(out["bf16"]["ms_per_block"] / out["fp8"]["ms_per_block"], 4),
+            "data": "synthetic (seeded packs; N(0,1) hidden image states instead of the latent embed)"}
+
+
 def run_cfg_sampler(args, rank, world, local_rank):
     """4-block stack, two prompts (1024x1024 and 768x1344, 256 text tokens when conditional),
     4 Euler steps from t = 1 to 0, guidance w = 4.  Packed: cond and uncond branches of both
@@ -675,6 +750,8 @@ def main():
         line = run_cfg_sampler(args, rank, world, local_rank)
     elif args.workload == "gemm":
         line = run_gemm_shapes(args, rank, world, local_rank)
+    elif args.workload == "fp8block":
+        line = run_fp8_block(args, rank, world, local_rank)
     else:
         line = run_mageflow(args, rank, world, local_rank)
     if rank == 0 and line is not None:
