@@ -124,3 +124,7 @@ def test_device_calls_fail_cleanly_without_gpu():
     assert B.STATUS[st] == "MF_ERR_CUDA"
     d = B.mf_dims(256, 4, 64, 4, 256)
     assert B.mf_block_workspace_bytes(p, d) > 0
+    # the fp8 block needs the bf16 workspace plus the codes and row scales of one
+    # projection input (N x 4H bytes at most)
+    extra = B.mf_block_fp8_workspace_bytes(p, d) - B.mf_block_workspace_bytes(p, d)
+    assert extra >= p.n_tok * 4 * 256 + 4 * p.n_tok
