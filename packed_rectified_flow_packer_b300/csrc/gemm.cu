@@ -1,15 +1,19 @@
-// Persistent grouped GEMM for sm_103a: TMA (128-byte swizzle) -> shared-memory ring ->
-// tcgen05.mma (one thread issues, f32 accumulators in TMEM, two accumulator buffers so the
-// epilogue of one tile overlaps the main loop of the next) -> tcgen05.ld epilogue warps.
+// Persistent grouped GEMMs for sm_103a: TMA (128-byte swizzle) -> shared-memory ring ->
+// tcgen05.mma (f32 accumulators in TMEM, two accumulator buffers so the epilogue of one tile
+// overlaps the main loop of the next) -> tcgen05.ld epilogue warps.
 //
-// Warp roles (192 threads):  warp 0 lane 0 TMA producer; warp 1 TMEM allocator and lane 0
-// MMA issuer; warps 2..5 epilogue (warp w reads TMEM lanes 32*(w%4)..+31, i.e. tile rows).
+// Two kernels.  gemm_kernel (single CTA, 128-row tiles, 192 threads: warp 0 TMA producer,
+// warp 1 TMEM allocator and MMA issuer, warps 2..5 epilogue) serves the narrow final projection
+// and small plain GEMMs.  gemm_pair_kernel (clusters of two CTAs, 256 x 256 tiles with
+// tcgen05.mma.cta_group::2, 320 threads: warp 0 producer, warp 1 MMA issuer of the even CTA,
+// warps 2..9 epilogue) serves every 256-wide projection of the block; its kEpiF8 flag switches
+// the operands to E4M3 (kind::f8f6f4) with per-row and per-column scales in the epilogue.
 //
 // The fused epilogues implement the NR-MMDiT chains that the Mage-Flow pages list as fused
 // memory-bound work - norm, RoPE, gating, residual (PaperReading review of "Mage-Flow: An
 // Efficient Native-Resolution Foundation Model for Image Generation and Editing", §2.2 (3);
-// hyper.ai summary, 方法): bias, RoPE over (frame, row, col) with the scatter to joint order,
-// GELU, and the gated residual x += gate * y.
+// hyper.ai summary, 方法): bias, RoPE over (frame, row, col) with the scatter to joint order
+// (and the optional per-head QK-RMSNorm), GELU, and the gated residual x += gate * y.
 #include "gemm.cuh"
 
 namespace mf {

@@ -1,6 +1,7 @@
-// Grouped, persistent bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA)
-// with the NR-MMDiT block's fused epilogues.  C[M][N] = A[M][K] B[N][K]^T for up to two
-// problems (text stream, image stream) in one launch.
+// Grouped, persistent GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA) with
+// the NR-MMDiT block's fused epilogues.  C[M][N] = A[M][K] B[N][K]^T for up to two problems
+// (text stream, image stream) in one launch; bf16 operands, or E4M3 ones (kEpiF8) on the
+// pair kernel.
 #pragma once
 
 #include "common.cuh"
