@@ -126,13 +126,37 @@ def blas_threads():
     return os.cpu_count()
 
 
+def tiny_single_thread(seconds=1.0):
+    """The oracle on the tiny configuration (2 samples, 144 tokens, H = 256) with one BLAS
+    thread: tokens/s and the number of passes timed."""
+    from threadpoolctl import threadpool_limits
+    from oracle import model as M
+    d = synth.TINY
+    w = synth.model_weights(d, 1, seed=0, bf16=False)
+    samples = synth.tiny_samples()
+    batch = synth.batch_inputs(samples, d, 0, bf16=False)
+    tok, n = 0, 0
+    with threadpool_limits(1):
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds or n == 0:
+            for i, smp in enumerate(samples):
+                M.forward(batch.x_txt[i], batch.z[i], smp, smp.t, w, d.heads)
+                tok += smp.length
+            n += 1
+        el = time.perf_counter() - t0
+    return tok / el, n
+
+
 def cpu_baseline(dims, weights, cands, order, seconds):
     sub, x, z = oracle_sample(dims, weights, cands, order, 2048)
     tps, el, n = time_oracle(dims, weights, sub, x, z, seconds)
+    tiny_tps, tiny_n = tiny_single_thread()
     return {"value": tps, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"fp64 NumPy oracle: embed + 1 block + final layer on one sample of pack 0 cut to "
                       f"{sub.txt_len} text + {sub.lat_h}x{sub.lat_w} image tokens ({sub.length} tokens), "
-                      f"{n} runs in {el:.1f} s"}
+                      f"{n} runs in {el:.1f} s",
+            "tiny_1thread": {"value": round(tiny_tps, 1), "unit": "tokens/s", "cores": 1,
+                             "sample": f"tiny configuration (2 samples, 144 tokens, H = 256), {tiny_n} passes"}}
 
 
 # ---------------------------------------------------------------- clocks
