@@ -14,10 +14,17 @@ can be checked against per-sample results.  Only the tests, the package's smoke 
 bench's CPU-baseline leg may import it; the product path never does.  It shares no code with
 the CUDA library and does not import it.
 
+Modules: `pack` (first-fit packing and the plan's index buffers), `model` (the block, the
+stack ends and the rectified-flow epilogues, with the QK-RMSNorm and fp8 variants), `brute`
+(pure-Python loops for the brute-force pins), `fp8` (E4M3 rounding, per-row quantisation and
+the quantised linear layer), `grad` (float64 PyTorch restatement of the block and its
+reverse-mode gradients, for the block backward).
+
 Parity status: the packer, RoPE, attention, LayerNorm, GELU, the timestep embedding, the
 block's residual structure, the interpolation, the loss, the Diffusion-NFT loss, the Euler
-step and CFG are each pinned by tests against closed forms, invariants, brute force or hand-computed values.  The
+step, CFG, the QK-RMSNorm, E4M3 rounding and the block's gradients are each pinned by tests
+against closed forms, invariants, brute force, finite differences or hand-computed values.  The
 whole-model numbers (a full block with random weights) have no printed worked example on the
 pages: "parity unpinned" for the composed block beyond those structural pins.
 """
-from . import pack, model, brute  # noqa: F401
+from . import pack, model, brute, fp8  # noqa: F401
