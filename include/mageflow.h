@@ -155,7 +155,7 @@ mf_status mf_plan_array(const mf_plan* plan, int32_t which, const int32_t** data
 /* ------------------------------------------------------------------------------------ */
 
 typedef struct {
-  int32_t hidden;     /* H; multiple of 64 */
+  int32_t hidden;     /* H; multiple of 256, at most 4096 */
   int32_t heads;      /* nh; H / nh = head dim D, D in {64, 128} */
   int32_t channels;   /* C: latent channels per patch token; 64 or 128 */
   int32_t mlp_ratio;  /* MLP width = mlp_ratio * H */
