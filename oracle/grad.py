@@ -101,3 +101,14 @@ def block_vjp(x_txt, x_img, pos_img, c, bw: dict, heads: int, g_txt, g_img):
             out[s][n] = np_(grads[i], w[s][n])
             i += 1
     return out
+
+
+def attention_vjp(q, k, v, do):
+    """Gradients (dq, dk, dv) of sum(do * attention(q, k, v)) for ONE sample, q, k, v, do
+    [L][nh][D] float64 (reverse-mode differentiation of the restated softmax attention)."""
+    qt, kt, vt = (_t(a).requires_grad_(True) for a in (q, k, v))
+    D = qt.shape[-1]
+    p = torch.softmax(torch.einsum("qhd,khd->hqk", qt, kt) / np.sqrt(D), dim=-1)
+    o = torch.einsum("hqk,khd->qhd", p, vt)
+    g = torch.autograd.grad((o * _t(do)).sum(), [qt, kt, vt])
+    return tuple(x.detach().numpy() for x in g)

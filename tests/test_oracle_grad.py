@@ -93,3 +93,23 @@ def test_gradient_special_cases():
                      rng2.standard_normal(xi2.shape))
     for n in ("w_qkv", "w_o", "w_1", "w_2", "b_qkv", "b_o", "b_1", "b_2"):
         np.testing.assert_array_equal(g2["txt"][n], 0.0)
+
+
+def test_attention_vjp_closed_form():
+    """The attention gradients against the textbook closed form written out in NumPy:
+    P = softmax(q k^T / sqrt(D)), dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(dP * P)),
+    dQ = dS K / sqrt(D), dK = dS^T Q / sqrt(D), per head."""
+    rng = np.random.default_rng(11)
+    L, nh, Dh = 7, 2, 8
+    q, k, v, do = (rng.standard_normal((L, nh, Dh)) for _ in range(4))
+    dq, dk, dv = G.attention_vjp(q, k, v, do)
+    for h in range(nh):
+        s = q[:, h] @ k[:, h].T / np.sqrt(Dh)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        dvh = p.T @ do[:, h]
+        dp = do[:, h] @ v[:, h].T
+        ds = p * (dp - (dp * p).sum(axis=1, keepdims=True))
+        np.testing.assert_allclose(dv[:, h], dvh, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dq[:, h], ds @ k[:, h] / np.sqrt(Dh), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dk[:, h], ds.T @ q[:, h] / np.sqrt(Dh), rtol=0, atol=1e-12)
