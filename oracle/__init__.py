@@ -21,6 +21,8 @@ the quantised linear layer), `grad` (float64 PyTorch restatement of the block an
 reverse-mode gradients, for the block backward).
 
 Parity status: the packer, RoPE, attention, LayerNorm, GELU, the timestep embedding, the
+timestep condition (the two-layer SiLU MLP on it: a hand-worked value and planted mistakes), the
+stack's composition (embed -> blocks -> final layer) and the CFG sampler's step sum, the
 block's residual structure, the interpolation, the loss, the Diffusion-NFT loss, the Euler
 step, CFG, the QK-RMSNorm, E4M3 rounding and the block's gradients are each pinned by tests
 against closed forms, invariants, brute force, finite differences or hand-computed values.  The

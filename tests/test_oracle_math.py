@@ -48,6 +48,73 @@ def test_timestep_embedding(golden):
     np.testing.assert_allclose(e[:, :128] ** 2 + e[:, 128:] ** 2, 1.0, atol=1e-14)
 
 
+def _golden_condition_weights(g):
+    w1 = np.zeros((g["hidden"], g["freq_dim"]))
+    for row, col in g["w_t1_ones"]:
+        w1[row, col] = 1.0
+    return {"w_t1": w1, "b_t1": np.array(g["b_t1"]), "w_t2": np.array(g["w_t2"]),
+            "b_t2": np.array(g["b_t2"])}
+
+
+def test_condition(golden):
+    """The timestep condition c = SiLU(W_t2 SiLU(W_t1 phi(t) + b_t1) + b_t2) that feeds every
+    adaLN modulation (the velocity v_theta(z_t, t, tau) takes t, PaperReading review §2.2(2);
+    the block's gating, §2.2(3)): a hand-worked value with one-hot first-layer rows and an
+    asymmetric second layer (a transposed W_t2, a dropped SiLU or bias, or swapped layers all
+    change it), and the batch axis (one row per sample) matches per-sample calls."""
+    g = golden("elementary.json")["condition"]
+    tw = _golden_condition_weights(g)
+    c = M.condition(np.array(g["t"]), tw, g["freq_dim"])
+    np.testing.assert_allclose(c, g["c"], rtol=0, atol=1e-15)
+    d = synth.Dims(hidden=32, heads=2, channels=16)
+    w = synth.model_weights(d, 1, 3, bf16=False)
+    ts = np.array([0.0, 0.3, 1.0])
+    batch = M.condition(ts, w.temb, d.freq_dim)
+    for i, t in enumerate(ts):
+        np.testing.assert_allclose(batch[i], M.condition(t, w.temb, d.freq_dim), rtol=0, atol=1e-15)
+
+
+def _identity_stack(H=32, C=32):
+    """A one-block stack whose image path is closed-form: identity latent embed, zero gates in
+    both streams (the block is the identity on x), zero final modulation and identity output
+    projection, so v = LN(z_t) row by row."""
+    d = synth.Dims(hidden=H, heads=1, channels=C)
+    w = synth.model_weights(d, 1, 11, bf16=False)
+    w.embed = {"w_in": np.eye(H, C), "b_in": np.zeros(H)}
+    for s in M.STREAMS:
+        for ch in ("gate1", "gate2"):
+            _set_mod(w.blocks[0], s, ch, 0.0, H)
+    w.final = {"w_fmod": np.zeros((2 * H, H)), "b_fmod": np.zeros(2 * H), "w_out": np.eye(C, H),
+               "b_out": np.zeros(C)}
+    return d, w
+
+
+def test_forward_composition():
+    """forward = embed -> blocks -> final layer on one sample: with the closed-form stack above
+    the velocity is LN(z_t), whatever the text tokens, t or the block's other weights."""
+    d, w = _identity_stack()
+    smp = synth.Sample(3, 1, 2, 5, 0.4)
+    z = R.standard_normal((smp.img_len, d.channels))
+    v = M.forward(R.standard_normal((3, d.hidden)), z, smp, 0.4, w, d.heads)
+    np.testing.assert_allclose(v, M.layer_norm(z), atol=1e-13)
+    assert v.shape == z.shape
+
+
+def test_sample_cfg_constant_velocity():
+    """The CFG sampler on a model whose velocity is a constant b (zero output weights, bias b):
+    the guided velocity is b whatever w, and the Euler steps over a grid from t = 1 to t = 0
+    add up to z0 + b (the steps' dt sum to 1 and move along +v)."""
+    d, w = _identity_stack()
+    b = R.standard_normal(d.channels)
+    w.final["w_out"] = np.zeros_like(w.final["w_out"])
+    w.final["b_out"] = b
+    sc, su = synth.Sample(4, 1, 2, 3, 1.0, 1, 1), synth.Sample(0, 1, 2, 3, 1.0, 2, 0)
+    z0 = R.standard_normal((sc.img_len, d.channels))
+    for grid in ([1.0, 0.75, 0.5, 0.25, 0.0], list(np.linspace(1.0, 0.0, 21))):
+        z = M.sample_cfg(R.standard_normal((4, d.hidden)), z0, sc, su, w, d.heads, 4.0, grid)
+        np.testing.assert_allclose(z, z0 + b, atol=1e-12)
+
+
 # ------------------------------------------------------------------ RoPE
 def test_rope_known_rotation(golden):
     g = golden("elementary.json")["rope"]
@@ -430,6 +497,7 @@ def _pins_pass():
         test_layer_norm(load_golden)
         test_gelu_silu(load_golden)
         test_timestep_embedding(load_golden)
+        test_condition(load_golden)
         test_rope_known_rotation(load_golden)
         test_rope_matches_complex_loops()
         for D in (32, 64):
@@ -442,6 +510,8 @@ def _pins_pass():
         test_block_position_shift_invariance_image_only()
         test_block_scale_minus_one_case()
         test_final_layer_scale_minus_one()
+        test_forward_composition()
+        test_sample_cfg_constant_velocity()
         test_flow_matching_hand_worked(load_golden)
         test_interpolation_endpoints_and_loss_zero()
         test_euler_straight_path()
@@ -449,12 +519,12 @@ def _pins_pass():
         test_nft_loss_pins()
         test_rms_norm_heads_pins()
         test_block_qk_norm_invariance()
-    except AssertionError:
+    except (AssertionError, ValueError):      # a mutant that breaks a shape is caught too
         return False
     return True
 
 
-ORIG = {n: getattr(M, n) for n in ("layer_norm", "gelu", "timestep_embedding", "rope_angles",
+ORIG = {n: getattr(M, n) for n in ("layer_norm", "gelu", "timestep_embedding", "condition", "rope_angles",
                                      "rms_norm_heads",
                                      "attention", "interpolate", "flow_loss", "euler_step",
                                      "cfg_combine", "nft_loss")}
@@ -475,11 +545,36 @@ def _mut_attention(q, k, v, rows=None):            # missing 1/sqrt(D)
     return np.einsum("hqk,khd->qhd", p / p.sum(-1, keepdims=True), v)
 
 
+def _mut_condition(kind):
+    """Planted mistakes in the timestep condition (c = SiLU(W_t2 SiLU(W_t1 phi + b_t1) + b_t2))."""
+    def cond(t, temb_w, freq_dim=256):
+        phi = M.timestep_embedding(t, freq_dim)
+        w1, b1, w2, b2 = (temb_w[k] for k in ("w_t1", "b_t1", "w_t2", "b_t2"))
+        if kind == "swapped_layers":
+            w1, b1, w2, b2 = w2, b2, w1, b1
+        h = M.linear(phi, w1, b1)
+        if kind != "no_inner_silu":
+            h = M.silu(h)
+        if kind == "w_t2_transposed":
+            out = h @ M.f64(w2) + M.f64(b2)
+        elif kind == "no_b_t2":
+            out = h @ M.f64(w2).T
+        else:
+            out = M.linear(h, w2, b2)
+        return out if kind == "no_final_silu" else M.silu(out)
+    return cond
+
+
 MUTANTS = {
     "layer_norm_unbiased_var": ("layer_norm", _mut_layer_norm),
     "gelu_wrong_sign": ("gelu", lambda x: 0.5 * M.f64(x) * (1.0 - M.erf(M.f64(x) / np.sqrt(2)))),
     "timestep_sin_cos_order": ("timestep_embedding",
                                lambda t, dim=256: np.roll(ORIG["timestep_embedding"](t, dim), dim // 2, -1)),
+    "condition_no_final_silu": ("condition", _mut_condition("no_final_silu")),
+    "condition_no_inner_silu": ("condition", _mut_condition("no_inner_silu")),
+    "condition_w_t2_transposed": ("condition", _mut_condition("w_t2_transposed")),
+    "condition_no_b_t2": ("condition", _mut_condition("no_b_t2")),
+    "condition_swapped_layers": ("condition", _mut_condition("swapped_layers")),
     "rope_axes_swapped": ("rope_angles", lambda pos, D: ORIG["rope_angles"](np.asarray(pos)[:, [1, 0, 2]], D)),
     "rope_base_wrong": ("rope_angles", lambda pos, D: ORIG["rope_angles"](pos, D) * 1.01),
     "attention_no_scale": ("attention", _mut_attention),
