@@ -172,7 +172,17 @@ def cpu_baseline(dims, weights, cands, order, seconds):
             "sample": f"fp64 NumPy oracle: embed + 1 block + final layer on one sample of pack 0 cut to "
                       f"{sub.txt_len} text + {sub.lat_h}x{sub.lat_w} image tokens ({sub.length} tokens), "
                       f"{n} runs in {el:.1f} s",
+            "config": {"workload": sample_workload(sub)},
             "tiny_1thread": tiny}
+
+
+def sample_workload(sub):
+    """What a bounded oracle sample of the native-resolution workload actually runs."""
+    return (f"bounded sample of the native-resolution 16K pack workload: one sample of pack 0 cut to "
+            f"{sub.length} tokens ({sub.txt_len} text + {sub.lat_h}x{sub.lat_w} image) per step, "
+            f"H = {synth.FULL.hidden}, embed + 1 NR-MMDiT block + final layer; attention over "
+            f"{sub.length} tokens instead of the packs' ~5K-token samples, so the oracle's per-token cost is "
+            f"lower than on the real packs")
 
 
 # ---------------------------------------------------------------- clocks
@@ -467,11 +477,14 @@ def run_mageflow(args, rank, world, local_rank):
     if os.path.exists(tfile):
         with open(tfile) as f:
             traffic = json.load(f).get(dom)
+    avg_ms = de["ms"] / de["launches"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                "peak_kind": f"sustained bf16 ({peaks['source']}); timed inside a long step",
-                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_kind": f"dense bf16 burst ({peaks['source']}: cuBLAS bf16 GEMM, best of 10)",
+                "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                "avg_ms": round(avg_ms, 4),
+                "avg_ms_x_sm_mhz": round(avg_ms * clocks["sm_mhz"], 1) if clocks.get("sm_mhz") else None,
                 "traffic": traffic,
                 "flops_per_launch": de["flops"] / de["launches"],
                 "all_gemms_tflops": round(g_fl / (g_ms / 1e3) / 1e12, 1) if g_ms else None,
@@ -635,11 +648,13 @@ def run_fp8_block(args, rank, world, local_rank):
 
 def run_cfg_sampler(args, rank, world, local_rank):
     """4-block stack, two prompts (1024x1024 and 768x1344, 256 text tokens when conditional),
-    4 Euler steps from t = 1 to 0, guidance w = 4.  Packed: cond and uncond branches of both
-    prompts in one pack (16768 tokens); the library combines the branches in place.
-    Unpacked: the cond pack and the uncond pack run one after the other, and the guided step
-    z += dt (v_u + w (v_c - v_u)) is applied as z += dt (1 - w) v_u, then z += dt w v_c.
-    Each arm's whole 4-step sampler is captured once as a CUDA graph and replayed."""
+    Euler steps on a uniform grid from t = 1 to 0, guidance w = 4, for 4 steps (the Turbo
+    setting) and 20 steps (the base model's, where the pages see the largest packed-CFG gain).
+    Packed: cond and uncond branches of both prompts in one pack (16768 tokens); the library
+    combines the branches in place.  Unpacked: the cond pack and the uncond pack run one after
+    the other, and the guided step z += dt (v_u + w (v_c - v_u)) is applied as
+    z += dt (1 - w) v_u, then z += dt w v_c.  Each arm's whole sampler is captured once as a
+    CUDA graph and replayed."""
     import torch
 
     import packed_rectified_flow_packer_b300 as mf
@@ -652,21 +667,19 @@ def run_cfg_sampler(args, rank, world, local_rank):
     H, C = dims.hidden, dims.channels
     weights = synth.model_weights(dims, 4, seed=3)
     model = DeviceModel(weights)
-    grid = [1.0, 0.75, 0.5, 0.25, 0.0]
     w = 4.0
 
     def arm(samples):
         plan = mf.mf_pack(samples, sum(s.length for s in samples))
         mf.mf_plan_upload(plan)
         order = plan.array("order")
-        n_txt, n_img, S = plan.n_txt, plan.n_img, plan.n_seq
+        n_txt, n_img = plan.n_txt, plan.n_img
         x0 = np.concatenate([synth.round_bf16(synth.normal(7, f"x_txt.{c}", (samples[c].txt_len, H)))
                              for c in order]) if n_txt else np.zeros((0, H), np.float32)
         return {"plan": plan, "ws": Workspace(plan, model.dims), "x0": to_bf16(x0),
                 "x": torch.empty((max(n_txt, 1), H), dtype=torch.bfloat16, device="cuda"),
                 "x_img": torch.empty((n_img, H), dtype=torch.bfloat16, device="cuda"),
                 "v": torch.empty((n_img, C), dtype=torch.float32, device="cuda"),
-                "t": [torch.full((S,), a, dtype=torch.float32, device="cuda") for a in grid[:-1]],
                 "n_tok": plan.n_tok, "n_img": n_img}
 
     packed = arm(synth.cfg_samples())
@@ -678,71 +691,82 @@ def run_cfg_sampler(args, rank, world, local_rank):
     zu, zbu = z0u.clone(), z0u.to(torch.bfloat16)
     vg = torch.empty_like(packed["v"])
 
-    def stack(a, zb, k):
+    def stack(a, zb, t):
         n = a["x0"].shape[0]
         if n:
             a["x"][:n].copy_(a["x0"])
-        run_stack(a["plan"], model, a["x"], zb, a["x_img"], a["v"], a["ws"], t=a["t"][k])
+        run_stack(a["plan"], model, a["x"], zb, a["x_img"], a["v"], a["ws"], t=t)
 
-    def sampler_packed():
-        zp.copy_(z0p)
-        zbp.copy_(zp)
-        for k in range(len(grid) - 1):
-            stack(packed, zbp, k)
-            mf.mf_cfg_combine(packed["plan"], C, w, packed["v"], vg)
-            mf.mf_euler_step(packed["plan"], C, grid[k] - grid[k + 1], vg, zp, zbp)
+    runs = {}
+    for n_steps in (4, 20):
+        grid = [float(x) for x in np.linspace(1.0, 0.0, n_steps + 1)]
+        tt = {id(a): [torch.full((a["plan"].n_seq,), g, dtype=torch.float32, device="cuda") for g in grid[:-1]]
+              for a in (packed, cond, unc)}
 
-    def sampler_unpacked():
-        zu.copy_(z0u)
-        zbu.copy_(zu)
-        for k in range(len(grid) - 1):
-            dt = grid[k] - grid[k + 1]
-            stack(cond, zbu, k)
-            stack(unc, zbu, k)
-            mf.mf_euler_step(unc["plan"], C, dt * (1.0 - w), unc["v"], zu, None)
-            mf.mf_euler_step(cond["plan"], C, dt * w, cond["v"], zu, zbu)
+        def sampler_packed():
+            zp.copy_(z0p)
+            zbp.copy_(zp)
+            for k in range(n_steps):
+                stack(packed, zbp, tt[id(packed)][k])
+                mf.mf_cfg_combine(packed["plan"], C, w, packed["v"], vg)
+                mf.mf_euler_step(packed["plan"], C, grid[k] - grid[k + 1], vg, zp, zbp)
 
-    result = {}
-    for name, fn, n_tok in (("packed", sampler_packed, packed["n_tok"]),
-                            ("unpacked", sampler_unpacked, cond["n_tok"] + unc["n_tok"])):
-        fn()                                   # first calls: library set-up outside the capture
-        torch.cuda.synchronize()
-        mf.mf_check()
-        l0 = mf.mf_launch_count()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        launches = mf.mf_launch_count() - l0
-        for _ in range(max(3, args.warmup)):
-            g.replay()
-        torch.cuda.synchronize()
-        mf.mf_check()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        mf.mf_check()
-        ms = e0.elapsed_time(e1) / args.steps
-        z_out = zp if name == "packed" else zu
-        z_graph = z_out.clone()
-        fn()                                   # eager run: the replay must give the same bits
-        torch.cuda.synchronize()
-        mf.mf_check()
-        result[name] = {"ms_per_sampler": round(ms, 3), "images_per_s": round(2 / (ms / 1e3), 2),
-                        "tokens_per_block_fwd": n_tok, "library_launches_per_sampler": int(launches),
-                        "graph_replay_equals_eager": bool(torch.equal(z_graph, z_out))}
-    speedup = result["unpacked"]["ms_per_sampler"] / result["packed"]["ms_per_sampler"]
-    return {"metric": "packed-CFG 4-step sampler throughput (2 prompts, 4 NR-MMDiT blocks)",
-            "value": result["packed"]["images_per_s"], "unit": "images/s", "n_gpus": 1,
+        def sampler_unpacked():
+            zu.copy_(z0u)
+            zbu.copy_(zu)
+            for k in range(n_steps):
+                dt = grid[k] - grid[k + 1]
+                stack(cond, zbu, tt[id(cond)][k])
+                stack(unc, zbu, tt[id(unc)][k])
+                mf.mf_euler_step(unc["plan"], C, dt * (1.0 - w), unc["v"], zu, None)
+                mf.mf_euler_step(cond["plan"], C, dt * w, cond["v"], zu, zbu)
+
+        result = {}
+        reps = max(1, args.steps if n_steps == 4 else max(1, args.steps // 5))
+        for name, fn, n_tok in (("packed", sampler_packed, packed["n_tok"]),
+                                ("unpacked", sampler_unpacked, cond["n_tok"] + unc["n_tok"])):
+            fn()                                   # first calls: library set-up outside the capture
+            torch.cuda.synchronize()
+            mf.mf_check()
+            l0 = mf.mf_launch_count()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            launches = mf.mf_launch_count() - l0
+            for _ in range(max(3, args.warmup)):
+                g.replay()
+            torch.cuda.synchronize()
+            mf.mf_check()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            mf.mf_check()
+            ms = e0.elapsed_time(e1) / reps
+            z_out = zp if name == "packed" else zu
+            z_graph = z_out.clone()
+            fn()                                   # eager run: the replay must give the same bits
+            torch.cuda.synchronize()
+            mf.mf_check()
+            result[name] = {"ms_per_sampler": round(ms, 3), "images_per_s": round(2 / (ms / 1e3), 2),
+                            "tokens_per_block_fwd": n_tok, "library_launches_per_sampler": int(launches),
+                            "replays_timed": reps,
+                            "graph_replay_equals_eager": bool(torch.equal(z_graph, z_out))}
+            del g
+        result["packed_speedup"] = round(result["unpacked"]["ms_per_sampler"] / result["packed"]["ms_per_sampler"], 4)
+        runs[f"steps{n_steps}"] = result
+    return {"metric": "packed-CFG sampler throughput (2 prompts, 4 NR-MMDiT blocks)",
+            "value": runs["steps4"]["packed"]["images_per_s"], "unit": "images/s", "n_gpus": 1,
             "steps": args.steps, "warmup": max(3, args.warmup), "higher_is_better": True,
-            "dtype": "bf16", "data": "synthetic", "graph": "whole sampler captured once per arm",
+            "dtype": "bf16", "data": "synthetic", "graph": "whole sampler captured once per arm and step count",
             "config": {"workload": "packed CFG: 1024x1024 + 768x1344, cond (256 text) + uncond, "
-                                   "4 blocks, 4 Euler steps, w = 4", "hidden": H, "heads": dims.heads},
-            "packed": result["packed"], "unpacked": result["unpacked"],
-            "packed_speedup": round(speedup, 4),
-            "pages_context": "1.09x-1.15x on one A100 (hyper.ai summary, 实验)"}
+                                   "4 blocks, 4 and 20 Euler steps, w = 4", "hidden": H, "heads": dims.heads},
+            "steps4": runs["steps4"], "steps20": runs["steps20"],
+            "packed_speedup_4": runs["steps4"]["packed_speedup"],
+            "packed_speedup_20": runs["steps20"]["packed_speedup"],
+            "pages_context": "1.09x-1.15x on one A100, largest for the 20-step base model (hyper.ai summary, 实验)"}
 
 
 # ---------------------------------------------------------------- the reference (oracle) arm
@@ -775,7 +799,8 @@ def run_reference(args, rank, world):
     return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_dict(dims),
+            "data": "synthetic", "config": dict(config_dict(dims), workload=sample_workload(sub),
+                                                sample_tokens=sub.length),
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

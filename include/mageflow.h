@@ -345,6 +345,7 @@ mf_status mf_nft_loss(const mf_plan* plan, int32_t channels, const float* d_z, c
  *   - All calls on a device share the array: calls that overlap on the GPU (unordered
  *     streams) race; order them on one stream.  Each call writes every scratch row before it
  *     reads it, so nothing left by an earlier call reaches the result.
+ * Its launches are counted and traced as MF_K_LOSS, like mf_flow_loss's.
  * Errors: as mf_flow_loss, and MF_ERR_WORKSPACE when the plan has more than
  * MF_NOALLOC_MAX_IMG_ROWS image rows (checked before any launch). */
 mf_status mf_flow_loss_noalloc(const mf_plan* plan, int32_t channels, const float* d_z,

@@ -93,30 +93,7 @@ cudaEvent_t trace_event() {
   return e;
 }
 
-// Counts the kernels of one library launch and, while tracing is on, brackets it with events.
-class Trace {
- public:
-  Trace(int kind, cudaStream_t st, double flops, double bytes, int nk) : st_(st) {
-    g_launches += nk;
-    std::lock_guard<std::mutex> lk(g_trace_mu);
-    if (!g_trace.on || ((g_trace.mask >> kind) & 1u) == 0) return;
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
-    rec_ = TraceRec{kind, trace_event(), trace_event(), flops, bytes, nk};
-    if (rec_.a == nullptr || rec_.b == nullptr) return;
-    active_ = cudaEventRecord(rec_.a, st) == cudaSuccess;
-  }
-  ~Trace() {
-    if (!active_) return;
-    std::lock_guard<std::mutex> lk(g_trace_mu);
-    if (cudaEventRecord(rec_.b, st_) == cudaSuccess) g_trace.recs.push_back(rec_);
-  }
-
- private:
-  cudaStream_t st_;
-  TraceRec rec_{};
-  bool active_ = false;
-};
+using mf::Trace;
 
 // ------------------------------------------------------------------ TMA descriptors
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -355,6 +332,34 @@ bool stream_ok(const mf_stream_weights& s) {
 }
 
 }  // namespace
+
+namespace mf {
+
+mf_status current_device(int* dev) {
+  DevInfo* di = nullptr;
+  return device_info(&di, dev);
+}
+
+Trace::Trace(int kind, cudaStream_t st, double flops, double bytes, int nk)
+    : st_(st), kind_(kind), nk_(nk), flops_(flops), bytes_(bytes) {
+  g_launches += nk;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (!g_trace.on || ((g_trace.mask >> kind) & 1u) == 0) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
+  a_ = trace_event();
+  b_ = trace_event();
+  if (a_ == nullptr || b_ == nullptr) return;
+  active_ = cudaEventRecord(a_, st) == cudaSuccess;
+}
+
+Trace::~Trace() {
+  if (!active_) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (cudaEventRecord(b_, st_) == cudaSuccess) g_trace.recs.push_back(TraceRec{kind_, a_, b_, flops_, bytes_, nk_});
+}
+
+}  // namespace mf
 
 // ====================================================================== plan upload / free
 extern "C" mf_status mf_plan_upload(mf_plan* p, void* stream) {

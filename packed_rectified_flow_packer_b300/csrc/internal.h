@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <vector>
 
+#include <cuda_runtime.h>
+
 #include "mageflow.h"
 
 // A pack and every index buffer the kernels read.  Built once by mf_pack (host only) and
@@ -53,4 +55,28 @@ struct mf_plan {
 namespace mf {
 
 constexpr int kQBlock = 256;  // query rows of one attention work item (two 128-row tiles)
+
+// Ordinal of the current device after checking that it is an sm_103a (the library's per-device
+// state is set up on first use).  MF_ERR_UNSUPPORTED on another architecture, MF_ERR_CUDA when
+// no device can be queried.
+mf_status current_device(int* dev);
+
+// One library launch of `nk` kernels of kind `kind` (mf_kernel_kind): counted always and, while
+// tracing is on (and the stream is not capturing), bracketed by two CUDA events on `st` -
+// the constructor records the first, the destructor the second.
+class Trace {
+ public:
+  Trace(int kind, cudaStream_t st, double flops, double bytes, int nk);
+  ~Trace();
+  Trace(const Trace&) = delete;
+  Trace& operator=(const Trace&) = delete;
+
+ private:
+  cudaStream_t st_;
+  int kind_ = 0, nk_ = 0;
+  cudaEvent_t a_ = nullptr, b_ = nullptr;
+  double flops_ = 0.0, bytes_ = 0.0;
+  bool active_ = false;
+};
+
 }  // namespace mf

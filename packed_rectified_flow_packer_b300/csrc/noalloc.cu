@@ -51,7 +51,9 @@ extern "C" mf_status mf_flow_loss_noalloc(const mf_plan* p, int32_t C, const flo
                                           const float* d_eps, const float* d_v, double* d_loss_sum,
                                           int64_t* d_count, double* d_mean, void* stream) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MF_ERR_CUDA;
+  mf_status st = mf::current_device(&dev);  // sm_103a check, as every other entry point
+  if (st != MF_OK) return st;
+  if (dev >= kMaxDevices) return MF_ERR_CUDA;
   if (p == nullptr) return MF_ERR_INVALID_ARG;
   if (p->d_blob == nullptr) return MF_ERR_NOT_UPLOADED;
   if (p->device != dev) return MF_ERR_INVALID_ARG;
@@ -63,8 +65,10 @@ extern "C" mf_status mf_flow_loss_noalloc(const mf_plan* p, int32_t C, const flo
     return MF_ERR_ALIGNMENT;
   if (p->Ni > MF_NOALLOC_MAX_IMG_ROWS) return MF_ERR_WORKSPACE;
   double* rows = nullptr;
-  mf_status st = scratch_address(dev, &rows);
+  st = scratch_address(dev, &rows);
   if (st != MF_OK) return st;
+  // counted and traced like mf_flow_loss (same kind, bytes and kernel count)
+  mf::Trace tr(MF_K_LOSS, static_cast<cudaStream_t>(stream), 0, (double)p->Ni * C * 12.0, 3);
   cudaError_t e = mf::launch_flow_loss(p->d_cui, p->d_img_target, p->S, p->Ni, C, d_z, d_eps, d_v, rows,
                                        d_loss_sum, reinterpret_cast<long long*>(d_count), d_mean,
                                        static_cast<cudaStream_t>(stream));
