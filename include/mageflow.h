@@ -228,6 +228,62 @@ mf_status mf_block_forward(const mf_plan* plan, const mf_dims* dims, const mf_bl
                            const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
                            size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------------------ */
+/* Training: the block forward that keeps what the backward reads, and the block backward  */
+/* (the pages' training step, PaperReading review section 3, Table 4, runs both)           */
+/* ------------------------------------------------------------------------------------ */
+
+/* Workspace of mf_block_forward_train (bytes): the mf_block_forward workspace (same offsets,
+ * see mf_block_workspace_layout; `a` holds the second LN + modulate output) followed by the
+ * values the backward reads: the block input and the residual after attention, the first
+ * LN + modulate output, the ungated out-projection and MLP outputs, the MLP pre-activation and
+ * the attention logsumexp. */
+size_t mf_block_train_workspace_bytes(const mf_plan* plan, const mf_dims* dims);
+
+/* mf_block_forward (same arguments, same result in d_x_txt / d_x_img) that also keeps, in d_ws
+ * (mf_block_train_workspace_bytes() bytes), everything mf_block_backward needs.  The plain bf16
+ * block only: MF_ERR_UNSUPPORTED with QK-RMSNorm scales.  Errors: as mf_block_forward. */
+mf_status mf_block_forward_train(const mf_plan* plan, const mf_dims* dims, const mf_block_weights* w,
+                                 const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
+                                 size_t ws_bytes, void* stream);
+
+/* Gradients of one stream's weights, f32 device arrays shaped like the weights
+ * (w_mod [6H][H], b_mod [6H], w_qkv [3H][H], b_qkv [3H], w_o [H][H], b_o [H], w_1 [rH][H],
+ * b_1 [rH], w_2 [H][rH], b_2 [H]); each is overwritten. */
+typedef struct {
+  float* w_mod; float* b_mod;
+  float* w_qkv; float* b_qkv;
+  float* w_o;   float* b_o;
+  float* w_1;   float* b_1;
+  float* w_2;   float* b_2;
+} mf_stream_grads;
+
+typedef struct {
+  mf_stream_grads txt;
+  mf_stream_grads img;
+} mf_block_grads;
+
+size_t mf_block_backward_workspace_bytes(const mf_plan* plan, const mf_dims* dims);
+
+/* Backward of one NR-MMDiT block over the pack (the block of mf_block_forward, differentiated
+ * exactly: adaLN modulation, LN, fused QKV, RoPE, per-sample joint attention, gated residuals,
+ * GELU MLP; attention gradients never cross samples).  Given G = dL/d(block output):
+ *   d_dx_txt, d_dx_img : in: G (bf16, laid out as the forward's x); out: dL/d(block input)
+ *   g                  : dL/d(every weight of both streams), f32, overwritten
+ *   d_dc               : f32 [S][H], dL/dc_s for each packed sample's condition vector
+ *                        c_s = SiLU(temb(t_s)) (the caller sums it over the blocks of a stack)
+ *   d_train_ws         : the workspace a mf_block_forward_train call with the same plan,
+ *                        dims, weights and t left behind (read only)
+ *   d_ws               : mf_block_backward_workspace_bytes() bytes, 256-byte aligned
+ * The QK-RMSNorm variant is not differentiated (MF_ERR_UNSUPPORTED).  Reductions over rows use
+ * atomic adds, so the last bits of the weight and modulation gradients may change from run to
+ * run.  Errors: MF_ERR_INVALID_ARG, MF_ERR_UNSUPPORTED, MF_ERR_NOT_UPLOADED, MF_ERR_ALIGNMENT,
+ * MF_ERR_WORKSPACE, MF_ERR_CUDA. */
+mf_status mf_block_backward(const mf_plan* plan, const mf_dims* dims, const mf_block_weights* w,
+                            const void* d_train_ws, size_t train_ws_bytes, void* d_dx_txt, void* d_dx_img,
+                            const mf_block_grads* g, float* d_dc, void* d_ws, size_t ws_bytes,
+                            void* stream);
+
 /* fp8 variant of the block (the pages name no fp8 arithmetic; see mf_gemm_fp8): the E4M3
  * codes of one stream's four projection matrices, as mf_quantize_fp8_rows writes them from the
  * bf16 weights (rows = output features), and their per-row scales. */
@@ -363,6 +419,36 @@ mf_status mf_flow_loss_noalloc(const mf_plan* plan, int32_t channels, const floa
 mf_status mf_attention(const mf_plan* plan, int32_t heads, int32_t head_dim, const void* d_q,
                        const void* d_k, const void* d_v, void* d_o, void* stream);
 
+/* mf_attention that also returns each query row's logsumexp, the input the backward reads:
+ * d_lse f32 [heads][N] (joint order inside each head),
+ *   lse[h][j] = ln sum_k exp(q_j . k_k / sqrt(D)) over the keys k of j's own sample.
+ * Same arguments, layouts and errors as mf_attention otherwise (d_lse 16-byte aligned). */
+mf_status mf_attention_lse(const mf_plan* plan, int32_t heads, int32_t head_dim, const void* d_q,
+                           const void* d_k, const void* d_v, void* d_o, float* d_lse, void* stream);
+
+/* Workspace of mf_attention_backward: an f32 dq accumulator [N][H], delta [heads][N] f32 and a
+ * joint-order copy of do [N][H] bf16 (bytes; 0 for bad arguments). */
+size_t mf_attention_backward_workspace_bytes(const mf_plan* plan, int32_t heads, int32_t head_dim);
+
+/* Backward of the varlen joint attention [PR 2.2(2)] (attention restricted to each sample):
+ * with s = q k^T / sqrt(D), P = softmax(s) over the sample's own keys, o = P v and the output
+ * gradient do, per sample and head
+ *   dv = P^T do,  ds = P * (do v^T - rowsum(do * o)),  dq = ds k / sqrt(D),  dk = ds^T q / sqrt(D),
+ * nothing crossing samples.  P is recomputed from q, k and the forward's lse
+ * (mf_attention_lse), so no L x L matrix is stored.
+ *   d_q, d_k, d_v : bf16 [N][H] joint order (the forward's inputs; q, k after RoPE)
+ *   d_o, d_do     : bf16 [N_txt + N_img][H] stream-sorted (the forward's output and its gradient)
+ *   d_lse         : f32 [heads][N] from mf_attention_lse
+ *   d_dq, d_dk, d_dv : bf16 [N][H] joint order, written
+ *   d_ws          : mf_attention_backward_workspace_bytes() bytes, 256-byte aligned
+ * H = heads * head_dim must be a multiple of 256; head_dim 64 or 128.
+ * Errors: MF_ERR_INVALID_ARG, MF_ERR_UNSUPPORTED, MF_ERR_NOT_UPLOADED, MF_ERR_ALIGNMENT,
+ * MF_ERR_WORKSPACE, MF_ERR_CUDA. */
+mf_status mf_attention_backward(const mf_plan* plan, int32_t heads, int32_t head_dim, const void* d_q,
+                                const void* d_k, const void* d_v, const void* d_o, const float* d_lse,
+                                const void* d_do, void* d_dq, void* d_dk, void* d_dv, void* d_ws,
+                                size_t ws_bytes, void* stream);
+
 /* fp8 variant (a knob of the block's projections; the pages name no fp8 arithmetic).
  * Per-row E4M3 quantisation: for each row r of d_x (bf16 [M][K], K a multiple of 16),
  * d_scale[r] = max_k |x[r][k]| / 448 (1 for an all-zero row) and d_q[r][k] =
@@ -422,7 +508,9 @@ typedef enum {
   MF_K_LATENT = 10,     /* interpolate, packed CFG, Euler step */
   MF_K_LOSS = 11,       /* flow-matching loss reduction */
   MF_K_FP8 = 12,        /* fp8 variant: row quantisation and the E4M3 GEMM */
-  MF_K_COUNT = 13
+  MF_K_ATTN_BWD = 13,   /* attention backward: delta / do gather, the tcgen05 loop, dq to bf16 */
+  MF_K_BLOCK_BWD = 14,  /* block backward's row, reduction, gather and modulation kernels */
+  MF_K_COUNT = 15
 } mf_kernel_kind;
 
 typedef struct {

@@ -112,3 +112,43 @@ def attention_vjp(q, k, v, do):
     o = torch.einsum("hqk,khd->qhd", p, vt)
     g = torch.autograd.grad((o * _t(do)).sum(), [qt, kt, vt])
     return tuple(x.detach().numpy() for x in g)
+
+
+def attention_lse(q, k):
+    """Per head and query row of ONE sample, the natural-log logsumexp of the scaled scores,
+    lse[h][j] = ln sum_k exp(q_j . k_k / sqrt(D)), float64 [nh][L] (the normaliser that the
+    backward uses to recompute P = exp(s - lse))."""
+    from scipy.special import logsumexp
+    q, k = np.asarray(q, np.float64), np.asarray(k, np.float64)
+    s = np.einsum("qhd,khd->hqk", q, k) / np.sqrt(q.shape[-1])
+    return logsumexp(s, axis=-1)
+
+
+def attention_vjp_rows(q, k, v, do, q_rows, k_rows):
+    """The attention gradients of ONE sample for selected rows, by the closed form of the
+    softmax backward (per head, s = q k^T / sqrt(D), P = softmax(s), o = P v,
+    delta = rowsum(do * o), dS = P * (do v^T - delta)):
+      dq[j] = sum_k dS[j, k] k_k / sqrt(D)        for the query rows j in q_rows,
+      dk[k] = sum_j dS[j, k] q_j / sqrt(D),  dv[k] = sum_j P[j, k] do_j   for k in k_rows.
+    q, k, v, do: [L][nh][D].  Returns (dq [len(q_rows)][nh][D], dk, dv [len(k_rows)][nh][D]).
+    Only the rows asked for are formed beyond the full P, so long samples stay affordable."""
+    q, k, v, do = (np.asarray(a, np.float64) for a in (q, k, v, do))
+    q_rows, k_rows = np.asarray(q_rows), np.asarray(k_rows)
+    L, nh, D = q.shape
+    dq = np.zeros((len(q_rows), nh, D))
+    dk = np.zeros((len(k_rows), nh, D))
+    dv = np.zeros((len(k_rows), nh, D))
+    for h in range(nh):
+        s = q[:, h] @ k[:, h].T / np.sqrt(D)
+        s -= s.max(axis=1, keepdims=True)
+        np.exp(s, out=s)
+        s /= s.sum(axis=1, keepdims=True)               # s is P from here on
+        delta = (do[:, h] * (s @ v[:, h])).sum(axis=1)
+        ds_r = s[q_rows] * (do[q_rows, h] @ v[:, h].T - delta[q_rows, None])
+        dq[:, h] = ds_r @ k[:, h] / np.sqrt(D)
+        p_c = s[:, k_rows]
+        dv[:, h] = p_c.T @ do[:, h]
+        ds_c = p_c * (do[:, h] @ v[k_rows, h].T - delta[:, None])
+        dk[:, h] = ds_c.T @ q[:, h] / np.sqrt(D)
+        del s
+    return dq, dk, dv

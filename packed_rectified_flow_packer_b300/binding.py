@@ -13,7 +13,7 @@ import os
 
 import numpy as np
 
-__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_block_fp8_workspace_bytes", "mf_block_forward_fp8", "block_struct_fp8", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
+__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_block_train_workspace_bytes", "mf_block_forward_train", "mf_block_backward_workspace_bytes", "mf_block_backward", "grads_struct", "mf_stream_grads", "mf_block_grads", "GRAD_FIELDS", "mf_block_fp8_workspace_bytes", "mf_block_forward_fp8", "block_struct_fp8", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_attention_lse", "mf_attention_backward_workspace_bytes", "mf_attention_backward", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmageflow.so")
 
@@ -79,13 +79,24 @@ class mf_block_weights_fp8(C.Structure):
     _fields_ = [("txt", mf_stream_weights_fp8), ("img", mf_stream_weights_fp8)]
 
 
+GRAD_FIELDS = STREAM_FIELDS   # mf_stream_grads: one f32 array per weight, same names
+
+
+class mf_stream_grads(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in GRAD_FIELDS]
+
+
+class mf_block_grads(C.Structure):
+    _fields_ = [("txt", mf_stream_grads), ("img", mf_stream_grads)]
+
+
 class mf_trace_entry(C.Structure):
     _fields_ = [("launches", C.c_int64), ("ms", C.c_double), ("flops", C.c_double),
                 ("bytes", C.c_double)]
 
 
 KERNEL_KINDS = ("cond", "ln", "gemm_qkv", "attn", "gemm_oproj", "gemm_up", "gemm_down", "gemm_embed",
-                "gemm_final", "gemm_plain", "latent", "loss", "fp8")
+                "gemm_final", "gemm_plain", "latent", "loss", "fp8", "attn_bwd", "block_bwd")
 
 _P = C.c_void_p
 _S = C.c_int   # mf_status
@@ -101,6 +112,12 @@ _sigs = {
     "mf_block_workspace_layout": (_S, [_P, C.POINTER(mf_dims), C.POINTER(C.c_size_t), C.c_int32]),
     "mf_block_forward": (_S, [_P, C.POINTER(mf_dims), C.POINTER(mf_block_weights), _P, _P, _P, _P,
                               C.c_size_t, _P]),
+    "mf_block_train_workspace_bytes": (C.c_size_t, [_P, C.POINTER(mf_dims)]),
+    "mf_block_forward_train": (_S, [_P, C.POINTER(mf_dims), C.POINTER(mf_block_weights), _P, _P, _P, _P,
+                                    C.c_size_t, _P]),
+    "mf_block_backward_workspace_bytes": (C.c_size_t, [_P, C.POINTER(mf_dims)]),
+    "mf_block_backward": (_S, [_P, C.POINTER(mf_dims), C.POINTER(mf_block_weights), _P, C.c_size_t, _P, _P,
+                               C.POINTER(mf_block_grads), _P, _P, C.c_size_t, _P]),
     "mf_embed": (_S, [_P, C.POINTER(mf_dims), _P, _P, _P, _P, _P]),
     "mf_final_workspace_bytes": (C.c_size_t, [_P, C.POINTER(mf_dims)]),
     "mf_final": (_S, [_P, C.POINTER(mf_dims), C.POINTER(mf_temb_weights), _P, _P, _P, _P, _P, _P,
@@ -113,6 +130,10 @@ _sigs = {
     "mf_flow_loss_noalloc": (_S, [_P, C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "mf_nft_loss": (_S, [_P, C.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "mf_attention": (_S, [_P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P]),
+    "mf_attention_lse": (_S, [_P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P]),
+    "mf_attention_backward_workspace_bytes": (C.c_size_t, [_P, C.c_int32, C.c_int32]),
+    "mf_attention_backward": (_S, [_P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   C.c_size_t, _P]),
     "mf_gemm": (_S, [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P, C.c_int32, _P]),
     "mf_quantize_fp8_rows": (_S, [C.c_int32, C.c_int32, _P, _P, _P, _P]),
     "mf_gemm_fp8": (_S, [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
@@ -270,6 +291,36 @@ def mf_block_forward(plan: Plan, dims, weights: mf_block_weights, t, x_txt, x_im
                              _ptr(x_img), _ptr(ws), nbytes, _stream(stream)), "mf_block_forward")
 
 
+def mf_block_train_workspace_bytes(plan: Plan, dims) -> int:
+    return lib.mf_block_train_workspace_bytes(plan.handle, C.byref(_dims(dims)))
+
+
+def mf_block_forward_train(plan: Plan, dims, weights: mf_block_weights, t, x_txt, x_img, ws, ws_bytes=None,
+                           stream=None):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _ok(lib.mf_block_forward_train(plan.handle, C.byref(_dims(dims)), C.byref(weights), _ptr(t), _ptr(x_txt),
+                                   _ptr(x_img), _ptr(ws), nbytes, _stream(stream)), "mf_block_forward_train")
+
+
+def grads_struct(txt, img) -> mf_block_grads:
+    """txt, img: dicts weight name -> f32 device tensor of that weight's shape."""
+    return mf_block_grads(mf_stream_grads(*[_ptr(txt[k]) for k in GRAD_FIELDS]),
+                          mf_stream_grads(*[_ptr(img[k]) for k in GRAD_FIELDS]))
+
+
+def mf_block_backward_workspace_bytes(plan: Plan, dims) -> int:
+    return lib.mf_block_backward_workspace_bytes(plan.handle, C.byref(_dims(dims)))
+
+
+def mf_block_backward(plan: Plan, dims, weights: mf_block_weights, train_ws, dx_txt, dx_img,
+                      grads: mf_block_grads, dc, ws, ws_bytes=None, train_ws_bytes=None, stream=None):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    tbytes = train_ws_bytes if train_ws_bytes is not None else train_ws.numel() * train_ws.element_size()
+    _ok(lib.mf_block_backward(plan.handle, C.byref(_dims(dims)), C.byref(weights), _ptr(train_ws), tbytes,
+                              _ptr(dx_txt), _ptr(dx_img), C.byref(grads), _ptr(dc), _ptr(ws), nbytes,
+                              _stream(stream)), "mf_block_backward")
+
+
 def block_struct_fp8(txt8, img8) -> mf_block_weights_fp8:
     """txt8, img8: dicts q_* (uint8 codes) / s_* (f32 scales) -> device tensors."""
     return mf_block_weights_fp8(mf_stream_weights_fp8(*[_ptr(txt8[k]) for k in STREAM_FP8_FIELDS]),
@@ -353,6 +404,23 @@ def mf_flow_loss_noalloc(plan: Plan, channels: int, z, eps, v, loss_sum, count, 
 def mf_attention(plan: Plan, heads: int, head_dim: int, q, k, v, o, stream=None):
     _ok(lib.mf_attention(plan.handle, heads, head_dim, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                          _stream(stream)), "mf_attention")
+
+
+def mf_attention_lse(plan: Plan, heads: int, head_dim: int, q, k, v, o, lse, stream=None):
+    _ok(lib.mf_attention_lse(plan.handle, heads, head_dim, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                             _stream(stream)), "mf_attention_lse")
+
+
+def mf_attention_backward_workspace_bytes(plan: Plan, heads: int, head_dim: int) -> int:
+    return lib.mf_attention_backward_workspace_bytes(plan.handle, heads, head_dim)
+
+
+def mf_attention_backward(plan: Plan, heads: int, head_dim: int, q, k, v, o, lse, do, dq, dk, dv, ws,
+                          ws_bytes=None, stream=None):
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _ok(lib.mf_attention_backward(plan.handle, heads, head_dim, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                  _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), nbytes, _stream(stream)),
+        "mf_attention_backward")
 
 
 def mf_quantize_fp8_rows(x, q, scale, stream=None):

@@ -23,7 +23,7 @@ NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
-SOURCES = ["plan.cpp", "api.cu", "gemm.cu", "attention.cu", "pointwise.cu", "noalloc.cu"]
+SOURCES = ["plan.cpp", "api.cu", "gemm.cu", "attention.cu", "attention_bwd.cu", "block_bwd.cu", "pointwise.cu", "noalloc.cu"]
 
 
 def _deps(src):

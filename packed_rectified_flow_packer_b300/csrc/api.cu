@@ -11,6 +11,8 @@
 #include <vector>
 
 #include "attention.cuh"
+#include "attention_bwd.cuh"
+#include "block_bwd.cuh"
 #include "gemm.cuh"
 #include "internal.h"
 #include "pointwise.cuh"
@@ -146,6 +148,20 @@ bool make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// f32 matrix [rows][cols] (row-major, contiguous), boxes of box_rows x box_cols, no swizzle.
+bool make_tmap_f32(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                   uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ validation helpers
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -217,6 +233,32 @@ size_t fp8_region_bytes(const mf_plan* p, const mf_dims* d) {
   return al256(N * R) + al256(N * 4);
 }
 
+// Training forward: the block workspace followed by what the backward reads - the block input
+// x0 and the residual after attention x1 (stream-sorted bf16 [N][H]), the first LN + modulate
+// output a1 (the block workspace's `a` keeps the second), the ungated out-projection and MLP
+// outputs y_o, y_m [N][H], the MLP pre-activation u [N][rH] and the attention lse [heads][N].
+struct TrainLayout {
+  BlockLayout base;
+  size_t x0, x1, a1, yo, ym, u, lse, total;
+};
+
+TrainLayout train_layout(const mf_plan* p, const mf_dims* d) {
+  TrainLayout L{};
+  L.base = block_layout(p, d);
+  size_t o = L.base.total;
+  auto take = [&](size_t bytes) { size_t r = o; o = al256(o + bytes); return r; };
+  const size_t N = p->N, H = d->hidden, R = (size_t)d->mlp_ratio * H;
+  L.x0 = take(N * H * 2);
+  L.x1 = take(N * H * 2);
+  L.a1 = take(N * H * 2);
+  L.yo = take(N * H * 2);
+  L.ym = take(N * H * 2);
+  L.u = take(N * R * 2);
+  L.lse = take((size_t)d->heads * N * 4);
+  L.total = o;
+  return L;
+}
+
 struct FinalLayout {
   size_t c, fmod, a, sinus, h1, total;
 };
@@ -246,10 +288,13 @@ struct GemmSpec {
   int row_off;
   int stream;
   const float* col_scale;  // E4M3 operands (kEpiF8): per-column dequantisation scale of B
+  void* aux;               // kEpiSave output / kEpiGeluBwd input, bf16 [M][ldo]
 };
 
+// maj (pair kernel, bf16): mf::kMajKK for C = A B^T with A [M][K], B [N][K]; kMajBMN with B
+// stored [K][N]; kMajMNMN with A stored [K][M] and B [K][N] (K may then be any length).
 mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmParams& p,
-                   const DevInfo* di, cudaStream_t st, int kind) {
+                   const DevInfo* di, cudaStream_t st, int kind, int maj = mf::kMajKK) {
   // 256-wide tiles run on CTA pairs (256 x 256 per pair), 128-wide ones on single CTAs
   const bool pair = BN == 256;
   p.n_prob = 0;
@@ -263,8 +308,11 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
       if (!pair || !make_tmap_u8(&p.tmA[i], g.A, g.K, g.M, 128) || !make_tmap_u8(&p.tmB[i], g.B, g.K, g.N, BN / 2))
         return MF_ERR_CUDA;
     } else {
-      if (!make_tmap(&p.tmA[i], g.A, g.K, g.M, 128)) return MF_ERR_CUDA;
-      if (!make_tmap(&p.tmB[i], g.B, g.K, g.N, pair ? BN / 2 : BN)) return MF_ERR_CUDA;
+      const bool amn = (maj & mf::kMajAMN) != 0, bmn = (maj & mf::kMajBMN) != 0;
+      if (amn ? !make_tmap(&p.tmA[i], g.A, g.M, g.K, 64) : !make_tmap(&p.tmA[i], g.A, g.K, g.M, 128))
+        return MF_ERR_CUDA;
+      if (bmn ? !make_tmap(&p.tmB[i], g.B, g.N, g.K, 64) : !make_tmap(&p.tmB[i], g.B, g.K, g.N, pair ? BN / 2 : BN))
+        return MF_ERR_CUDA;
     }
     p.prob[i].M = g.M;
     p.prob[i].N = g.N;
@@ -275,11 +323,13 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
     p.prob[i].bias = static_cast<const bf16*>(g.bias);
     p.prob[i].col_scale = g.col_scale;
     p.prob[i].out = g.out;
+    p.prob[i].aux = g.aux;
     p.tiles_m[i] = pair ? (g.M + 255) / 256 : (g.M + 127) / 128;
     p.tiles_n[i] = (g.N + BN - 1) / BN;
     p.tma_store[i] = 0;
     const int base = epi & ~mf::kEpiF8;
-    if (pair && (base == mf::kEpiBiasBf16 || base == mf::kEpiGelu) && g.ldo == g.N && g.N % 64 == 0 &&
+    if (pair && (base == mf::kEpiBiasBf16 || base == mf::kEpiGelu || base == mf::kEpiGeluBwd) && g.ldo == g.N &&
+        g.N % 64 == 0 &&
         aligned(g.out, 16)) {
       if (!make_tmap(&p.tmC[i], g.out, g.N, g.M, 32)) return MF_ERR_CUDA;
       p.tma_store[i] = 1;
@@ -298,7 +348,8 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
   double flops = 0;
   for (int i = 0; i < p.n_prob; ++i) flops += 2.0 * p.prob[i].M * (double)p.prob[i].N * p.prob[i].K;
   Trace tr(kind, st, flops, 0, 1);
-  return cuda_status(pair ? mf::launch_gemm_pair(p, epi, di->sms, st)
+  if (!pair && maj != mf::kMajKK) return MF_ERR_UNSUPPORTED;
+  return cuda_status(pair ? mf::launch_gemm_pair(p, epi, di->sms, st, maj)
                           : mf::launch_gemm(p, BN, epi, di->sms, st));
 }
 
@@ -372,13 +423,13 @@ extern "C" mf_status mf_plan_upload(mf_plan* p, void* stream) {
   const int32_t* srcs[] = {p->cu.data(), p->cui.data(), p->pos.data(), p->srow_joint.data(),
                            p->srow_seq.data(), p->joint_srow.data(), p->img_seq.data(),
                            p->img_pair.data(), p->img_target.data(), p->seq_role.data(),
-                           p->items.data()};
+                           p->items.data(), p->row_chunks.data()};
   size_t counts[] = {p->cu.size(), p->cui.size(), p->pos.size(), p->srow_joint.size(),
                      p->srow_seq.size(), p->joint_srow.size(), p->img_seq.size(),
                      p->img_pair.size(), p->img_target.size(), p->seq_role.size(),
-                     p->items.size()};
-  const int np = 11;
-  size_t off[12];
+                     p->items.size(), p->row_chunks.size()};
+  const int np = 12;
+  size_t off[13];
   size_t o = 0;
   for (int i = 0; i < np; ++i) {
     off[i] = o;
@@ -416,7 +467,8 @@ extern "C" mf_status mf_plan_upload(mf_plan* p, void* stream) {
   p->d_img_target = reinterpret_cast<const int32_t*>(b + off[8]);
   p->d_seq_role = reinterpret_cast<const int32_t*>(b + off[9]);
   p->d_items = reinterpret_cast<const int32_t*>(b + off[10]);
-  p->d_t = reinterpret_cast<const float*>(b + off[11]);
+  p->d_row_chunks = reinterpret_cast<const int32_t*>(b + off[11]);
+  p->d_t = reinterpret_cast<const float*>(b + off[12]);
   p->d_blob = blob;
   p->device = dev;
   return MF_OK;
@@ -461,9 +513,11 @@ bool stream8_ok(const mf_stream_weights_fp8& s) {
 // The block forward; with w8 the four projections run on E4M3 operands: each input (a, o, a,
 // hidden) is quantised per row right before its GEMM, into the fp8 region after the bf16
 // workspace.
+// With `train`, the workspace has the training layout and the forward also keeps what the
+// backward reads (TrainLayout).
 mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weights* w,
                         const mf_block_weights_fp8* w8, const float* d_t, void* d_x_txt, void* d_x_img,
-                        void* d_ws, size_t ws_bytes, void* stream) {
+                        void* d_ws, size_t ws_bytes, void* stream, bool train = false) {
   DevInfo* di = nullptr;
   int dev = -1;
   MF_TRY(device_info(&di, &dev));
@@ -479,7 +533,10 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
     return MF_ERR_ALIGNMENT;
   const BlockLayout L = block_layout(p, d);
   const size_t fp8_bytes = w8 ? fp8_region_bytes(p, d) : 0;
-  if (ws_bytes < L.total + fp8_bytes) return MF_ERR_WORKSPACE;
+  const TrainLayout TL = train_layout(p, d);
+  if (train && (w8 != nullptr || w->txt.w_qnorm != nullptr || w->img.w_qnorm != nullptr))
+    return MF_ERR_UNSUPPORTED;  // the backward covers the plain bf16 block
+  if (ws_bytes < (train ? TL.total : L.total + fp8_bytes)) return MF_ERR_WORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(d_ws);
@@ -502,6 +559,20 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
   uint8_t* q8 = reinterpret_cast<uint8_t*>(ws + L.total);
   float* s8 = reinterpret_cast<float*>(ws + L.total + al256((size_t)N * R));
   const int F8 = w8 ? mf::kEpiF8 : 0;
+  // training: saved values (null otherwise)
+  bf16* x0 = train ? reinterpret_cast<bf16*>(ws + TL.x0) : nullptr;
+  bf16* x1 = train ? reinterpret_cast<bf16*>(ws + TL.x1) : nullptr;
+  bf16* a1 = train ? reinterpret_cast<bf16*>(ws + TL.a1) : a;
+  bf16* yo = train ? reinterpret_cast<bf16*>(ws + TL.yo) : nullptr;
+  bf16* ym = train ? reinterpret_cast<bf16*>(ws + TL.ym) : nullptr;
+  bf16* u = train ? reinterpret_cast<bf16*>(ws + TL.u) : nullptr;
+  float* lse = train ? reinterpret_cast<float*>(ws + TL.lse) : nullptr;
+  const int SAVE = train ? mf::kEpiSave : 0;
+  auto copy_x = [&](bf16* dst) -> mf_status {  // stream-sorted copy of the residual
+    if (Nt > 0) MF_CUDA(cudaMemcpyAsync(dst, xt, (size_t)Nt * H * 2, cudaMemcpyDeviceToDevice, st));
+    if (Ni > 0) MF_CUDA(cudaMemcpyAsync(dst + (size_t)Nt * H, xi, (size_t)Ni * H * 2, cudaMemcpyDeviceToDevice, st));
+    return MF_OK;
+  };
   auto quantize = [&](const bf16* src, int K) -> mf_status {
     Trace tr(MF_K_FP8, st, 0, 3.0 * N * (double)K, 1);
     return cuda_status(mf::launch_quantize_e4m3_rows(src, N, K, q8, s8, st));
@@ -518,11 +589,13 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
   }
 
   // 2. a = LN(x)(1 + scale1) + shift1, stream-sorted
-  mf::LnModArgs ln{xt, xi, Nt, N, H, p->d_srow_seq, mod, 12LL * H, 6LL * H, 0, H, a};
+  if (train) MF_TRY(copy_x(x0));
+  mf::LnModArgs ln{xt, xi, Nt, N, H, p->d_srow_seq, mod, 12LL * H, 6LL * H, 0, H, a1};
   {
     Trace tr(MF_K_LN, st, 0, 4.0 * N * H, 1);
     MF_CUDA(mf::launch_ln_modulate(ln, st));
   }
+  ln.out = a;
 
   // 3. q | k | v = a W_qkv^T + b, RoPE, scattered to joint order
   mf::GemmParams gp{};
@@ -547,8 +620,8 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
                        w8->img.s_qkv}};
     MF_TRY(run_gemm(sp, 2, mf::kEpiQkvRope | F8, 256, gp, di, st, MF_K_GEMM_QKV));
   } else {
-    GemmSpec sp[2] = {{Nt, 3 * H, H, a, w->txt.w_qkv, w->txt.b_qkv, nullptr, 0, 0, 0},
-                      {Ni, 3 * H, H, a + (size_t)Nt * H, w->img.w_qkv, w->img.b_qkv, nullptr, 0, Nt, 1}};
+    GemmSpec sp[2] = {{Nt, 3 * H, H, a1, w->txt.w_qkv, w->txt.b_qkv, nullptr, 0, 0, 0},
+                      {Ni, 3 * H, H, a1 + (size_t)Nt * H, w->img.w_qkv, w->img.b_qkv, nullptr, 0, Nt, 1}};
     MF_TRY(run_gemm(sp, 2, mf::kEpiQkvRope, 256, gp, di, st, MF_K_GEMM_QKV));
   }
 
@@ -562,9 +635,11 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
     ap.items = p->d_items;
     ap.joint_srow = p->d_joint_srow;
     ap.out = o;
+    ap.lse = lse;
     ap.H = H;
     ap.heads = d->heads;
     ap.n_items = p->n_items;
+    ap.n_tok = N;
     ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     ap.status = di->status;
     ap.wait_limit_ns = wait_limit_ns();
@@ -580,10 +655,12 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
                       {Ni, H, H, q8 + (size_t)Nt * H, w8->img.q_o, w->img.b_o, xi, H, Nt, 1, w8->img.s_o}};
     MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid | F8, 256, gp, di, st, MF_K_GEMM_OPROJ));
   } else {
-    GemmSpec sp[2] = {{Nt, H, H, o, w->txt.w_o, w->txt.b_o, xt, H, 0, 0},
-                      {Ni, H, H, o + (size_t)Nt * H, w->img.w_o, w->img.b_o, xi, H, Nt, 1}};
-    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid, 256, gp, di, st, MF_K_GEMM_OPROJ));
+    GemmSpec sp[2] = {{Nt, H, H, o, w->txt.w_o, w->txt.b_o, xt, H, 0, 0, nullptr, yo},
+                      {Ni, H, H, o + (size_t)Nt * H, w->img.w_o, w->img.b_o, xi, H, Nt, 1, nullptr,
+                       yo ? yo + (size_t)Nt * H : nullptr}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid | SAVE, 256, gp, di, st, MF_K_GEMM_OPROJ));
   }
+  if (train) MF_TRY(copy_x(x1));
 
   // 6. a = LN(x)(1 + scale2) + shift2
   ln.shift_off = 3 * H;
@@ -601,9 +678,10 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
                        w8->img.s_1}};
     MF_TRY(run_gemm(sp, 2, mf::kEpiGelu | F8, 256, gp, di, st, MF_K_GEMM_UP));
   } else {
-    GemmSpec sp[2] = {{Nt, R, H, a, w->txt.w_1, w->txt.b_1, hid, R, 0, 0},
-                      {Ni, R, H, a + (size_t)Nt * H, w->img.w_1, w->img.b_1, hid + (size_t)Nt * R, R, Nt, 1}};
-    MF_TRY(run_gemm(sp, 2, mf::kEpiGelu, 256, gp, di, st, MF_K_GEMM_UP));
+    GemmSpec sp[2] = {{Nt, R, H, a, w->txt.w_1, w->txt.b_1, hid, R, 0, 0, nullptr, u},
+                      {Ni, R, H, a + (size_t)Nt * H, w->img.w_1, w->img.b_1, hid + (size_t)Nt * R, R, Nt, 1, nullptr,
+                       u ? u + (size_t)Nt * R : nullptr}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGelu | SAVE, 256, gp, di, st, MF_K_GEMM_UP));
   }
 
   // 8. x += gate2 (hidden W_2^T + b_2)
@@ -614,9 +692,10 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
                       {Ni, H, R, q8 + (size_t)Nt * R, w8->img.q_2, w->img.b_2, xi, H, Nt, 1, w8->img.s_2}};
     MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid | F8, 256, gp, di, st, MF_K_GEMM_DOWN));
   } else {
-    GemmSpec sp[2] = {{Nt, H, R, hid, w->txt.w_2, w->txt.b_2, xt, H, 0, 0},
-                      {Ni, H, R, hid + (size_t)Nt * R, w->img.w_2, w->img.b_2, xi, H, Nt, 1}};
-    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid, 256, gp, di, st, MF_K_GEMM_DOWN));
+    GemmSpec sp[2] = {{Nt, H, R, hid, w->txt.w_2, w->txt.b_2, xt, H, 0, 0, nullptr, ym},
+                      {Ni, H, R, hid + (size_t)Nt * R, w->img.w_2, w->img.b_2, xi, H, Nt, 1, nullptr,
+                       ym ? ym + (size_t)Nt * H : nullptr}};
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid | SAVE, 256, gp, di, st, MF_K_GEMM_DOWN));
   }
   return MF_OK;
 }
@@ -626,6 +705,306 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
                                       const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
                                       size_t ws_bytes, void* stream) {
   return block_forward(p, d, w, nullptr, d_t, d_x_txt, d_x_img, d_ws, ws_bytes, stream);
+}
+
+extern "C" size_t mf_block_train_workspace_bytes(const mf_plan* p, const mf_dims* d) {
+  if (p == nullptr || check_dims(d) != MF_OK) return 0;
+  return train_layout(p, d).total;
+}
+
+extern "C" mf_status mf_block_forward_train(const mf_plan* p, const mf_dims* d, const mf_block_weights* w,
+                                            const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
+                                            size_t ws_bytes, void* stream) {
+  return block_forward(p, d, w, nullptr, d_t, d_x_txt, d_x_img, d_ws, ws_bytes, stream, true);
+}
+
+// ====================================================================== block backward
+namespace {
+mf_status attention_args(const mf_plan* p, int32_t heads, int32_t head_dim, DevInfo** di) {
+  int dev = -1;
+  MF_TRY(device_info(di, &dev));
+  MF_TRY(check_plan(p, dev));
+  if (heads <= 0) return MF_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
+  return MF_OK;
+}
+
+// Backward workspace: the f32 dq accumulator [N][H], delta [heads][N] f32, do in joint order
+// [N][H] bf16.
+struct AttnBwdLayout {
+  size_t acc, delta, do_joint, total;
+};
+AttnBwdLayout attn_bwd_layout(const mf_plan* p, int heads, int head_dim) {
+  AttnBwdLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = al256(o + bytes); return r; };
+  const size_t N = p->N, H = (size_t)heads * head_dim;
+  L.acc = take(N * H * 4);
+  L.delta = take((size_t)heads * N * 4);
+  L.do_joint = take(N * H * 2);
+  L.total = o;
+  return L;
+}
+
+// CTAs of the attention backward: one per (sample, 128-key block, head).
+long long attn_bwd_ctas(const mf_plan* p, int heads) {
+  long long n = 0;
+  for (int s = 0; s < p->S; ++s) n += (p->cu[s + 1] - p->cu[s] + 127) / 128;
+  return n * heads;
+}
+
+mf_status attention_backward(const mf_plan* p, int heads, int head_dim, const bf16* q, const bf16* k,
+                             const bf16* v, const bf16* o, const float* lse, const bf16* dout, int dout_joint,
+                             bf16* dq, bf16* dk, bf16* dv, char* ws, const DevInfo* di, cudaStream_t st) {
+  const int H = heads * head_dim, N = p->N;
+  const AttnBwdLayout L = attn_bwd_layout(p, heads, head_dim);
+  float* acc = reinterpret_cast<float*>(ws + L.acc);
+  float* delta = reinterpret_cast<float*>(ws + L.delta);
+  bf16* dj = dout_joint ? nullptr : reinterpret_cast<bf16*>(ws + L.do_joint);
+  {
+    Trace tr(MF_K_ATTN_BWD, st, 0, (double)N * H * (2.0 + 2.0 + (dj ? 2.0 : 0.0) + 4.0), 1);
+    MF_CUDA(mf::launch_attention_bwd_prep(o, dout, dout_joint, p->d_joint_srow, N, H, head_dim, dj, delta, acc,
+                                          di->sms, st));
+  }
+  mf::AttnBwdParams bp{};
+  if (!make_tmap(&bp.tmK, k, H, N, 128) || !make_tmap(&bp.tmV, v, H, N, 128) ||
+      !make_tmap(&bp.tmQ, q, H, N, 64) || !make_tmap(&bp.tmDO, dj ? dj : dout, H, N, 64) ||
+      !make_tmap_f32(&bp.tmDQ, acc, H, N, 32, 64))
+    return MF_ERR_CUDA;
+  bp.cu = p->d_cu;
+  bp.items = p->d_items;
+  bp.n_items = p->n_items;
+  bp.lse = lse;
+  bp.delta = delta;
+  bp.dk = dk;
+  bp.dv = dv;
+  bp.n_tok = N;
+  bp.H = H;
+  bp.heads = heads;
+  bp.head_dim = head_dim;
+  bp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+  bp.scale = (float)(1.0 / std::sqrt((double)head_dim));
+  bp.status = di->status;
+  bp.wait_limit_ns = wait_limit_ns();
+  {
+    // S^T, dP^T, dV, dK, dQ: five products of 2 L_i^2 D flops per head
+    Trace tr(MF_K_ATTN_BWD, st, 10.0 * p->sum_L2 * H, 0, 1);
+    MF_CUDA(mf::launch_attention_bwd(bp, attn_bwd_ctas(p, heads), st));
+  }
+  if (dq != nullptr) {
+    Trace tr(MF_K_ATTN_BWD, st, 0, (double)N * H * 6.0, 1);
+    MF_CUDA(mf::launch_attention_bwd_dq(acc, dq, (long long)N * H, di->sms, st));
+  }
+  return MF_OK;
+}
+}  // namespace
+
+namespace {
+// Backward workspace: dmod [S][2][6H] f32; dy (the gated-residual gradients of the MLP and then
+// the attention branch) [N][H] bf16; du [N][rH] bf16; da (LN + modulate output gradients) [N][H]
+// bf16; dx1 [N][H] f32; do [N][H] bf16; dqkv [N][3H] bf16; dk, dv [N][H] bf16 joint order; the
+// attention backward's own workspace.
+struct BwdLayout {
+  size_t dmod, dy, du, da, dx1, dout, dqkv, dk, dv, attn, total;
+};
+
+BwdLayout bwd_layout(const mf_plan* p, const mf_dims* d) {
+  BwdLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = al256(o + bytes); return r; };
+  const size_t S = p->S, N = p->N, H = d->hidden, R = (size_t)d->mlp_ratio * H;
+  L.dmod = take(S * 12 * H * 4);
+  L.dy = take(N * H * 2);
+  L.du = take(N * R * 2);
+  L.da = take(N * H * 2);
+  L.dx1 = take(N * H * 4);
+  L.dout = take(N * H * 2);
+  L.dqkv = take(N * 3 * H * 2);
+  L.dk = take(N * H * 2);
+  L.dv = take(N * H * 2);
+  L.attn = take(attn_bwd_layout(p, d->heads, H / d->heads).total);
+  L.total = o;
+  return L;
+}
+
+bool grads_ok(const mf_stream_grads& g) {
+  const float* ptrs[] = {g.w_mod, g.b_mod, g.w_qkv, g.b_qkv, g.w_o, g.b_o, g.w_1, g.b_1, g.w_2, g.b_2};
+  for (const float* q : ptrs)
+    if (q == nullptr || !aligned(q, 16)) return false;
+  return true;
+}
+}  // namespace
+
+extern "C" size_t mf_block_backward_workspace_bytes(const mf_plan* p, const mf_dims* d) {
+  if (p == nullptr || check_dims(d) != MF_OK) return 0;
+  return bwd_layout(p, d).total;
+}
+
+extern "C" mf_status mf_block_backward(const mf_plan* p, const mf_dims* d, const mf_block_weights* w,
+                                       const void* d_train_ws, size_t train_ws_bytes, void* d_dx_txt,
+                                       void* d_dx_img, const mf_block_grads* g, float* d_dc, void* d_ws,
+                                       size_t ws_bytes, void* stream) {
+  DevInfo* di = nullptr;
+  int dev = -1;
+  MF_TRY(device_info(&di, &dev));
+  MF_TRY(check_plan(p, dev));
+  MF_TRY(check_dims(d));
+  if (w == nullptr || !stream_ok(w->txt) || !stream_ok(w->img) || g == nullptr || !grads_ok(g->txt) ||
+      !grads_ok(g->img))
+    return MF_ERR_INVALID_ARG;
+  if (w->txt.w_qnorm != nullptr || w->img.w_qnorm != nullptr) return MF_ERR_UNSUPPORTED;
+  if (p->N == 0) return MF_OK;
+  if ((p->Nt > 0 && d_dx_txt == nullptr) || (p->Ni > 0 && d_dx_img == nullptr) || d_train_ws == nullptr ||
+      d_ws == nullptr || d_dc == nullptr)
+    return MF_ERR_INVALID_ARG;
+  if (!aligned(d_dx_txt, 16) || !aligned(d_dx_img, 16) || !aligned(d_train_ws, 256) || !aligned(d_ws, 256) ||
+      !aligned(d_dc, 16))
+    return MF_ERR_ALIGNMENT;
+  const TrainLayout TL = train_layout(p, d);
+  const BwdLayout L = bwd_layout(p, d);
+  if (train_ws_bytes < TL.total || ws_bytes < L.total) return MF_ERR_WORKSPACE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const char* tw = static_cast<const char*>(d_train_ws);
+  char* ws = static_cast<char*>(d_ws);
+  const int S = p->S, N = p->N, Nt = p->Nt, Ni = p->Ni, H = d->hidden, heads = d->heads, D = H / heads;
+  const int R = d->mlp_ratio * H;
+  auto T = [&](size_t off) { return reinterpret_cast<const bf16*>(tw + off); };
+  const float* c = reinterpret_cast<const float*>(tw + TL.base.off[0]);
+  const float* mod = reinterpret_cast<const float*>(tw + TL.base.off[1]);
+  const bf16* a2 = T(TL.base.off[2]);
+  const bf16 *q = T(TL.base.off[3]), *k = T(TL.base.off[4]), *v = T(TL.base.off[5]), *o = T(TL.base.off[6]);
+  const bf16* hid = T(TL.base.off[7]);
+  const bf16 *x0 = T(TL.x0), *x1 = T(TL.x1), *a1 = T(TL.a1), *yo = T(TL.yo), *ym = T(TL.ym), *u = T(TL.u);
+  const float* lse = reinterpret_cast<const float*>(tw + TL.lse);
+  float* dmod = reinterpret_cast<float*>(ws + L.dmod);
+  bf16* dy = reinterpret_cast<bf16*>(ws + L.dy);
+  bf16* du = reinterpret_cast<bf16*>(ws + L.du);
+  bf16* da = reinterpret_cast<bf16*>(ws + L.da);
+  float* dx1 = reinterpret_cast<float*>(ws + L.dx1);
+  bf16* dout = reinterpret_cast<bf16*>(ws + L.dout);
+  bf16* dqkv = reinterpret_cast<bf16*>(ws + L.dqkv);
+  bf16* dk = reinterpret_cast<bf16*>(ws + L.dk);
+  bf16* dv = reinterpret_cast<bf16*>(ws + L.dv);
+  bf16* gx_t = static_cast<bf16*>(d_dx_txt);
+  bf16* gx_i = static_cast<bf16*>(d_dx_img);
+  const mf_stream_grads* gs[2] = {&g->txt, &g->img};
+  const mf_stream_weights* wsm[2] = {&w->txt, &w->img};
+  const int rows[2] = {Nt, Ni}, roff[2] = {0, Nt};
+
+  // accumulated outputs start at zero; a stream without rows has zero weight gradients
+  MF_CUDA(cudaMemsetAsync(dmod, 0, (size_t)S * 12 * H * 4, st));
+  for (int m = 0; m < 2; ++m) {
+    MF_CUDA(cudaMemsetAsync(gs[m]->b_o, 0, (size_t)H * 4, st));
+    MF_CUDA(cudaMemsetAsync(gs[m]->b_1, 0, (size_t)R * 4, st));
+    MF_CUDA(cudaMemsetAsync(gs[m]->b_2, 0, (size_t)H * 4, st));
+    MF_CUDA(cudaMemsetAsync(gs[m]->b_qkv, 0, (size_t)3 * H * 4, st));
+    if (rows[m] == 0) {
+      MF_CUDA(cudaMemsetAsync(gs[m]->w_qkv, 0, (size_t)3 * H * H * 4, st));
+      MF_CUDA(cudaMemsetAsync(gs[m]->w_o, 0, (size_t)H * H * 4, st));
+      MF_CUDA(cudaMemsetAsync(gs[m]->w_1, 0, (size_t)R * H * 4, st));
+      MF_CUDA(cudaMemsetAsync(gs[m]->w_2, 0, (size_t)H * R * 4, st));
+    }
+  }
+  mf::RowBwdArgs ra{};
+  ra.H = H;
+  ra.n_first = Nt;
+  ra.chunks = p->d_row_chunks;
+  ra.n_chunks = p->n_row_chunks;
+  ra.g_first = gx_t;
+  ra.g_second = gx_i;
+  ra.mod = mod;
+  ra.dmod = dmod;
+  mf::GemmParams gp{};
+  // input-gradient GEMM per stream: out[rows][N] = A[rows][K] W, W stored [K][N]
+  auto dgrad = [&](const bf16* A, int K, int Nn, const void* W0, const void* W1, bf16* out, int epi,
+                   const bf16* aux, int kind) -> mf_status {
+    GemmSpec sp[2];
+    int n = 0;
+    for (int m = 0; m < 2; ++m) {
+      if (rows[m] == 0) continue;
+      sp[n++] = GemmSpec{rows[m], Nn, K, A + (size_t)roff[m] * K, m ? W1 : W0, nullptr, out + (size_t)roff[m] * Nn,
+                         Nn, roff[m], m, nullptr, aux ? const_cast<bf16*>(aux) + (size_t)roff[m] * Nn : nullptr};
+    }
+    return run_gemm(sp, n, epi, 256, gp, di, st, kind, mf::kMajBMN);
+  };
+  // weight-gradient GEMM per stream: dW[Mo][Ni] = dY^T X over the stream's rows
+  auto wgrad = [&](const bf16* dY, int Mo, const bf16* X, int Nn, float* out0, float* out1, int kind) -> mf_status {
+    GemmSpec sp[2];
+    int n = 0;
+    for (int m = 0; m < 2; ++m) {
+      if (rows[m] == 0) continue;
+      sp[n++] = GemmSpec{Mo, Nn, rows[m], dY + (size_t)roff[m] * Mo, X + (size_t)roff[m] * Nn, nullptr,
+                         m ? out1 : out0, Nn, 0, m};
+    }
+    return run_gemm(sp, n, mf::kEpiBiasF32, 256, gp, di, st, kind, mf::kMajMNMN);
+  };
+  auto row_kernel = [&](int mode, double bytes_per_row) -> mf_status {
+    ra.mode = mode;
+    Trace tr(MF_K_BLOCK_BWD, st, 0, bytes_per_row * N, 1);
+    return cuda_status(mf::launch_row_bwd(ra, st));
+  };
+
+  // 1. MLP branch: dy_m = gate2 g; dgate2, db_2
+  ra.y = ym;
+  ra.out_bf16 = dy;
+  ra.bias_grad[0] = gs[0]->b_2;
+  ra.bias_grad[1] = gs[1]->b_2;
+  MF_TRY(row_kernel(mf::kRowGate2, 6.0 * H));
+  // 2. du = (dy_m W_2) * GELU'(u);  dW_2 = dy_m^T h
+  MF_TRY(dgrad(dy, H, R, w->txt.w_2, w->img.w_2, du, mf::kEpiGeluBwd, u, MF_K_GEMM_DOWN));
+  MF_TRY(wgrad(dy, H, hid, R, gs[0]->w_2, gs[1]->w_2, MF_K_GEMM_DOWN));
+  // 3. da_2 = du W_1;  dW_1 = du^T a_2;  db_1
+  MF_TRY(dgrad(du, R, H, w->txt.w_1, w->img.w_1, da, mf::kEpiBiasBf16, nullptr, MF_K_GEMM_UP));
+  MF_TRY(wgrad(du, R, a2, H, gs[0]->w_1, gs[1]->w_1, MF_K_GEMM_UP));
+  {
+    Trace tr(MF_K_BLOCK_BWD, st, 0, 2.0 * N * R, 1);
+    MF_CUDA(mf::launch_col_sum(du, R, p->d_row_chunks, p->n_row_chunks, gs[0]->b_1, gs[1]->b_1, st));
+  }
+  // 4. LN + modulate #2 backward: dx1 = g + LN'(da_2 (1 + scale2)); dy_o = gate1 dx1; dshift2,
+  //    dscale2, dgate1, db_o
+  ra.da = da;
+  ra.x = x1;
+  ra.y = yo;
+  ra.out_f32 = dx1;
+  ra.out_bf16 = dy;
+  ra.bias_grad[0] = gs[0]->b_o;
+  ra.bias_grad[1] = gs[1]->b_o;
+  MF_TRY(row_kernel(mf::kRowLn2, 16.0 * H));
+  // 5. do = dy_o W_o;  dW_o = dy_o^T o
+  MF_TRY(dgrad(dy, H, H, w->txt.w_o, w->img.w_o, dout, mf::kEpiBiasBf16, nullptr, MF_K_GEMM_OPROJ));
+  MF_TRY(wgrad(dy, H, o, H, gs[0]->w_o, gs[1]->w_o, MF_K_GEMM_OPROJ));
+  // 6. attention backward (dq kept in the f32 accumulator), then dqkv with the inverse RoPE
+  char* aws = ws + L.attn;
+  MF_TRY(attention_backward(p, heads, D, q, k, v, o, lse, dout, 0, nullptr, dk, dv, aws, di, st));
+  {
+    Trace tr(MF_K_BLOCK_BWD, st, 0, (double)N * H * (4.0 + 2.0 + 2.0 + 6.0), 1);
+    MF_CUDA(mf::launch_qkv_grad_gather(reinterpret_cast<const float*>(aws + attn_bwd_layout(p, heads, D).acc), dk, dv,
+                                       p->d_srow_joint, p->d_pos, N, H, D, dqkv, di->sms, st));
+  }
+  // 7. da_1 = dqkv W_qkv;  dW_qkv = dqkv^T a_1;  db_qkv
+  MF_TRY(dgrad(dqkv, 3 * H, H, w->txt.w_qkv, w->img.w_qkv, da, mf::kEpiBiasBf16, nullptr, MF_K_GEMM_QKV));
+  MF_TRY(wgrad(dqkv, 3 * H, a1, H, gs[0]->w_qkv, gs[1]->w_qkv, MF_K_GEMM_QKV));
+  {
+    Trace tr(MF_K_BLOCK_BWD, st, 0, 2.0 * N * 3 * H, 1);
+    MF_CUDA(mf::launch_col_sum(dqkv, 3 * H, p->d_row_chunks, p->n_row_chunks, gs[0]->b_qkv, gs[1]->b_qkv, st));
+  }
+  // 8. LN + modulate #1 backward: dx0 = dx1 + LN'(da_1 (1 + scale1)) into the caller's buffers;
+  //    dshift1, dscale1
+  ra.x = x0;
+  ra.carry = dx1;
+  ra.out_first = gx_t;
+  ra.out_second = gx_i;
+  MF_TRY(row_kernel(mf::kRowLn1, 14.0 * H));
+  // 9. modulation: dW_mod = dmod^T c, db_mod, dc = W_mod^T dmod (both streams)
+  {
+    Trace tr(MF_K_BLOCK_BWD, st, 2.0 * 2 * 2 * S * 6.0 * H * H, 2.0 * 6.0 * H * H * (4.0 + 2.0), 3);
+    MF_CUDA(mf::launch_mod_bwd(dmod, c, S, H, static_cast<const bf16*>(w->txt.w_mod),
+                               static_cast<const bf16*>(w->img.w_mod), gs[0]->w_mod, gs[0]->b_mod, gs[1]->w_mod,
+                               gs[1]->b_mod, d_dc, st));
+  }
+  (void)wsm;
+  return MF_OK;
 }
 
 extern "C" size_t mf_block_fp8_workspace_bytes(const mf_plan* p, const mf_dims* d) {
@@ -836,11 +1215,68 @@ extern "C" mf_status mf_attention(const mf_plan* p, int32_t heads, int32_t head_
   ap.H = H;
   ap.heads = heads;
   ap.n_items = p->n_items;
+  ap.n_tok = p->N;
   ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
   ap.status = di->status;
   ap.wait_limit_ns = wait_limit_ns();
   Trace tr(MF_K_ATTN, static_cast<cudaStream_t>(stream), 4.0 * p->sum_L2 * H, 0, 1);
   return cuda_status(mf::launch_attention(ap, head_dim, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" mf_status mf_attention_lse(const mf_plan* p, int32_t heads, int32_t head_dim, const void* d_q,
+                                      const void* d_k, const void* d_v, void* d_o, float* d_lse, void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(attention_args(p, heads, head_dim, &di));
+  if (p->N == 0) return MF_OK;
+  if (d_q == nullptr || d_k == nullptr || d_v == nullptr || d_o == nullptr || d_lse == nullptr)
+    return MF_ERR_INVALID_ARG;
+  if (!aligned(d_q, 16) || !aligned(d_k, 16) || !aligned(d_v, 16) || !aligned(d_o, 16) || !aligned(d_lse, 16))
+    return MF_ERR_ALIGNMENT;
+  const int H = heads * head_dim;
+  mf::AttnParams ap{};
+  if (!make_tmap(&ap.tmQ, d_q, H, p->N, 128) || !make_tmap(&ap.tmK, d_k, H, p->N, 128) ||
+      !make_tmap(&ap.tmV, d_v, H, p->N, 128))
+    return MF_ERR_CUDA;
+  ap.cu = p->d_cu;
+  ap.items = p->d_items;
+  ap.joint_srow = p->d_joint_srow;
+  ap.out = static_cast<bf16*>(d_o);
+  ap.lse = d_lse;
+  ap.H = H;
+  ap.heads = heads;
+  ap.n_items = p->n_items;
+  ap.n_tok = p->N;
+  ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+  ap.status = di->status;
+  ap.wait_limit_ns = wait_limit_ns();
+  Trace tr(MF_K_ATTN, static_cast<cudaStream_t>(stream), 4.0 * p->sum_L2 * H, 0, 1);
+  return cuda_status(mf::launch_attention(ap, head_dim, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" size_t mf_attention_backward_workspace_bytes(const mf_plan* p, int32_t heads, int32_t head_dim) {
+  if (p == nullptr || heads <= 0 || (head_dim != 64 && head_dim != 128)) return 0;
+  return attn_bwd_layout(p, heads, head_dim).total;
+}
+
+extern "C" mf_status mf_attention_backward(const mf_plan* p, int32_t heads, int32_t head_dim, const void* d_q,
+                                           const void* d_k, const void* d_v, const void* d_o, const float* d_lse,
+                                           const void* d_do, void* d_dq, void* d_dk, void* d_dv, void* d_ws,
+                                           size_t ws_bytes, void* stream) {
+  DevInfo* di = nullptr;
+  MF_TRY(attention_args(p, heads, head_dim, &di));
+  if ((heads * head_dim) % 256 != 0) return MF_ERR_UNSUPPORTED;
+  if (p->N == 0) return MF_OK;
+  const void* ptrs[] = {d_q, d_k, d_v, d_o, d_lse, d_do, d_dq, d_dk, d_dv, d_ws};
+  for (const void* x : ptrs)
+    if (x == nullptr) return MF_ERR_INVALID_ARG;
+  for (const void* x : ptrs)
+    if (!aligned(x, 16)) return MF_ERR_ALIGNMENT;
+  if (!aligned(d_ws, 256)) return MF_ERR_ALIGNMENT;
+  if (ws_bytes < attn_bwd_layout(p, heads, head_dim).total) return MF_ERR_WORKSPACE;
+  return attention_backward(p, heads, head_dim, static_cast<const bf16*>(d_q), static_cast<const bf16*>(d_k),
+                            static_cast<const bf16*>(d_v), static_cast<const bf16*>(d_o), d_lse,
+                            static_cast<const bf16*>(d_do), 0, static_cast<bf16*>(d_dq), static_cast<bf16*>(d_dk),
+                            static_cast<bf16*>(d_dv), static_cast<char*>(d_ws), di, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" mf_status mf_quantize_fp8_rows(int32_t M, int32_t K, const void* d_x, void* d_q, float* d_scale,

@@ -7,6 +7,10 @@
 // block, head) and loops over that sample's own 128-row key tiles, so the cost is
 // sum_i L_i^2, not (sum_i L_i)^2.
 //
+// CTAs are ordered sample by sample (longest first); inside a sample the query blocks run
+// fastest, then the heads, so the CTAs resident at the same time share one or a few heads' K
+// and V in L2 instead of streaming every head of the sample at once.
+//
 // One CTA per work item, 320 threads.  The 256 query rows are two 128-row tiles t = 0, 1,
 // each with its own softmax warpgroup, so the tensor core works on one tile while the other
 // tile's exponentials run:
@@ -116,12 +120,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const int lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
 
-  const int item = blockIdx.x / p.heads;
-  const int h = blockIdx.x - item * p.heads;
-  const int seq = __ldg(p.items + 2 * item);
-  const int qb = __ldg(p.items + 2 * item + 1);
-  const int kv0 = __ldg(p.cu + seq);
-  const int len = __ldg(p.cu + seq + 1) - kv0;
+  // (sample, head, query block) of this CTA: the work list holds each sample's query blocks
+  // contiguously, samples longest first; a sample spans (query blocks) x heads CTAs
+  int seq = 0, kv0 = 0, len = 0, nqb = 1, base = 0;
+  for (int it = 0; it < p.n_items;) {
+    seq = __ldg(p.items + 2 * it);
+    kv0 = __ldg(p.cu + seq);
+    len = __ldg(p.cu + seq + 1) - kv0;
+    nqb = (len + 2 * kT - 1) / (2 * kT);
+    if ((int)blockIdx.x < base + nqb * p.heads) break;
+    base += nqb * p.heads;
+    it += nqb;
+  }
+  const int h = ((int)blockIdx.x - base) / nqb;
+  const int qb = ((int)blockIdx.x - base) - h * nqb;
   const int q0 = kv0 + qb * 2 * kT;
   const int n_kv = (len + kT - 1) / kT;
   const int n_t = (len - qb * 2 * kT) > kT ? 2 : 1;  // query tiles of this block inside the sample
@@ -351,6 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           // row, then writes whole rows (D bf16 each) with consecutive lanes on consecutive
           // 16-byte chunks of a row
           const float inv_l = 1.0f / l;
+          if (p.lse != nullptr && q0 + t * kT + row < kv0 + len)  // ln sum_k exp(s_k), s = q.k / sqrt(D)
+            p.lse[(size_t)h * p.n_tok + q0 + t * kT + row] = (m + log2f(l)) * 0.6931471805599453f;
           uint8_t* stg = smem + L::off_q + t * L::Q;   // [128 rows][D bf16]
           constexpr int kChunks = D / 8;               // 16-byte chunks per row
 #pragma unroll

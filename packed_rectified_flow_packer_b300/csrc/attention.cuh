@@ -11,6 +11,9 @@ struct AttnParams {
   const int* items;           // [n_items][2] (sample, query tile), longest samples first
   const int* joint_srow;      // [N] stream-sorted row of each joint token
   bf16* out;                  // [N][H] stream-sorted output
+  float* lse;                 // [heads][N] natural-log logsumexp of each query row's scaled
+                              // scores, or null (not written)
+  int n_tok;                  // N
   int H;
   int heads;
   int n_items;

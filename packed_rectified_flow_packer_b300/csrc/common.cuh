@@ -105,6 +105,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int x, int y
                "r"(x), "r"(y), "r"(smem_u32(smem_src))
                : "memory");
 }
+// 2-D tiled reduce-add of one f32 box from shared memory into global memory (bulk-group
+// completion); element-wise atomic with respect to other reductions of the same elements.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* tm, int x, int y, const void* smem_src) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(x), "r"(y), "r"(smem_u32(smem_src))
+      : "memory");
+}
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -165,6 +174,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
          | ((b_mn_major ? 1u : 0u) << 16)     // B major-ness
          | ((uint32_t)(N >> 3) << 17)         // N / 8
          | ((uint32_t)(M >> 4) << 24);        // M / 16
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, each K-major or MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return idesc_bf16_f32(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);  // A major-ness
 }
 
 // Instruction descriptor, kind::f8f6f4: D f32, A and B E4M3 (format code 0), both K-major.

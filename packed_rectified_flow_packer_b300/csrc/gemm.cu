@@ -209,8 +209,31 @@ __device__ __forceinline__ void epi_row16(const GemmParams& p, const GemmProblem
   }
   add_bias16(pr, col0, v);
   if constexpr (E == kEpiGelu) {
+    if constexpr ((EPI & kEpiSave) != 0) {  // the pre-activation, for the backward
+      uint4* a = reinterpret_cast<uint4*>(static_cast<bf16*>(pr.aux) + (size_t)row * pr.ldo + col0);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        a[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                          pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.7071067811865476f));
+  } else if constexpr (E == kEpiGeluBwd) {
+    // d/du GELU(u) = Phi(u) + u phi(u), phi the standard normal density
+    const uint4* a = reinterpret_cast<const uint4*>(static_cast<const bf16*>(pr.aux) + (size_t)row * pr.ldo + col0);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 w = __ldg(a + i);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 u = unpack_bf16x2(ww[j]);
+        const float g0 = 0.5f * (1.0f + erff(u.x * 0.7071067811865476f)) + u.x * 0.3989422804014327f * __expf(-0.5f * u.x * u.x);
+        const float g1 = 0.5f * (1.0f + erff(u.y * 0.7071067811865476f)) + u.y * 0.3989422804014327f * __expf(-0.5f * u.y * u.y);
+        v[8 * i + 2 * j] *= g0;
+        v[8 * i + 2 * j + 1] *= g1;
+      }
+    }
   } else if constexpr (E == kEpiQkvRope) {
     const int which = col0 / p.H;
     if (qk_g != nullptr) {
@@ -271,6 +294,10 @@ __device__ __forceinline__ void epi_store8(const GemmParams& p, const GemmProble
     dst = static_cast<bf16*>(pr.out) + (size_t)row * pr.ldo + col;
   }
   if constexpr (E == kEpiGateResid) {
+    if constexpr ((EPI & kEpiSave) != 0)  // the ungated branch output, for the backward
+      *reinterpret_cast<uint4*>(static_cast<bf16*>(pr.aux) + (size_t)row * pr.ldo + col) =
+          make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                     pack_bf16x2(v[6], v[7]));
     const int seq = __ldg(p.srow_seq + pr.row_off + row);
     const float4* g = reinterpret_cast<const float4*>(
         p.mod + ((size_t)seq * 2 + pr.stream) * 6 * (size_t)p.H + p.gate_off + col);
@@ -500,7 +527,7 @@ constexpr int kPairThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 // lane quarter, each take 128 of the tile's 256 columns through the staged epilogue above; the
 // epilogue warps of both CTAs release an accumulator buffer by arriving on the even CTA's
 // barrier.
-template <int EPI>
+template <int EPI, int MAJ>
 __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   constexpr int STAGES = 6;
   constexpr int BN = 256;
@@ -513,7 +540,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
   constexpr bool F8 = (EPI & kEpiF8) != 0;
   constexpr int E = EPI & 7;
   constexpr int KE = F8 ? 2 * kBK : kBK;  // K elements per stage
-  constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(2 * kBM, BN) : idesc_bf16_f32(2 * kBM, BN, false);
+  constexpr bool AMN = (MAJ & kMajAMN) != 0, BMN = (MAJ & kMajBMN) != 0;
+  static_assert(!F8 || MAJ == kMajKK, "E4M3 operands are K-major");
+  constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(2 * kBM, BN) : idesc_bf16_f32_mn(2 * kBM, BN, AMN, BMN);
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
@@ -579,7 +608,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     for (int tile = pair; ok && tile < total; tile += n_pairs) {
       int pi, m, n;
       decode_tile(p, tile, pi, m, n);
-      const int nkb = p.prob[pi].K / KE;
+      const int nkb = (p.prob[pi].K + KE - 1) / KE;
       for (int kb = 0; kb < nkb; ++kb) {
         if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1, lim)) ||
             __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
@@ -590,8 +619,19 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
           uint8_t* sa = smem + stage * STAGE_BYTES;
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * STAGE_BYTES);
           const uint32_t fb = mapa_shared(&full_bar[stage], 0);
-          tma_load_2d_pair(sa, &p.tmA[pi], kb * KE, m * 2 * kBM + rank * kBM, fb);
-          tma_load_2d_pair(sa + A_BYTES, &p.tmB[pi], kb * KE, n * BN + rank * (BN / 2), fb);
+          const int a_row = m * 2 * kBM + rank * kBM, b_row = n * BN + rank * (BN / 2);
+          if constexpr (AMN) {  // [K][M] storage: two 64 (M) x 64 (K) boxes
+            tma_load_2d_pair(sa, &p.tmA[pi], a_row, kb * KE, fb);
+            tma_load_2d_pair(sa + A_BYTES / 2, &p.tmA[pi], a_row + 64, kb * KE, fb);
+          } else {
+            tma_load_2d_pair(sa, &p.tmA[pi], kb * KE, a_row, fb);
+          }
+          if constexpr (BMN) {
+            tma_load_2d_pair(sa + A_BYTES, &p.tmB[pi], b_row, kb * KE, fb);
+            tma_load_2d_pair(sa + A_BYTES + B_BYTES / 2, &p.tmB[pi], b_row + 64, kb * KE, fb);
+          } else {
+            tma_load_2d_pair(sa + A_BYTES, &p.tmB[pi], kb * KE, b_row, fb);
+          }
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -612,7 +652,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
       for (int tile = pair; ok && tile < total; tile += n_pairs) {
         int pi, m, n;
         decode_tile(p, tile, pi, m, n);
-        const int nkb = p.prob[pi].K / KE;
+        const int nkb = (p.prob[pi].K + KE - 1) / KE;
         if (!__all_sync(0xffffffffu, mbar_wait(&tempty_bar[acc], acc_phase ^ 1, lim)) ||
             __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
           ok = false;
@@ -626,14 +666,19 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_sw128(smem_u32(smem + stage * STAGE_BYTES), 16, 1024);
-          const uint64_t bd = ad + (A_BYTES >> 4);
+          // K-major: 128-byte rows of K, a K = 16 step is 32 bytes into the row.  MN-major:
+          // 128-byte rows of 64 MN elements per K index, the two 64-wide MN halves A_BYTES / 2
+          // apart, a K = 16 step is 16 rows (2048 bytes)
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t ad = AMN ? sdesc_sw128(sa, A_BYTES / 2, 1024) : sdesc_sw128(sa, 16, 1024);
+          const uint64_t bd = BMN ? sdesc_sw128(sa + A_BYTES, B_BYTES / 2, 1024) : sdesc_sw128(sa + A_BYTES, 16, 1024);
+          constexpr uint32_t a_step = AMN ? (2048 >> 4) : 2, b_step = BMN ? (2048 >> 4) : 2;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
             if constexpr (F8)
               mma_f8_pair_if(el, d_tmem, ad + k * 2, bd + k * 2, IDESC, (kb | k) != 0 ? 1u : 0u);
             else
-              mma_bf16_pair_if(el, d_tmem, ad + k * 2, bd + k * 2, IDESC, (kb | k) != 0 ? 1u : 0u);
+              mma_bf16_pair_if(el, d_tmem, ad + k * a_step, bd + k * b_step, IDESC, (kb | k) != 0 ? 1u : 0u);
           mma_commit_pair_mc_if(el, &empty_bar[stage], 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -674,7 +719,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
       const GemmProblem& pr = p.prob[pi];
       const int row0 = m * 2 * kBM + rank * kBM + q * 32;  // first of this warp's 32 rows
       float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES) + (warp - 2) * 32 * kStageRow;
-      if constexpr (E == kEpiBiasBf16 || E == kEpiGelu) {
+      if constexpr (E == kEpiBiasBf16 || E == kEpiGelu || E == kEpiGeluBwd) {
         if (p.tma_store[pi]) {
           // bf16 rows of 64 columns, 16-byte chunks swizzled as the 128-byte-swizzle tensor map
           // expects, then one TMA store of 32 rows x 64 columns per group
@@ -793,13 +838,13 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
   }
 }
 
-template <int EPI>
+template <int EPI, int MAJ = kMajKK>
 cudaError_t launch_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
   constexpr int STAGES = 6;
   // epilogue staging: 8 warps x max(32 rows of kStageRow floats, a 32 x 64 bf16 store box)
   constexpr int kStaging = 8 * (32 * kStageRow * 4 > 4096 ? 32 * kStageRow * 4 : 4096);
   const int smem = STAGES * (kBM * kBK * 2 + 128 * kBK * 2) + kStaging + 1024;
-  auto kern = gemm_pair_kernel<EPI>;
+  auto kern = gemm_pair_kernel<EPI, MAJ>;
   static int max_pairs = 0;  // clusters of two that fit on the device at once (per instantiation)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -831,8 +876,22 @@ cudaError_t launch_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_gemm_pair(const GemmParams& p, int epi, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gemm_pair(const GemmParams& p, int epi, int num_sms, cudaStream_t stream, int maj) {
+  if (maj == kMajBMN) {  // input gradients: dY W (W stored [K = out][N = in])
+    switch (epi) {
+      case kEpiBiasBf16: return launch_pair<kEpiBiasBf16, kMajBMN>(p, num_sms, stream);
+      case kEpiGeluBwd: return launch_pair<kEpiGeluBwd, kMajBMN>(p, num_sms, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (maj == kMajMNMN) {  // weight gradients: dY^T X, both stored [K = tokens][...]
+    if (epi == kEpiBiasF32) return launch_pair<kEpiBiasF32, kMajMNMN>(p, num_sms, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (maj != kMajKK) return cudaErrorInvalidValue;
   switch (epi) {
+    case kEpiGelu | kEpiSave: return launch_pair<kEpiGelu | kEpiSave>(p, num_sms, stream);
+    case kEpiGateResid | kEpiSave: return launch_pair<kEpiGateResid | kEpiSave>(p, num_sms, stream);
     case kEpiBiasBf16: return launch_pair<kEpiBiasBf16>(p, num_sms, stream);
     case kEpiBiasF32: return launch_pair<kEpiBiasF32>(p, num_sms, stream);
     case kEpiQkvRope: return launch_pair<kEpiQkvRope>(p, num_sms, stream);

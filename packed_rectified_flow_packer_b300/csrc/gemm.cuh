@@ -15,9 +15,18 @@ enum GemmEpi : int {
   kEpiQkvRope = 2,    // q | k | v = acc + bias; RoPE on q, k; rows scattered to joint order
   kEpiGateResid = 3,  // x += gate[seq] * (acc + bias), x bf16 in place
   kEpiGelu = 4,       // out bf16 = GELU(acc + bias)
+  kEpiGeluBwd = 5,    // out bf16 = acc * GELU'(aux[row][col]) (aux: the saved pre-activation)
   kEpiF8 = 8,         // flag on any of the above (pair kernel): E4M3 operands, and the
                       // accumulator is first multiplied by row_scale[row_off + row] * col_scale[col]
+  kEpiSave = 16,      // flag on kEpiGelu / kEpiGateResid (pair kernel, bf16): the value before
+                      // GELU / before the gate (acc + bias) is also written to aux[row][col]
 };
+
+// Operand majorness of the pair kernel (bf16 only): bit 0 A, bit 1 B.  K-major (0): the matrix
+// is stored [rows][K], as in C = A B^T.  MN-major (1): it is stored [K][rows] (A^T or B^T in
+// memory), boxes of 64 x 64 with the MN dimension innermost; used by the backward's weight-
+// gradient (both) and input-gradient (B) products.
+enum GemmMajor : int { kMajKK = 0, kMajAMN = 1, kMajBMN = 2, kMajMNMN = 3 };
 
 struct GemmProblem {
   int M, N, K;
@@ -27,6 +36,7 @@ struct GemmProblem {
   const bf16* bias;       // [N] or nullptr
   const float* col_scale; // kEpiF8: [N] dequantisation scale of B's rows (output columns)
   void* out;              // output (or the residual x for kEpiGateResid)
+  void* aux;              // bf16 [M][ldo]: kEpiSave output, kEpiGeluBwd input; else null
 };
 
 struct GemmParams {
@@ -61,7 +71,8 @@ cudaError_t launch_gemm(const GemmParams& p, int BN, int epi, int num_sms, cudaS
 
 // Launches the persistent CTA-pair kernel: 256 x 256 tiles, tmA boxes of 128 rows (each CTA's
 // half of the tile's rows), tmB boxes of 128 rows (each CTA's half of the tile's columns),
-// tiles_m counted in 256-row tiles.
-cudaError_t launch_gemm_pair(const GemmParams& p, int epi, int num_sms, cudaStream_t stream);
+// tiles_m counted in 256-row tiles.  An MN-major operand's tensor map has boxes of 64 (MN) x 64
+// (K) over its [K][MN] storage; K need not be a multiple of 64 (the tail reads zeros).
+cudaError_t launch_gemm_pair(const GemmParams& p, int epi, int num_sms, cudaStream_t stream, int maj = kMajKK);
 
 }  // namespace mf

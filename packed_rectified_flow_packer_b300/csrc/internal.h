@@ -27,6 +27,9 @@ struct mf_plan {
   std::vector<int32_t> img_target;  // [Ni]  1 = target frame
   std::vector<int32_t> seq_role;    // [S]   cfg_role
   std::vector<int32_t> items;       // [n_items*2] (sequence, query block), longest first
+  std::vector<int32_t> row_chunks;  // [n_row_chunks*4] (row0, row1, sample, stream): stream-sorted
+                                    // rows in pieces of <= kRowChunk inside one segment
+  int32_t n_row_chunks = 0;
   std::vector<float> t;             // [S]   flow time per packed sample
 
   // stream-sorted rows: text rows 0..Nt-1, then image rows Nt..Nt+Ni-1
@@ -49,12 +52,14 @@ struct mf_plan {
   const int32_t* d_img_target = nullptr;
   const int32_t* d_seq_role = nullptr;
   const int32_t* d_items = nullptr;
+  const int32_t* d_row_chunks = nullptr;
   const float* d_t = nullptr;
 };
 
 namespace mf {
 
 constexpr int kQBlock = 256;  // query rows of one attention work item (two 128-row tiles)
+constexpr int kRowChunk = 64; // rows of one chunk of the backward's row kernels
 
 // Ordinal of the current device after checking that it is an sm_103a (the library's per-device
 // state is set up on first use).  MF_ERR_UNSUPPORTED on another architecture, MF_ERR_CUDA when

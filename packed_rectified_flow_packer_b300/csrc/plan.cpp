@@ -152,6 +152,20 @@ extern "C" mf_status mf_pack(const mf_sample* samples, int32_t n, int32_t budget
     }
   }
   p->n_items = (int32_t)(p->items.size() / 2);
+
+  // row chunks of the backward's row kernels: stream-sorted rows in pieces of at most
+  // kRowChunk rows, each inside one (sample, stream) segment, as (row0, row1, sample, stream)
+  for (int32_t m = 0; m < 2; ++m)
+    for (int32_t k = 0; k < S; ++k) {
+      const int32_t a = m ? Nt + p->cui[k] : p->cut[k], b = m ? Nt + p->cui[k + 1] : p->cut[k + 1];
+      for (int32_t r = a; r < b; r += mf::kRowChunk) {
+        p->row_chunks.push_back(r);
+        p->row_chunks.push_back(std::min(b, r + mf::kRowChunk));
+        p->row_chunks.push_back(k);
+        p->row_chunks.push_back(m);
+      }
+    }
+  p->n_row_chunks = (int32_t)(p->row_chunks.size() / 4);
   *out = p;
   return MF_OK;
 }

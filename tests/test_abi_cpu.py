@@ -14,7 +14,8 @@ from tests.conftest import ROOT
 B = pytest.importorskip("packed_rectified_flow_packer_b300.binding")
 HEADER = os.path.join(ROOT, "include", "mageflow.h")
 STRUCTS = ["mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights",
-           "mf_block_weights", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_trace_entry"]
+           "mf_block_weights", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_stream_grads",
+           "mf_block_grads", "mf_trace_entry"]
 
 
 def _header_fields(name):

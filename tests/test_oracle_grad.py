@@ -113,3 +113,23 @@ def test_attention_vjp_closed_form():
         np.testing.assert_allclose(dv[:, h], dvh, rtol=0, atol=1e-12)
         np.testing.assert_allclose(dq[:, h], ds @ k[:, h] / np.sqrt(Dh), rtol=0, atol=1e-12)
         np.testing.assert_allclose(dk[:, h], ds.T @ q[:, h] / np.sqrt(Dh), rtol=0, atol=1e-12)
+
+
+def test_attention_lse_and_row_gradients():
+    """attention_lse normalises the softmax (exp(s - lse) sums to 1 over the keys, and equals
+    the softmax the forward oracle uses), and the selected-row gradients equal the
+    reverse-mode gradients on every row asked for."""
+    rng = np.random.default_rng(12)
+    L, nh, Dh = 9, 3, 16
+    q, k, v, do = (rng.standard_normal((L, nh, Dh)) for _ in range(4))
+    lse = G.attention_lse(q, k)
+    s = np.einsum("qhd,khd->hqk", q, k) / np.sqrt(Dh)
+    p = np.exp(s - lse[:, :, None])
+    np.testing.assert_allclose(p.sum(-1), 1.0, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(np.einsum("hqk,khd->qhd", p, v), M.attention(q, k, v), rtol=0, atol=1e-12)
+    dq, dk, dv = G.attention_vjp(q, k, v, do)
+    rows_q, rows_k = np.array([0, 4, 8]), np.array([1, 2, 7])
+    gq, gk, gv = G.attention_vjp_rows(q, k, v, do, rows_q, rows_k)
+    np.testing.assert_allclose(gq, dq[rows_q], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gk, dk[rows_k], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gv, dv[rows_k], rtol=0, atol=1e-12)
