@@ -44,10 +44,12 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=120)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["native16k", "cfg", "gemm", "fp8block"], default="native16k",
+    ap.add_argument("--workload", choices=["native16k", "cfg", "gemm", "fp8block", "train", "attn"], default="native16k",
                     help="native16k: the headline block-forward pack; cfg: packed vs unpacked CFG sampler; "
                          "gemm: bf16 and fp8 GEMMs alone at the block's shapes; fp8block: the block "
-                         "forward with fp8 projections against the bf16 one on the 16K packs")
+                         "forward with fp8 projections against the bf16 one on the 16K packs; train: the "
+                         "block's training forward + backward on the 16K packs; attn: varlen attention "
+                         "forward and backward alone on the 16K packs")
     return ap.parse_args()
 
 
@@ -646,6 +648,203 @@ def run_fp8_block(args, rank, world, local_rank):
             "data": "synthetic (seeded packs; N(0,1) hidden image states instead of the latent embed)"}
 
 
+def run_train(args, rank, world, local_rank):
+    """Training step of one NR-MMDiT block on the eight seeded 16K packs: mf_block_forward_train
+    (the forward that keeps what the backward reads), then mf_block_backward with a seeded
+    output gradient (input, weight, modulation and condition gradients of both streams).
+    Inputs resident in HBM; CUDA events around K steps after W warm-up steps; one traced pass
+    before the timed region gives the per-kernel table and names the dominant kernel, whose
+    launches alone carry events inside the timed region."""
+    import torch
+    import packed_rectified_flow_packer_b300 as mf
+    from packed_rectified_flow_packer_b300.device import DeviceModel, to_bf16
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dims = synth.FULL
+    H, R = dims.hidden, dims.mlp_ratio * dims.hidden
+    weights = synth.model_weights(dims, 1, seed=0)
+    model = DeviceModel(weights, device=dev)
+    d, bs = model.dims, model.block_structs[0]
+    packs = []
+    for seed in rank_seeds(rank):
+        cands = synth.native_candidates(seed)
+        plan = mf.mf_pack(cands, BUDGET)
+        mf.mf_plan_upload(plan)
+        x, _, _ = synth.pack_inputs(cands, plan.array("order"), dims, seed)
+        gen = torch.Generator(device=dev).manual_seed(1000 + seed)
+        ni, nt = plan.n_img, plan.n_txt
+        cu = plan.array("cu_seqlens").astype(np.float64)
+        packs.append({"plan": plan, "n_tok": plan.n_tok, "n_seq": plan.n_seq, "x_txt": to_bf16(x, dev),
+                      "x_img": torch.randn((ni, H), device=dev, generator=gen).to(torch.bfloat16),
+                      "g_txt": torch.randn((max(nt, 1), H), device=dev, generator=gen).to(torch.bfloat16),
+                      "g_img": torch.randn((ni, H), device=dev, generator=gen).to(torch.bfloat16),
+                      "sum_L2": float((np.diff(cu) ** 2).sum())})
+    tws = torch.empty(max(mf.mf_block_train_workspace_bytes(p["plan"], d) for p in packs), dtype=torch.uint8, device=dev)
+    bws = torch.empty(max(mf.mf_block_backward_workspace_bytes(p["plan"], d) for p in packs), dtype=torch.uint8,
+                      device=dev)
+    xt = torch.empty((BUDGET, H), dtype=torch.bfloat16, device=dev)
+    xi = torch.empty((BUDGET, H), dtype=torch.bfloat16, device=dev)
+    grads = {s: {k: torch.empty(v.shape, dtype=torch.float32, device=dev) for k, v in weights.blocks[0][s].items()}
+             for s in ("txt", "img")}
+    gstruct = mf.grads_struct(grads["txt"], grads["img"])
+    dc = torch.empty((64, H), dtype=torch.float32, device=dev)
+
+    def step(p):
+        nt, ni = p["x_txt"].shape[0], p["x_img"].shape[0]
+        xt[:nt].copy_(p["x_txt"])
+        xi[:ni].copy_(p["x_img"])
+        mf.mf_block_forward_train(p["plan"], d, bs, None, xt, xi, tws)
+        xt[:p["g_txt"].shape[0]].copy_(p["g_txt"])
+        xi[:ni].copy_(p["g_img"])
+        mf.mf_block_backward(p["plan"], d, bs, tws, xt, xi, gstruct, dc, bws)
+
+    def flops(p):
+        N, S, L2 = p["n_tok"], p["n_seq"], p["sum_L2"]
+        fwd = 24.0 * H * H * N + 4.0 * H * L2 + 2.0 * 2 * 6.0 * H * H * S
+        bwd = 48.0 * H * H * N + 10.0 * H * L2 + 2.0 * 2 * 2 * 6.0 * H * H * S
+        return fwd, bwd
+
+    for i in range(args.warmup):
+        step(packs[i % N_PACKS])
+    torch.cuda.synchronize(dev)
+    mf.mf_check()
+    mf.mf_trace_kinds(None)
+    mf.mf_trace_enable(True)
+    for i in range(N_PACKS):
+        step(packs[i])
+    breakdown = mf.mf_trace_read()
+    mf.mf_trace_enable(False)
+    torch.cuda.synchronize(dev)
+    dom = max((k for k in breakdown if breakdown[k]["flops"] > 0), key=lambda k: breakdown[k]["ms"])
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    sampler = ClockSampler(("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or local_rank)
+    time.sleep(0.3)
+    mf.mf_trace_kinds([dom])
+    mf.mf_trace_enable(True)
+    l0 = mf.mf_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record()
+    tokens, fl_f, fl_b = 0, 0.0, 0.0
+    for i in range(args.steps):
+        p = packs[i % N_PACKS]
+        step(p)
+        tokens += p["n_tok"]
+        f, b = flops(p)
+        fl_f += f
+        fl_b += b
+    e1.record()
+    torch.cuda.synchronize(dev)
+    launches = mf.mf_launch_count() - l0
+    trace = mf.mf_trace_read()
+    mf.mf_trace_enable(False)
+    mf.mf_trace_kinds(None)
+    clocks = sampler.stop()
+    mf.mf_check()
+    if rank != 0:
+        return None
+    el = e0.elapsed_time(e1) / 1e3
+    peaks = read_peaks()
+    tot_ms = sum(e["ms"] for e in breakdown.values())
+    kernels = {}
+    for k, e in breakdown.items():
+        if e["launches"] == 0:
+            continue
+        row = {"launches": e["launches"], "ms_total": round(e["ms"], 3), "share": round(e["ms"] / tot_ms, 4)}
+        if e["flops"] > 0 and e["ms"] > 0:
+            row["tflops"] = round(e["flops"] / (e["ms"] / 1e3) / 1e12, 1)
+        if e["bytes"] > 0 and e["ms"] > 0:
+            row["gbs"] = round(e["bytes"] / (e["ms"] / 1e3) / 1e9, 1)
+        kernels[k] = row
+    de = trace[dom]
+    achieved = de["flops"] / (de["ms"] / 1e3) / 1e12
+    tflops = (fl_f + fl_b) / el / 1e12
+    return {"metric": "packed tokens/s per NR-MMDiT block training step (fwd + bwd, 1xB300)",
+            "value": round(tokens / el, 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic (seeded packs; N(0,1) hidden states and output gradients)",
+            "config": dict(config_dict(dims), workload="native-resolution pack, 16384-token budget, 8 seeded packs, "
+                           "1 NR-MMDiT block: training forward + backward (all weight, input and condition "
+                           "gradients)"),
+            "tflops": round(tflops, 1), "mfu_of_burst": round(tflops / peaks["bf16_tflops"], 4),
+            "flops_note": "fwd 24 H^2 N + 4 H sum L_i^2, bwd 48 H^2 N + 10 H sum L_i^2, + modulation; "
+                          "diagonal attention blocks only",
+            "fwd_flops_share": round(fl_f / (fl_f + fl_b), 4),
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "peak_kind": f"dense bf16 burst ({peaks['source']})", "traffic": None},
+            "gpu_launches": int(launches), "clocks": clocks, "kernels": kernels,
+            "pages_context": "training step 1.9259 s -> 0.7748 s, MFU 33.20 % -> 77.26 % on 8xB200 "
+                             "(PaperReading review, section 3, Table 4; whole model, 50K-token packs)"}
+
+
+def run_attention(args, rank, world, local_rank):
+    """Varlen attention alone on the eight seeded 16K packs (24 heads x 128): the forward with
+    its logsumexp (mf_attention_lse) and the backward (mf_attention_backward), seeded N(0,1)
+    q, k, v and output gradients; CUDA events around each launch, K launches after W warm-up
+    launches per pack cycle.  FLOPs over the sample diagonals only: 4 H sum L_i^2 forward,
+    10 H sum L_i^2 backward (S^T, dP^T, dV, dK, dQ)."""
+    import torch
+    import packed_rectified_flow_packer_b300 as mf
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dims = synth.FULL
+    H, heads, D = dims.hidden, dims.heads, dims.head_dim
+    packs = []
+    for seed in rank_seeds(rank):
+        cands = synth.native_candidates(seed)
+        plan = mf.mf_pack(cands, BUDGET)
+        mf.mf_plan_upload(plan)
+        cu = plan.array("cu_seqlens").astype(np.float64)
+        packs.append({"plan": plan, "n_tok": plan.n_tok, "sum_L2": float((np.diff(cu) ** 2).sum())})
+    gen = torch.Generator(device=dev).manual_seed(77)
+    q, k, v, do = (torch.randn((BUDGET, H), device=dev, generator=gen).to(torch.bfloat16) for _ in range(4))
+    o = torch.empty((BUDGET, H), dtype=torch.bfloat16, device=dev)
+    dq, dk, dv = (torch.empty((BUDGET, H), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    lse = torch.empty((heads, BUDGET), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(mf.mf_attention_backward_workspace_bytes(p["plan"], heads, D) for p in packs),
+                     dtype=torch.uint8, device=dev)
+    out = {}
+    for tag in ("fwd", "bwd"):
+        def call(p):
+            if tag == "fwd":
+                mf.mf_attention_lse(p["plan"], heads, D, q, k, v, o, lse)
+            else:
+                mf.mf_attention_backward(p["plan"], heads, D, q, k, v, o, lse, do, dq, dk, dv, ws)
+        for i in range(max(args.warmup, N_PACKS)):
+            p = packs[i % N_PACKS]
+            mf.mf_attention_lse(p["plan"], heads, D, q, k, v, o, lse)
+            call(p)
+        torch.cuda.synchronize(dev)
+        mf.mf_check()
+        mf.mf_trace_kinds(["attn" if tag == "fwd" else "attn_bwd"])
+        mf.mf_trace_enable(True)
+        fl = 0.0
+        for i in range(args.steps):
+            p = packs[i % N_PACKS]
+            if tag == "bwd":   # the backward reads the lse of the same pack (not bracketed)
+                mf.mf_attention_lse(p["plan"], heads, D, q, k, v, o, lse)
+            call(p)
+            fl += (4.0 if tag == "fwd" else 10.0) * H * p["sum_L2"]
+        tr = mf.mf_trace_read()
+        mf.mf_trace_enable(False)
+        mf.mf_trace_kinds(None)
+        mf.mf_check()
+        e = tr["attn" if tag == "fwd" else "attn_bwd"]
+        out[tag] = {"launches": e["launches"], "ms_avg": round(e["ms"] / e["launches"], 4),
+                    "tflops": round(fl / (e["ms"] / 1e3) / 1e12, 1)}
+    if rank != 0:
+        return None
+    peaks = read_peaks()
+    for tag in out:
+        out[tag]["frac_of_burst"] = round(out[tag]["tflops"] / peaks["bf16_tflops"], 4)
+    return {"metric": "varlen joint attention TFLOP/s, forward and backward (1xB300)", "workload": "attn",
+            "steps": args.steps, "warmup": args.warmup, "fwd": out["fwd"], "bwd": out["bwd"],
+            "config": {"workload": "8 seeded native-resolution 16K packs, 24 heads x 128, diagonal blocks only"},
+            "data": "synthetic (N(0,1) q, k, v, output gradients)", "peaks": peaks}
+
+
 def run_cfg_sampler(args, rank, world, local_rank):
     """4-block stack, two prompts (1024x1024 and 768x1344, 256 text tokens when conditional),
     Euler steps on a uniform grid from t = 1 to 0, guidance w = 4, for 4 steps (the Turbo
@@ -817,6 +1016,10 @@ def main():
         line = run_gemm_shapes(args, rank, world, local_rank)
     elif args.workload == "fp8block":
         line = run_fp8_block(args, rank, world, local_rank)
+    elif args.workload == "train":
+        line = run_train(args, rank, world, local_rank)
+    elif args.workload == "attn":
+        line = run_attention(args, rank, world, local_rank)
     else:
         line = run_mageflow(args, rank, world, local_rank)
     if rank == 0 and line is not None:

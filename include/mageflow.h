@@ -508,9 +508,12 @@ typedef enum {
   MF_K_LATENT = 10,     /* interpolate, packed CFG, Euler step */
   MF_K_LOSS = 11,       /* flow-matching loss reduction */
   MF_K_FP8 = 12,        /* fp8 variant: row quantisation and the E4M3 GEMM */
-  MF_K_ATTN_BWD = 13,   /* attention backward: delta / do gather, the tcgen05 loop, dq to bf16 */
-  MF_K_BLOCK_BWD = 14,  /* block backward's row, reduction, gather and modulation kernels */
-  MF_K_COUNT = 15
+  MF_K_ATTN_BWD = 13,   /* attention backward: the tcgen05 kernel */
+  MF_K_BLOCK_BWD = 14,  /* backward's memory-bound kernels: gate / LN rows, bias sums, delta and
+                           do gather, dq conversion, q / k / v gradient gather, modulation */
+  MF_K_GEMM_DGRAD = 15, /* backward input-gradient GEMMs (dY W) */
+  MF_K_GEMM_WGRAD = 16, /* backward weight-gradient GEMMs (dY^T X) */
+  MF_K_COUNT = 17
 } mf_kernel_kind;
 
 typedef struct {

@@ -96,7 +96,8 @@ class mf_trace_entry(C.Structure):
 
 
 KERNEL_KINDS = ("cond", "ln", "gemm_qkv", "attn", "gemm_oproj", "gemm_up", "gemm_down", "gemm_embed",
-                "gemm_final", "gemm_plain", "latent", "loss", "fp8", "attn_bwd", "block_bwd")
+                "gemm_final", "gemm_plain", "latent", "loss", "fp8", "attn_bwd", "block_bwd",
+                "gemm_dgrad", "gemm_wgrad")
 
 _P = C.c_void_p
 _S = C.c_int   # mf_status

@@ -762,7 +762,7 @@ mf_status attention_backward(const mf_plan* p, int heads, int head_dim, const bf
   float* delta = reinterpret_cast<float*>(ws + L.delta);
   bf16* dj = dout_joint ? nullptr : reinterpret_cast<bf16*>(ws + L.do_joint);
   {
-    Trace tr(MF_K_ATTN_BWD, st, 0, (double)N * H * (2.0 + 2.0 + (dj ? 2.0 : 0.0) + 4.0), 1);
+    Trace tr(MF_K_BLOCK_BWD, st, 0, (double)N * H * (2.0 + 2.0 + (dj ? 2.0 : 0.0) + 4.0), 1);
     MF_CUDA(mf::launch_attention_bwd_prep(o, dout, dout_joint, p->d_joint_srow, N, H, head_dim, dj, delta, acc,
                                           di->sms, st));
   }
@@ -792,7 +792,7 @@ mf_status attention_backward(const mf_plan* p, int heads, int head_dim, const bf
     MF_CUDA(mf::launch_attention_bwd(bp, attn_bwd_ctas(p, heads), st));
   }
   if (dq != nullptr) {
-    Trace tr(MF_K_ATTN_BWD, st, 0, (double)N * H * 6.0, 1);
+    Trace tr(MF_K_BLOCK_BWD, st, 0, (double)N * H * 6.0, 1);
     MF_CUDA(mf::launch_attention_bwd_dq(acc, dq, (long long)N * H, di->sms, st));
   }
   return MF_OK;
@@ -926,7 +926,8 @@ extern "C" mf_status mf_block_backward(const mf_plan* p, const mf_dims* d, const
       sp[n++] = GemmSpec{rows[m], Nn, K, A + (size_t)roff[m] * K, m ? W1 : W0, nullptr, out + (size_t)roff[m] * Nn,
                          Nn, roff[m], m, nullptr, aux ? const_cast<bf16*>(aux) + (size_t)roff[m] * Nn : nullptr};
     }
-    return run_gemm(sp, n, epi, 256, gp, di, st, kind, mf::kMajBMN);
+    (void)kind;
+    return run_gemm(sp, n, epi, 256, gp, di, st, MF_K_GEMM_DGRAD, mf::kMajBMN);
   };
   // weight-gradient GEMM per stream: dW[Mo][Ni] = dY^T X over the stream's rows
   auto wgrad = [&](const bf16* dY, int Mo, const bf16* X, int Nn, float* out0, float* out1, int kind) -> mf_status {
@@ -937,7 +938,8 @@ extern "C" mf_status mf_block_backward(const mf_plan* p, const mf_dims* d, const
       sp[n++] = GemmSpec{Mo, Nn, rows[m], dY + (size_t)roff[m] * Mo, X + (size_t)roff[m] * Nn, nullptr,
                          m ? out1 : out0, Nn, 0, m};
     }
-    return run_gemm(sp, n, mf::kEpiBiasF32, 256, gp, di, st, kind, mf::kMajMNMN);
+    (void)kind;
+    return run_gemm(sp, n, mf::kEpiBiasF32, 256, gp, di, st, MF_K_GEMM_WGRAD, mf::kMajMNMN);
   };
   auto row_kernel = [&](int mode, double bytes_per_row) -> mf_status {
     ra.mode = mode;
