@@ -769,7 +769,7 @@ mf_status attention_backward(const mf_plan* p, int heads, int head_dim, const bf
   mf::AttnBwdParams bp{};
   if (!make_tmap(&bp.tmK, k, H, N, 128) || !make_tmap(&bp.tmV, v, H, N, 128) ||
       !make_tmap(&bp.tmQ, q, H, N, 64) || !make_tmap(&bp.tmDO, dj ? dj : dout, H, N, 64) ||
-      !make_tmap_f32(&bp.tmDQ, acc, H, N, 32, 64))
+      !make_tmap_f32(&bp.tmDQ, acc, H, N, 32, 32))
     return MF_ERR_CUDA;
   bp.cu = p->d_cu;
   bp.items = p->d_items;

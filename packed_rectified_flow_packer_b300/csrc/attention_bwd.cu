@@ -21,20 +21,21 @@
 // lanes), so the key-side accumulators dV, dK stay in TMEM for the whole loop:
 //   S^T  = K Q_i^T                    [128 keys x 64 queries]   (A = K, B = Q_i, both K-major)
 //   P^T  = exp2(S^T log2e/sqrt(D) - lse2_i)  in f32 registers, bf16 copy into TMEM over S^T
+//                                     (each warpgroup's 32 queries over the first 16 of its
+//                                     own 32 columns)
 //   dV  += P^T dO_i                   (A = P^T from TMEM, B = dO_i MN-major)
 //   dP^T = V dO_i^T                   [128 x 64]
-//   dS^T = P^T * (dP^T - delta_i)     bf16, written to shared memory over dO_i (whose readers,
-//                                     dV and dP^T, completed before dP^T was signalled)
+//   dS^T = P^T * (dP^T - delta_i)     bf16, written to one of two shared-memory buffers
 //   dK  += dS^T Q_i                   (A = dS^T K-major, B = Q_i MN-major)
 //   dQ_i^T = K^T dS                   [D x 64]  (A = K MN-major, B = dS^T read MN-major)
-// dQ_i^T lives in one of two TMEM buffers; four warps read it (lane = head dimension), stage
-// it as [64 queries][32 dims] f32 per warp and add it into the f32 dq accumulator with one TMA
-// reduce-add per warp, so nothing waits on that drain but the buffer's reuse two tiles later.
-// Warp roles: 0 TMA producer (K, V once; Q_i, dO_i per tile, plus lse_i and delta_i copied by
-// the warp's lanes), 1 TMEM allocator and MMA issuer (warp-uniform loop, one elected lane
-// issues), 2..5 the P / dS warpgroup (thread = key row), 6..9 the dQ warpgroup.
-// TMEM (512 columns): S^T/P^T @0 (64), dP^T @64 (64), dV @128 (128), dK @256 (128),
-// dQ^T buffers @384 and @448 (64 each).
+// S^T has two TMEM buffers and dP^T is computed one tile ahead, so the tensor core has queued
+// work while the P / dS warps run.  Four warps read dQ_i^T (lane = head dimension), stage it
+// in shared memory and add it into the f32 dq accumulator with TMA reduce-adds.
+// Warp roles (448 threads): 0 TMA producer (K, V once; Q_i, dO_i per tile, plus lse_i and
+// delta_i copied by the warp's lanes), 1 TMEM allocator and MMA issuer (warp-uniform loop, one
+// elected lane issues), 2..5 and 10..13 the two P / dS warpgroups (thread = key row, each
+// warpgroup half of the tile's query columns), 6..9 the dQ warpgroup.
+// TMEM (512 columns): S^T/P^T @0 and @64, dP^T @128, dV @192 (128), dK @320 (128), dQ^T @448.
 // Head dim 64 runs the same code with the head dim padded to 128: the upper half of every K
 // and V tile is zero (so S^T and dP^T are unchanged) and the padded dV / dK / dQ columns are
 // never stored.
@@ -47,31 +48,32 @@ namespace {
 constexpr int kKeys = 128;         // key rows per CTA (TMEM lanes)
 constexpr int kQT = 64;            // query rows per tile
 constexpr int kDP = 128;           // padded head dim inside the kernel
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;     // producer, MMA, 4 dQ warps, 8 P / dS warps
 constexpr int kStages = 3;
 constexpr uint32_t kKVBytes = kKeys * kDP * 2;          // 32 KB: two 16 KB atoms of 128 rows
 constexpr uint32_t kKVAtom = kKeys * 128;               // 16 KB
 constexpr uint32_t kQTBytes = kQT * kDP * 2;            // 16 KB: two 8 KB atoms of 64 rows
 constexpr uint32_t kQTAtom = kQT * 128;                 // 8 KB
 constexpr uint32_t kStageBytes = 2 * kQTBytes + 1024;   // Q_i, dO_i, lse2_i[64], delta_i[64]
+constexpr uint32_t kDSBytes = kKeys * kQT * 2;          // 16 KB: dS^T [128 keys][64 queries]
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kKVBytes;
 constexpr uint32_t kOffStage = 2 * kKVBytes;
-constexpr uint32_t kOffDq = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kDqStage = kQT * 32 * 4;             // 8 KB per dQ warp
+constexpr uint32_t kOffDS = kOffStage + kStages * kStageBytes;
+constexpr uint32_t kOffDq = kOffDS + 2 * kDSBytes;
+constexpr uint32_t kDqStage = 32 * 32 * 4;              // 4 KB per dQ warp: [32 queries][32 dims]
 constexpr uint32_t kSmemTotal = kOffDq + 4 * kDqStage;
 
-constexpr uint32_t kColS = 0, kColDP = 64, kColDV = 128, kColDK = 256, kColDQ = 384;
+// TMEM columns: S^T / P^T double buffer, dP^T, the dV and dK accumulators, dQ^T.
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 192, kColDK = 320, kColDQ = 448;
 
-// 2 (from TMEM) * K operand: D[tmem] (+)= A[tmem] * B[smem]^T, issued by the lane whose pred
-// is non-zero.
-__device__ __forceinline__ void mma_ts_if(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
-      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 
@@ -95,6 +97,13 @@ __device__ __forceinline__ void decode_cta(const AttnBwdParams& p, int& kv0, int
   kb = ((int)blockIdx.x - base) - h * nkb;
 }
 
+// Issue order of the MMA warp, per query tile i (b = i & 1):
+//   [P_i ready]   dP_{i+1} = V dO_{i+1}^T (the P / dS warps load dP_i together with S_i, before
+//                 computing P_i), then dV += P_i^T dO_i
+//   [dS_i ready]  dK += dS_i^T Q_i, [dQ drained] dQ_i^T = K^T dS_i, then S_{i+2} into the S^T
+//                 buffer b that dV just finished reading.
+// So a tile's S^T and dP^T are both in TMEM when the P / dS warps reach it, and the tensor
+// core has the next products queued while the exponentials and dS of a tile run.
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ AttnBwdParams p) {
   constexpr uint32_t IDESC_S = idesc_bf16_f32_mn(kKeys, kQT, false, false);   // S^T, dP^T
   constexpr uint32_t IDESC_KV = idesc_bf16_f32_mn(kKeys, kDP, false, true);   // dV, dK
@@ -102,8 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   constexpr uint32_t TMEM_COLS = 512;
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t kv_full, full[kStages], empty[kStages], s_full, p_full, dp_full, ds_full;
-  __shared__ uint64_t dq_full[2], dq_free[2], done_bar, drain_bar;
+  __shared__ uint64_t kv_full, full[kStages], empty[kStages], s_full[2], p_full[2], dp_full, ds_full;
+  __shared__ uint64_t ds_free[2], dq_full, dq_free, done_bar, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -139,14 +148,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       mbar_init(&full[s], 2);  // the producer's expect-tx arrival + its lse / delta arrival
       mbar_init(&empty[s], 1);
     }
-    mbar_init(&s_full, 1);
-    mbar_init(&p_full, 128);
-    mbar_init(&dp_full, 1);
-    mbar_init(&ds_full, 128);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&dq_full[b], 1);
-      mbar_init(&dq_free[b], 128);
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 256);
+      mbar_init(&ds_free[b], 1);
     }
+    mbar_init(&dp_full, 1);
+    mbar_init(&ds_full, 256);
+    mbar_init(&dq_full, 1);
+    mbar_init(&dq_free, 128);
     mbar_init(&done_bar, 1);
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
@@ -180,11 +190,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     uint32_t armed = 0, armed_par = 0;
     const float* lse_h = p.lse + (size_t)h * p.n_tok + kv0;
     const float* dl_h = p.delta + (size_t)h * p.n_tok + kv0;
+    // lse (log2 units) and delta of tile i's 64 query rows, two per lane, loaded one tile ahead
+    // so their latency overlaps the wait for the stage; rows past the sample get lse = +inf
+    // (so P = 0 there) and delta = 0
+    float nl[2], nd[2];
+    auto load_rows = [&](int i) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = i * kQT + lane + 32 * u;
+        nl[u] = q < len ? __ldg(lse_h + q) * 1.4426950408889634f : INFINITY;
+        nd[u] = q < len ? __ldg(dl_h + q) : 0.0f;
+      }
+    };
+    load_rows(0);
     for (int i = 0; ok && i < n_q; ++i) {
       const int st = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&empty[st], ph ^ 1, lim)) ||
-          __any_sync(0xffffffffu, *(volatile int*)&abort_flag)) {
+      uint32_t okw = 1;
+      if (lane == 0) okw = mbar_wait(&empty[st], ph ^ 1, lim) && !*(volatile int*)&abort_flag ? 1u : 0u;
+      if (__shfl_sync(0xffffffffu, okw, 0) == 0) {
         ok = false;
         break;
       }
@@ -198,16 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       }
       armed |= 1u << st;
       armed_par = (armed_par & ~(1u << st)) | (ph << st);
-      // lse in log2 units and delta of the tile's 64 query rows; rows past the sample get
-      // lse = +inf (so P = 0 there) and delta = 0
       float* l2s = reinterpret_cast<float*>(sp + 2 * kQTBytes);
       float* dls = l2s + kQT;
 #pragma unroll
-      for (int c = lane; c < kQT; c += 32) {
-        const int q = i * kQT + c;
-        l2s[c] = q < len ? __ldg(lse_h + q) * 1.4426950408889634f : INFINITY;
-        dls[c] = q < len ? __ldg(dl_h + q) : 0.0f;
+      for (int u = 0; u < 2; ++u) {
+        l2s[lane + 32 * u] = nl[u];
+        dls[lane + 32 * u] = nd[u];
       }
+      if (i + 1 < n_q) load_rows(i + 1);
       __syncwarp();
       if (el) mbar_arrive(&full[st]);
       __syncwarp();
@@ -225,60 +247,82 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     const uint32_t el = elect_one();
+    // one lane polls (every lane spinning would take issue slots from the P / dS warps on this
+    // scheduler and crowd the barrier unit), then the warp continues together
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, lim));
+      uint32_t okw = 1;
+      if (lane == 0) okw = mbar_wait(bar, parity, lim) ? 1u : 0u;
+      const bool r_ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
+      __syncwarp();
+      return r_ok;
     };
     const uint32_t k_addr = smem_u32(smem + kOffK), v_addr = smem_u32(smem + kOffV);
-    // S^T (or dP^T) = A B^T: A = K (V) K-major [128 rows][128 dims], B = Q_i (dO_i) K-major
+    // K-major operands step 32 bytes per K = 16 (descriptor +2); MN-major ones 16 rows (+128)
+    constexpr uint64_t kStepK = 2, kStepMN = 2048 >> 4;
+    const uint64_t k_desc_mn = sdesc_sw128(k_addr, kKVAtom, 1024);   // K as the MN-major A of dQ^T
+    // S^T (or dP^T) = A B^T: A = K (V) K-major [128 rows][128 dims], B = Q_i (dO_i) K-major;
+    // the two 64-dim halves live in separate atoms
     auto issue_rowdot = [&](uint32_t a_addr, uint32_t b_addr, uint32_t d_col) {
-#pragma unroll
-      for (int kk = 0; kk < kDP / 16; ++kk) {
-        const uint64_t ad = sdesc_sw128(a_addr + (kk >> 2) * kKVAtom + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(b_addr + (kk >> 2) * kQTAtom + (kk & 3) * 32, 16, 1024);
-        mma_bf16_if(el, tmem_base + d_col, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
-      }
+      mma_group_ss<4>(el, tmem_base + d_col, sdesc_sw128(a_addr, 16, 1024), kStepK, sdesc_sw128(b_addr, 16, 1024),
+                      kStepK, IDESC_S, 0u);
+      mma_group_ss<4>(el, tmem_base + d_col, sdesc_sw128(a_addr + kKVAtom, 16, 1024), kStepK,
+                      sdesc_sw128(b_addr + kQTAtom, 16, 1024), kStepK, IDESC_S, 1u);
     };
-    bool ok = wait_all(&kv_full, 0) && wait_all(&full[0], 0);
+    auto stage_wait = [&](int i) { return wait_all(&full[i % kStages], (i / kStages) & 1); };
+    // prologue: S_0, S_1 into both S^T buffers, dP_0
+    bool ok = wait_all(&kv_full, 0) && stage_wait(0);
     if (ok) {
       tc_fence_after();
       issue_rowdot(k_addr, smem_u32(stage_ptr(0)), kColS);
-      mma_commit_if(el, &s_full);
+      mma_commit_if(el, &s_full[0]);
+      issue_rowdot(v_addr, smem_u32(stage_ptr(0)) + kQTBytes, kColDP);
+      mma_commit_if(el, &dp_full);
+      if (n_q > 1) {
+        ok = stage_wait(1);
+        if (ok) {
+          tc_fence_after();
+          issue_rowdot(k_addr, smem_u32(stage_ptr(1)), kColS + kQT);
+          mma_commit_if(el, &s_full[1]);
+        }
+      }
     }
     for (int i = 0; ok && i < n_q; ++i) {
-      const int st = i % kStages;
+      const int st = i % kStages, b = i & 1;
       const uint32_t q_addr = smem_u32(stage_ptr(st));
-      const uint32_t do_addr = q_addr + kQTBytes;   // dO_i, later dS^T
-      // dV += P^T dO_i, then dP^T = V dO_i^T
-      if (!wait_all(&p_full, i & 1)) { ok = false; break; }
+      const uint32_t do_addr = q_addr + kQTBytes;
+      const uint32_t ds_addr = smem_u32(smem + kOffDS + b * kDSBytes);
+      // P_i is in TMEM and the P / dS warps hold dP_i in registers: dP_{i+1} may overwrite
+      // dP_i (its stage was waited for when S_{i+1} was issued), then dV += P_i^T dO_i
+      if (!wait_all(&p_full[b], (i >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kQT / 16; ++kk)
-        mma_ts_if(el, tmem_base + kColDV, tmem_base + kColS + kk * 8,
-                  sdesc_sw128(do_addr + kk * 2048, kQTAtom, 1024), IDESC_KV, (i > 0 || kk > 0) ? 1u : 0u);
-      issue_rowdot(v_addr, do_addr, kColDP);
-      mma_commit_if(el, &dp_full);
-      // S^T of the next tile, while the dS warps work on this one
       if (i + 1 < n_q) {
-        if (!wait_all(&full[(i + 1) % kStages], ((i + 1) / kStages) & 1)) { ok = false; break; }
-        tc_fence_after();
-        issue_rowdot(k_addr, smem_u32(stage_ptr((i + 1) % kStages)), kColS);
-        mma_commit_if(el, &s_full);
+        issue_rowdot(v_addr, smem_u32(stage_ptr((i + 1) % kStages)) + kQTBytes, kColDP);
+        mma_commit_if(el, &dp_full);
       }
-      // dK += dS^T Q_i and dQ_i^T = K^T dS
+      // P^T of queries 0..31 sits in columns 0..15 of the S^T buffer, queries 32..63 in 32..47
+      mma_group2_ts(el, tmem_base + kColDV, tmem_base + kColS + b * kQT, 8, sdesc_sw128(do_addr, kQTAtom, 1024),
+                    kStepMN, IDESC_KV, i > 0 ? 1u : 0u);
+      mma_group2_ts(el, tmem_base + kColDV, tmem_base + kColS + b * kQT + 32, 8,
+                    sdesc_sw128(do_addr + 2 * 2048, kQTAtom, 1024), kStepMN, IDESC_KV, 1u);
+      // dK += dS_i^T Q_i, dQ_i^T = K^T dS_i
       if (!wait_all(&ds_full, i & 1)) { ok = false; break; }
-      const int b = i & 1;
-      if (i >= 2 && !wait_all(&dq_free[b], ((i >> 1) & 1) ^ 1)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kQT / 16; ++kk)
-        mma_bf16_if(el, tmem_base + kColDK, sdesc_sw128(do_addr + kk * 32, 16, 1024),
-                    sdesc_sw128(q_addr + kk * 2048, kQTAtom, 1024), IDESC_KV, (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk)
-        mma_bf16_if(el, tmem_base + kColDQ + b * kQT, sdesc_sw128(k_addr + kk * 2048, kKVAtom, 1024),
-                    sdesc_sw128(do_addr + kk * 2048, kKVAtom, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
-      mma_commit_if(el, &dq_full[b]);
+      mma_group_ss<4>(el, tmem_base + kColDK, sdesc_sw128(ds_addr, 16, 1024), kStepK,
+                      sdesc_sw128(q_addr, kQTAtom, 1024), kStepMN, IDESC_KV, i > 0 ? 1u : 0u);
+      if (i >= 1 && !wait_all(&dq_free, (i - 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      mma_group_ss<8>(el, tmem_base + kColDQ, k_desc_mn, kStepMN, sdesc_sw128(ds_addr, kKVAtom, 1024), kStepMN,
+                      IDESC_DQ, 0u);
+      mma_commit_if(el, &dq_full);
+      mma_commit_if(el, &ds_free[b]);
       mma_commit_if(el, &empty[st]);
+      // S_{i+2} into buffer b (its P_i was read by the dV above)
+      if (i + 2 < n_q) {
+        if (!stage_wait(i + 2)) { ok = false; break; }
+        tc_fence_after();
+        issue_rowdot(k_addr, smem_u32(stage_ptr((i + 2) % kStages)), kColS + b * kQT);
+        mma_commit_if(el, &s_full[b]);
+      }
     }
     if (ok) {
       mma_commit_if(el, &done_bar);
@@ -292,15 +336,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       mbar_wait(&drain_bar, 0, lim);
     }
     __syncwarp();
-  } else if (warp < 6) {
-    // ---------------------------------------------------------------- P / dS warpgroup
+  } else if (warp < 6 || warp >= 10) {
+    // ---------------------------------------------------------------- P / dS warpgroups
+    // Two warpgroups on the same key rows: warps 2..5 take the tile's query columns 0..31,
+    // warps 10..13 columns 32..63.
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;                  // key row inside the block = TMEM lane
+    const int c0 = warp >= 10 ? 32 : 0;            // this warpgroup's query columns c0 .. c0 + 31
     const bool kvalid = kb * kKeys + r < len;
     const uint32_t lane_base = tmem_addr(tmem_base, q4 * 32, 0);
     const float c = p.scale_log2;
     bool ok = true;
+    // a barrier that has completed is seen by one try_wait of every lane; otherwise one lane
+    // polls and the warp continues together
     auto poll = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (__all_sync(0xffffffffu, mbar_try_wait(smem_u32(bar), parity))) return true;
       uint32_t okw = 1;
       if (lane == 0) okw = mbar_wait(bar, parity, lim) ? 1u : 0u;
       const bool r_ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
@@ -308,80 +358,75 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       return r_ok;
     };
     for (int i = 0; i < n_q; ++i) {
+      const int b = i & 1;
       uint8_t* sp = stage_ptr(i % kStages);
       const float* l2s = reinterpret_cast<const float*>(sp + 2 * kQTBytes);
       const float* dls = l2s + kQT;
       // the producer's lse / delta writes are acquired from the stage's own barrier (complete
-      // already: S^T of this tile was computed from the same stage)
-      if (!(ok = poll(&full[i % kStages], (i / kStages) & 1) && poll(&s_full, i & 1))) break;
+      // already: S^T of this tile was computed from the same stage); S_i and dP_i are both in
+      // TMEM by now (dP_i was issued one tile ahead) and are read together
+      if (!(ok = poll(&full[i % kStages], (i / kStages) & 1) && poll(&s_full[b], (i >> 1) & 1) &&
+                 poll(&dp_full, i & 1)))
+        break;
       tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(lane_base + kColS, sr[0]);
-      tmem_ld32(lane_base + kColS + 32, sr[1]);
+      uint32_t sr[32], dr[32];
+      tmem_ld32(lane_base + kColS + b * kQT + c0, sr);
+      tmem_ld32(lane_base + kColDP + c0, dr);
       tmem_ld_wait();
-      tmem_reg_fence(sr[0]);
-      tmem_reg_fence(sr[1]);
-      float pv[kQT];
+      tmem_reg_fence(sr);
+      tmem_reg_fence(dr);
+      float pv[32];
 #pragma unroll
-      for (int j = 0; j < kQT; j += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(l2s + j);
-        pv[j + 0] = ex2_approx(fmaf(__uint_as_float(sr[j >> 5][(j + 0) & 31]), c, -l4.x));
-        pv[j + 1] = ex2_approx(fmaf(__uint_as_float(sr[j >> 5][(j + 1) & 31]), c, -l4.y));
-        pv[j + 2] = ex2_approx(fmaf(__uint_as_float(sr[j >> 5][(j + 2) & 31]), c, -l4.z));
-        pv[j + 3] = ex2_approx(fmaf(__uint_as_float(sr[j >> 5][(j + 3) & 31]), c, -l4.w));
+      for (int j = 0; j < 32; j += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(l2s + c0 + j);
+        pv[j + 0] = ex2_approx(fmaf(__uint_as_float(sr[j + 0]), c, -l4.x));
+        pv[j + 1] = ex2_approx(fmaf(__uint_as_float(sr[j + 1]), c, -l4.y));
+        pv[j + 2] = ex2_approx(fmaf(__uint_as_float(sr[j + 2]), c, -l4.z));
+        pv[j + 3] = ex2_approx(fmaf(__uint_as_float(sr[j + 3]), c, -l4.w));
       }
       if (!kvalid) {
 #pragma unroll
-        for (int j = 0; j < kQT; ++j) pv[j] = 0.0f;
+        for (int j = 0; j < 32; ++j) pv[j] = 0.0f;
       }
-      uint32_t pk[32];
+      uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(pv[2 * j], pv[2 * j + 1]);
-      tmem_st32(lane_base + kColS, pk);  // P^T in bf16, two queries per column
+      for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(pv[2 * j], pv[2 * j + 1]);
+      // P^T in bf16, two queries per column, over the first half of the S^T columns this
+      // warpgroup read itself (the other warpgroup may still be reading its own)
+      tmem_st16(lane_base + kColS + b * kQT + c0, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full);
+      mbar_arrive(&p_full[b]);  // also releases the dP^T columns (read above)
 
-      if (!(ok = poll(&dp_full, i & 1))) break;
-      tc_fence_after();
-      // dS^T row r over this tile's queries, bf16, into the dO_i buffer (128-byte swizzle,
+      if (i >= 2 && !(ok = poll(&ds_free[b], ((i >> 1) & 1) ^ 1))) break;
+      // dS^T row r over this warpgroup's queries, bf16, into dS buffer b (128-byte swizzle:
       // K-major for dK += dS^T Q_i, read MN-major by dQ^T = K^T dS)
-      uint8_t* ds_row = sp + kQTBytes + r * 128;
+      uint8_t* ds_row = smem + kOffDS + b * kDSBytes + r * 128;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t dr[32];
-        tmem_ld32(lane_base + kColDP + half * 32, dr);
-        tmem_ld_wait();
-        tmem_reg_fence(dr);
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const int j0 = half * 32 + ch * 8;
-          const float4 d0 = *reinterpret_cast<const float4*>(dls + j0);
-          const float4 d1 = *reinterpret_cast<const float4*>(dls + j0 + 4);
-          uint4 w;
-          w.x = pack_bf16x2(pv[j0 + 0] * (__uint_as_float(dr[ch * 8 + 0]) - d0.x),
-                            pv[j0 + 1] * (__uint_as_float(dr[ch * 8 + 1]) - d0.y));
-          w.y = pack_bf16x2(pv[j0 + 2] * (__uint_as_float(dr[ch * 8 + 2]) - d0.z),
-                            pv[j0 + 3] * (__uint_as_float(dr[ch * 8 + 3]) - d0.w));
-          w.z = pack_bf16x2(pv[j0 + 4] * (__uint_as_float(dr[ch * 8 + 4]) - d1.x),
-                            pv[j0 + 5] * (__uint_as_float(dr[ch * 8 + 5]) - d1.y));
-          w.w = pack_bf16x2(pv[j0 + 6] * (__uint_as_float(dr[ch * 8 + 6]) - d1.z),
-                            pv[j0 + 7] * (__uint_as_float(dr[ch * 8 + 7]) - d1.w));
-          const int chunk = half * 4 + ch;
-          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) = w;
-        }
+      for (int ch = 0; ch < 4; ++ch) {
+        const int j0 = ch * 8;
+        const float4 d0 = *reinterpret_cast<const float4*>(dls + c0 + j0);
+        const float4 d1 = *reinterpret_cast<const float4*>(dls + c0 + j0 + 4);
+        const uint32_t* dp = &dr[j0];
+        uint4 w;
+        w.x = pack_bf16x2(pv[j0 + 0] * (__uint_as_float(dp[0]) - d0.x), pv[j0 + 1] * (__uint_as_float(dp[1]) - d0.y));
+        w.y = pack_bf16x2(pv[j0 + 2] * (__uint_as_float(dp[2]) - d0.z), pv[j0 + 3] * (__uint_as_float(dp[3]) - d0.w));
+        w.z = pack_bf16x2(pv[j0 + 4] * (__uint_as_float(dp[4]) - d1.x), pv[j0 + 5] * (__uint_as_float(dp[5]) - d1.y));
+        w.w = pack_bf16x2(pv[j0 + 6] * (__uint_as_float(dp[6]) - d1.z), pv[j0 + 7] * (__uint_as_float(dp[7]) - d1.w));
+        const int chunk = c0 / 8 + ch;
+        *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) = w;
       }
       fence_proxy_async_smem();
-      tc_fence_before();
       mbar_arrive(&ds_full);
     }
     if (ok) ok = poll(&done_bar, 0);
     if (ok) {
       tc_fence_after();
-      // dV and dK (scaled by 1 / sqrt(D)) of this thread's key row, real head dims only
+      // dV (first warpgroup) or dK (second, scaled by 1 / sqrt(D)) of this thread's key row,
+      // real head dims only
       const int key = k0 + r;
-#pragma unroll 1
-      for (int part = 0; part < 2; ++part) {
+      {
+        const int part = c0 ? 1 : 0;
         const uint32_t col = part ? kColDK : kColDV;
         const float sc = part ? p.scale : 1.0f;
         bf16* dst = (part ? p.dk : p.dv) + (size_t)key * p.H + h * Dr;
@@ -411,40 +456,45 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     }
   } else {
     // ---------------------------------------------------------------- dQ warpgroup
-    const int q4 = warp & 3;                      // TMEM lanes = head dims q4*32 .. +31
+    // Lane = head dim d (TMEM lane).  The tile's 64 queries leave in two halves: a warp stages
+    // [32 queries][32 dims] f32 and one lane adds the box into the f32 accumulator with a TMA
+    // reduce; rows past the sample hold exact zeros (and rows past the pack are clipped).
+    const int q4 = warp & 3;
     const uint32_t lane_base = tmem_addr(tmem_base, q4 * 32, 0);
     const bool real = q4 * 32 < Dr;
-    float* stg = reinterpret_cast<float*>(smem + kOffDq + (warp - 6) * kDqStage);  // [64 q][32 dims]
+    float* stg = reinterpret_cast<float*>(smem + kOffDq + (warp - 6) * kDqStage);
     const uint32_t el = elect_one();
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
-      const int b = i & 1;
       uint32_t okw = 1;
-      if (lane == 0) okw = mbar_wait(&dq_full[b], (i >> 1) & 1, lim) ? 1u : 0u;
+      if (lane == 0) okw = mbar_wait(&dq_full, i & 1, lim) ? 1u : 0u;
       ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
       uint32_t v[2][32];
-      tmem_ld32(lane_base + kColDQ + b * kQT, v[0]);
-      tmem_ld32(lane_base + kColDQ + b * kQT + 32, v[1]);
+      tmem_ld32(lane_base + kColDQ, v[0]);
+      tmem_ld32(lane_base + kColDQ + 32, v[1]);
       tmem_ld_wait();
       tmem_reg_fence(v[0]);
       tmem_reg_fence(v[1]);
       tc_fence_before();
-      mbar_arrive(&dq_free[b]);
+      mbar_arrive(&dq_free);
       if (real) {
-        if (el) tma_store_wait_read();  // the previous tile's reduce has read the staging rows
-        __syncwarp();
 #pragma unroll
-        for (int j = 0; j < kQT; ++j) stg[j * 32 + lane] = __uint_as_float(v[j >> 5][j & 31]) * p.scale;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (el) {
-          tma_reduce_add_2d(&p.tmDQ, h * Dr + q4 * 32, kv0 + i * kQT, stg);
-          tma_store_commit();
+        for (int half = 0; half < 2; ++half) {
+          if (el) tma_store_wait_read();  // the previous box has been read from the staging rows
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) stg[j * 32 + lane] = __uint_as_float(v[half][j]) * p.scale;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (el) {
+            tma_reduce_add_2d(&p.tmDQ, h * Dr + q4 * 32, kv0 + i * kQT + half * 32, stg);
+            tma_store_commit();
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
     if (el) tma_store_wait_all();

@@ -8,7 +8,7 @@ namespace mf {
 struct AttnBwdParams {
   CUtensorMap tmK, tmV;       // [N][H] bf16 joint order, box {64, 128}, 128-byte swizzle
   CUtensorMap tmQ, tmDO;      // [N][H] bf16 joint order, box {64, 64}, 128-byte swizzle
-  CUtensorMap tmDQ;           // dq accumulator [N][H] f32, box {32, 64}, no swizzle
+  CUtensorMap tmDQ;           // dq accumulator [N][H] f32, box {32, 32}, no swizzle
   const int* cu;              // [S+1] joint offsets
   const int* items;           // work list (sequence, 256-row query block), longest first
   int n_items;

@@ -379,6 +379,50 @@ __device__ __forceinline__ void mma_commit_pair_mc_if(uint32_t pred, uint64_t* b
       : "memory");
 }
 
+// ------------------------------------------------------------------ MMA groups
+// A run of `n` kind::f16 MMAs into one accumulator along K, issued from one asm block by the
+// lane whose pred is non-zero: step j uses descriptors a_desc + j * a_step and b_desc +
+// j * b_step (the 14-bit address fields never carry: shared memory is below 256 KB), and the
+// first step accumulates iff `accumulate`.  Cheaper to issue than n separate calls, which
+// each rebuild both 64-bit descriptors and the predicates.
+template <int n>
+__device__ __forceinline__ void mma_group_ss(uint32_t pred, uint32_t d_tmem, uint64_t a_desc, uint64_t a_step,
+                                             uint64_t b_desc, uint64_t b_step, uint32_t idesc, uint32_t accumulate) {
+  static_assert(n == 4 || n == 8, "4 or 8 steps");
+  if constexpr (n == 4) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 q, %7, 0;\n\t"
+        "mov.b64 a, %1;\n\tmov.b64 b, %3;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n\t"
+        "add.s64 a, a, %2;\n\tadd.s64 b, b, %4;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, 1;\n\t"
+        "add.s64 a, a, %2;\n\tadd.s64 b, b, %4;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, 1;\n\t"
+        "add.s64 a, a, %2;\n\tadd.s64 b, b, %4;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, 1;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(a_step), "l"(b_desc), "l"(b_step), "r"(idesc), "r"(accumulate), "r"(pred)
+        : "memory");
+  } else {
+    mma_group_ss<4>(pred, d_tmem, a_desc, a_step, b_desc, b_step, idesc, accumulate);
+    mma_group_ss<4>(pred, d_tmem, a_desc + 4 * a_step, a_step, b_desc + 4 * b_step, b_step, idesc, 1u);
+  }
+}
+
+// Two MMAs with A read from TMEM (columns a_tmem, a_tmem + a_step), as mma_group4_ts.
+__device__ __forceinline__ void mma_group2_ts(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem, uint32_t a_step,
+                                              uint64_t b_desc, uint64_t b_step, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 q, %7, 0;\n\t"
+      "mov.b32 a, %1;\n\tmov.b64 b, %3;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, p;\n\t"
+      "add.u32 a, a, %2;\n\tadd.s64 b, b, %4;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %5, 1;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(a_step), "l"(b_desc), "l"(b_step), "r"(idesc), "r"(accumulate), "r"(pred)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ math / packing
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -1,4 +1,4 @@
-"""The allocation-free flow loss, mf_flow_loss_noalloc, against mf_flow_loss.
+"""The allocation-free flow loss, mf_flow_loss_noalloc, against mf_flow_loss and the oracle.
 
 mf_flow_loss_noalloc is for callers that cannot allocate device memory where they compute
 the loss: their allocator belongs to another framework that forbids side allocations, their
@@ -6,12 +6,14 @@ memory budget is fixed up front, or an allocation there would synchronise the de
 wrong moment.  It keeps its per-row scratch in a fixed array inside the library instead of
 taking a workspace.  These tests call it through the C ABI several times in a row, on packs of
 different sizes (so rows left by an earlier call would show up if they leaked), and compare
-every result with mf_flow_loss on the same inputs.  The file runs last in the suite and also
-passes on its own in a fresh process."""
+every result with mf_flow_loss on the same inputs and with the oracle's per-sample sums.  The
+file runs last in the suite and also passes on its own in a fresh process."""
 import numpy as np
 import pytest
 
 import synth
+from oracle import model as M
+from oracle import pack as opack
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -54,8 +56,9 @@ def test_noalloc_loss_matches_workspace_loss_on_consecutive_calls():
     big = [synth.Sample(40, 2, 30, 41, 0.3), synth.Sample(7, 1, 50, 33, 0.8),
            synth.Sample(0, 1, 61, 64, 0.5)]
     small = [synth.Sample(5, 1, 3, 4, 0.3), synth.Sample(3, 2, 2, 5, 0.7)]
-    cases = [(_plan(big), 128, 1), (_plan(small), 64, 2), (_plan(big), 128, 3)]
-    for plan, C, seed in cases:
+    cases = [(big, 128, 1), (small, 64, 2), (big, 128, 3)]
+    for samples, C, seed in cases:
+        plan = _plan(samples)
         z, e, v = _inputs(plan.n_img, C, seed)
         ref = _with_workspace(plan, C, z, e, v)
         got = _without_workspace(plan, C, z, e, v)
@@ -63,6 +66,18 @@ def test_noalloc_loss_matches_workspace_loss_on_consecutive_calls():
         np.testing.assert_allclose(got[0].cpu().numpy(), ref[0].cpu().numpy(), rtol=1e-12)
         np.testing.assert_array_equal(got[1].cpu().numpy(), ref[1].cpu().numpy())
         np.testing.assert_allclose(got[2].cpu().numpy(), ref[2].cpu().numpy(), rtol=1e-12)
+        # and the oracle: per-sample sums over target-frame elements, counts, the mean
+        op = opack.build_plan(samples, sum(s.length for s in samples))
+        zh, eh, vh = (x.double().cpu().numpy() for x in (z, e, v))
+        sums, counts = [], []
+        for k, c in enumerate(op.order):
+            a, b = op.cu_img[k], op.cu_img[k + 1]
+            sm, n = M.flow_loss(vh[a:b], zh[a:b], eh[a:b], M.target_mask(samples[c]))
+            sums.append(sm)
+            counts.append(n)
+        np.testing.assert_allclose(got[0].cpu().numpy(), sums, rtol=1e-12)
+        np.testing.assert_array_equal(got[1].cpu().numpy(), counts)
+        assert abs(got[2].item() - M.mean_loss(sums, counts)) <= 1e-12 * abs(got[2].item())
 
 
 def test_noalloc_rejects_packs_beyond_its_scratch():
