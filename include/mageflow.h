@@ -61,7 +61,9 @@ typedef enum {
   MF_ERR_DEVICE_TIMEOUT = 6,   /* a bounded wait inside a kernel ran out (see mf_check) */
   MF_ERR_UNSUPPORTED = 7,      /* dims outside what the kernels implement */
   MF_ERR_NOT_UPLOADED = 8,     /* the plan has no device copy (call mf_plan_upload) */
-  MF_ERR_WORKSPACE = 9         /* workspace smaller than the *_workspace_bytes() figure */
+  MF_ERR_WORKSPACE = 9,        /* workspace smaller than the *_workspace_bytes() figure */
+  MF_ERR_DEVICE_BOUNDS = 10    /* checked build only: a kernel met a plan index out of range
+                                  (see mf_check) */
 } mf_status;
 
 /* Human-readable name of a status; never NULL. */
@@ -480,7 +482,13 @@ mf_status mf_gemm(int32_t M, int32_t N, int32_t K, const void* d_a, const void* 
 
 /* Synchronises `stream`, then returns and clears the device status word of the current
  * device: MF_OK, or MF_ERR_DEVICE_TIMEOUT if a bounded wait ran out since the last check;
- * MF_ERR_CUDA if the synchronisation itself failed. */
+ * MF_ERR_CUDA if the synchronisation itself failed.
+ * The checked build (libmageflow_checked.so, compiled with -DMF_CHECKED; same ABI) also
+ * checks, inside the kernels, every plan-derived index it reads (sample ids against S, joint
+ * and stream-sorted rows against N, cu_seqlens bounds, CFG partner rows, backward row
+ * chunks): a failing check skips the access, sets a flag, and mf_check then returns
+ * MF_ERR_DEVICE_BOUNDS (before MF_ERR_DEVICE_TIMEOUT).  It never traps.  The default build
+ * compiles these checks out. */
 mf_status mf_check(void* stream);
 
 /* Self-test of the bounded-wait path: launches one tiny kernel that waits on a barrier no

@@ -15,11 +15,15 @@ import numpy as np
 
 __all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_block_train_workspace_bytes", "mf_block_forward_train", "mf_block_backward_workspace_bytes", "mf_block_backward", "grads_struct", "mf_stream_grads", "mf_block_grads", "GRAD_FIELDS", "mf_block_fp8_workspace_bytes", "mf_block_forward_fp8", "block_struct_fp8", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_attention_lse", "mf_attention_backward_workspace_bytes", "mf_attention_backward", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmageflow.so")
+# MAGEFLOW_LIB=checked selects the bounds-checked build (same ABI; see mf_check)
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "libmageflow_checked.so" if os.environ.get("MAGEFLOW_LIB") == "checked"
+                        else "libmageflow.so")
 
 STATUS = {0: "MF_OK", 1: "MF_ERR_INVALID_ARG", 2: "MF_ERR_SAMPLE_TOO_LONG", 3: "MF_ERR_BUDGET",
           4: "MF_ERR_ALIGNMENT", 5: "MF_ERR_CUDA", 6: "MF_ERR_DEVICE_TIMEOUT",
-          7: "MF_ERR_UNSUPPORTED", 8: "MF_ERR_NOT_UPLOADED", 9: "MF_ERR_WORKSPACE"}
+          7: "MF_ERR_UNSUPPORTED", 8: "MF_ERR_NOT_UPLOADED", 9: "MF_ERR_WORKSPACE",
+          10: "MF_ERR_DEVICE_BOUNDS"}
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 

@@ -18,6 +18,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmageflow.so")
+# the bounds-checked variant (-DMF_CHECKED): same sources and ABI, kernels check every
+# plan-derived index they read
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libmageflow_checked.so")
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 
@@ -38,37 +42,39 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src, force):
-    obj = os.path.join(BUILD, src + ".o")
+def _compile(src, force, checked=False):
+    obj = os.path.join(BUILD_CHECKED if checked else BUILD, src + ".o")
     if not force and not _stale(obj, _deps(src)):
         return obj, None
-    cmd = [NVCC] + ARCH + COMMON + ["-c", os.path.join(CSRC, src), "-o", obj]
+    flags = COMMON + (["-DMF_CHECKED"] if checked else [])
+    cmd = [NVCC] + ARCH + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
     if src.endswith(".cpp"):
-        cmd = [NVCC] + COMMON + ["-x", "c++", "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [NVCC] + flags + ["-x", "c++", "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         return obj, f"{' '.join(cmd)}\n{r.stdout}\n{r.stderr}"
     return obj, None
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    lib = LIB_CHECKED if checked else LIB
+    os.makedirs(BUILD_CHECKED if checked else BUILD, exist_ok=True)
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(lambda s: _compile(s, force), SOURCES))
+        results = list(ex.map(lambda s: _compile(s, force, checked), SOURCES))
     errors = [e for _, e in results if e]
     if errors:
         raise RuntimeError("libmageflow build failed:\n" + "\n".join(errors))
     objs = [o for o, _ in results]
-    if force or _stale(LIB, objs):
-        cmd = [NVCC] + ARCH + ["-shared", "-cudart", "shared", "-o", LIB] + objs + [
+    if force or _stale(lib, objs):
+        cmd = [NVCC] + ARCH + ["-shared", "-cudart", "shared", "-o", lib] + objs + [
             "-Xlinker", "-rpath=" + os.path.join(CUDA_HOME, "lib64")]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"libmageflow link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
     if verbose:
-        print(LIB)
-    return LIB
+        print(lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True)
+    build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv)

@@ -590,7 +590,7 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
 
   // 2. a = LN(x)(1 + scale1) + shift1, stream-sorted
   if (train) MF_TRY(copy_x(x0));
-  mf::LnModArgs ln{xt, xi, Nt, N, H, p->d_srow_seq, mod, 12LL * H, 6LL * H, 0, H, a1};
+  mf::LnModArgs ln{xt, xi, Nt, N, H, p->d_srow_seq, mod, 12LL * H, 6LL * H, 0, H, a1, S};
   {
     Trace tr(MF_K_LN, st, 0, 4.0 * N * H, 1);
     MF_CUDA(mf::launch_ln_modulate(ln, st));
@@ -605,6 +605,8 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
   gp.mod = mod;
   gp.H = H;
   gp.head_dim = D;
+  gp.n_tok = N;
+  gp.n_seq = S;
   gp.q = q;
   gp.k = k;
   gp.v = v;
@@ -640,6 +642,7 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
     ap.heads = d->heads;
     ap.n_items = p->n_items;
     ap.n_tok = N;
+    ap.n_seq = S;
     ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     ap.status = di->status;
     ap.wait_limit_ns = wait_limit_ns();
@@ -779,6 +782,7 @@ mf_status attention_backward(const mf_plan* p, int heads, int head_dim, const bf
   bp.dk = dk;
   bp.dv = dv;
   bp.n_tok = N;
+  bp.n_seq = p->S;
   bp.H = H;
   bp.heads = heads;
   bp.head_dim = head_dim;
@@ -915,6 +919,8 @@ extern "C" mf_status mf_block_backward(const mf_plan* p, const mf_dims* d, const
   ra.g_second = gx_i;
   ra.mod = mod;
   ra.dmod = dmod;
+  ra.n_rows = N;
+  ra.n_seq = S;
   mf::GemmParams gp{};
   // input-gradient GEMM per stream: out[rows][N] = A[rows][K] W, W stored [K][N]
   auto dgrad = [&](const bf16* A, int K, int Nn, const void* W0, const void* W1, bf16* out, int epi,
@@ -1079,7 +1085,7 @@ extern "C" mf_status mf_final(const mf_plan* p, const mf_dims* d, const mf_temb_
                             2 * H, fmod, 2 * H, 0, 0, st));
   }
   mf::LnModArgs ln{static_cast<const bf16*>(d_x_img), nullptr, p->Ni, p->Ni, H,
-                   p->d_srow_seq + p->Nt, fmod, 2LL * H, 0, 0, H, a};
+                   p->d_srow_seq + p->Nt, fmod, 2LL * H, 0, 0, H, a, p->S};
   {
     Trace tr(MF_K_LN, st, 0, 4.0 * p->Ni * H, 1);
     MF_CUDA(mf::launch_ln_modulate(ln, st));
@@ -1218,6 +1224,7 @@ extern "C" mf_status mf_attention(const mf_plan* p, int32_t heads, int32_t head_
   ap.heads = heads;
   ap.n_items = p->n_items;
   ap.n_tok = p->N;
+  ap.n_seq = p->S;
   ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
   ap.status = di->status;
   ap.wait_limit_ns = wait_limit_ns();
@@ -1248,6 +1255,7 @@ extern "C" mf_status mf_attention_lse(const mf_plan* p, int32_t heads, int32_t h
   ap.heads = heads;
   ap.n_items = p->n_items;
   ap.n_tok = p->N;
+  ap.n_seq = p->S;
   ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
   ap.status = di->status;
   ap.wait_limit_ns = wait_limit_ns();
@@ -1336,12 +1344,17 @@ extern "C" mf_status mf_check(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MF_ERR_CUDA;
   unsigned v = 0;
   if (cudaMemcpy(&v, di->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MF_ERR_CUDA;
+  // bounds-check flags of the checked build (always 0 otherwise); read and cleared
+  const unsigned bounds = mf::bounds_flag_gemm() | mf::bounds_flag_attention() | mf::bounds_flag_attention_bwd() |
+                          mf::bounds_flag_pointwise() | mf::bounds_flag_block_bwd();
+  if (bounds & 2u) return MF_ERR_CUDA;
   if (v != 0) {
     const unsigned zero = 0;
     if (cudaMemcpy(di->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
       return MF_ERR_CUDA;
-    return MF_ERR_DEVICE_TIMEOUT;
   }
+  if (bounds != 0) return MF_ERR_DEVICE_BOUNDS;
+  if (v != 0) return MF_ERR_DEVICE_TIMEOUT;
   return MF_OK;
 }
 

@@ -125,8 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   int seq = 0, kv0 = 0, len = 0, nqb = 1, base = 0;
   for (int it = 0; it < p.n_items;) {
     seq = __ldg(p.items + 2 * it);
+    if (!MF_IDX_OK(seq >= 0 && seq < p.n_seq)) { len = 0; break; }
     kv0 = __ldg(p.cu + seq);
     len = __ldg(p.cu + seq + 1) - kv0;
+    if (!MF_IDX_OK(len > 0)) break;
     nqb = (len + 2 * kT - 1) / (2 * kT);
     if ((int)blockIdx.x < base + nqb * p.heads) break;
     base += nqb * p.heads;
@@ -134,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   }
   const int h = ((int)blockIdx.x - base) / nqb;
   const int qb = ((int)blockIdx.x - base) - h * nqb;
+  if (!MF_IDX_OK(seq >= 0 && seq < p.n_seq && kv0 >= 0 && len > 0 && kv0 + len <= p.n_tok && h < p.heads))
+    return;  // before any barrier or TMEM allocation: the whole CTA leaves together
   const int q0 = kv0 + qb * 2 * kT;
   const int n_kv = (len + kT - 1) / kT;
   const int n_t = (len - qb * 2 * kT) > kT ? 2 : 1;  // query tiles of this block inside the sample
@@ -390,9 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           for (int r0 = 0; r0 < 32; r0 += kRowsPerStore) {
             const int rr = qw * 32 + r0 + lane / kChunks, ch = lane % kChunks;
             const int qrow = q0 + t * kT + rr;
-            if (qrow < kv0 + len) {
+            const int srow = qrow < kv0 + len ? __ldg(p.joint_srow + qrow) : 0;
+            if (qrow < kv0 + len && MF_IDX_OK(srow >= 0 && srow < p.n_tok)) {
               const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * (D * 2) + ((ch ^ (rr & 7)) << 4));
-              bf16* dst = p.out + (size_t)__ldg(p.joint_srow + qrow) * p.H + h * D;
+              bf16* dst = p.out + (size_t)srow * p.H + h * D;
               reinterpret_cast<uint4*>(dst)[ch] = w;
             }
           }
@@ -432,5 +437,7 @@ cudaError_t launch_attention(const AttnParams& p, int head_dim, cudaStream_t str
   if (head_dim == 64) return launch_d<64>(p, stream);
   return cudaErrorInvalidValue;
 }
+
+MF_BOUNDS_EXPORT(attention)
 
 }  // namespace mf

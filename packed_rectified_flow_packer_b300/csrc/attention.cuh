@@ -14,6 +14,7 @@ struct AttnParams {
   float* lse;                 // [heads][N] natural-log logsumexp of each query row's scaled
                               // scores, or null (not written)
   int n_tok;                  // N
+  int n_seq;                  // S
   int H;
   int heads;
   int n_items;

@@ -86,8 +86,10 @@ __device__ __forceinline__ void decode_cta(const AttnBwdParams& p, int& kv0, int
   int nkb = 1;
   for (int it = 0; it < p.n_items;) {
     const int seq = __ldg(p.items + 2 * it);
+    if (!MF_IDX_OK(seq >= 0 && seq < p.n_seq)) { len = 0; return; }
     kv0 = __ldg(p.cu + seq);
     len = __ldg(p.cu + seq + 1) - kv0;
+    if (!MF_IDX_OK(len > 0)) return;
     nkb = (len + kKeys - 1) / kKeys;
     if ((int)blockIdx.x < base + nkb * p.heads) break;
     base += nkb * p.heads;
@@ -124,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 
   int kv0, len, h, kb;
   decode_cta(p, kv0, len, h, kb);
+  if (!MF_IDX_OK(kv0 >= 0 && len > 0 && kv0 + len <= p.n_tok && h < p.heads)) return;  // before any barrier
   const int k0 = kv0 + kb * kKeys;          // first key row (joint) of this CTA
   const int n_q = (len + kQT - 1) / kQT;    // query tiles of the sample
 
@@ -524,6 +527,7 @@ __global__ void attn_bwd_prep_kernel(const bf16* __restrict__ o, const bf16* __r
   const int cph = head_dim / 8;  // 16-byte chunks per head (8 or 16), a power of two <= 16
   for (int j = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; j < N; j += warps) {
     const int sr = __ldg(joint_srow + j);
+    if (!MF_IDX_OK(sr >= 0 && sr < N)) continue;
     const uint4* orow = reinterpret_cast<const uint4*>(o + (size_t)sr * H);
     const uint4* drow = reinterpret_cast<const uint4*>(dout + (size_t)(dout_joint ? j : sr) * H);
     uint4* jrow = do_joint ? reinterpret_cast<uint4*>(do_joint + (size_t)j * H) : nullptr;
@@ -582,5 +586,7 @@ cudaError_t launch_attention_bwd_dq(const float* acc, bf16* dq, long long n, int
   attn_bwd_dq_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(acc), reinterpret_cast<uint2*>(dq), n4);
   return cudaGetLastError();
 }
+
+MF_BOUNDS_EXPORT(attention_bwd)
 
 }  // namespace mf

@@ -16,7 +16,7 @@ struct AttnBwdParams {
   const float* delta;         // [heads][N] rowsum(do * o)
   bf16* dk;                   // [N][H] joint order
   bf16* dv;                   // [N][H] joint order
-  int n_tok, H, heads, head_dim;
+  int n_tok, n_seq, H, heads, head_dim;
   float scale_log2;           // log2(e) / sqrt(D)
   float scale;                // 1 / sqrt(D)
   unsigned* status;

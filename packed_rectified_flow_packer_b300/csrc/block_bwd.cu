@@ -52,6 +52,9 @@ __global__ void __launch_bounds__(512) row_bwd_kernel(const RowBwdArgs a) {
   float4* stats = reinterpret_cast<float4*>(sm + 2 * H);  // [64] (mean, rstd, mean dn, mean dn n)
   const int* ch = a.chunks + 4 * blockIdx.x;
   const int row0 = __ldg(ch), row1 = __ldg(ch + 1), seq = __ldg(ch + 2), stream = __ldg(ch + 3);
+  if (!MF_IDX_OK(row0 >= 0 && row0 <= row1 && row1 <= a.n_rows && row1 - row0 <= kChunkRows && seq >= 0 &&
+                 seq < a.n_seq && (stream == 0 || stream == 1)))
+    return;  // before the block-wide barriers: the whole CTA leaves together
   const float* modrow = a.mod + ((size_t)seq * 2 + stream) * 6 * (size_t)H;
   float* dmodrow = a.dmod + ((size_t)seq * 2 + stream) * 6 * (size_t)H;
   const int tid = threadIdx.x, nthr = blockDim.x;
@@ -224,6 +227,7 @@ __global__ void qkv_grad_gather_kernel(const float* __restrict__ dq_acc, const b
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
     const int j = __ldg(srow_joint + r);
+    if (!MF_IDX_OK(j >= 0 && j < rows)) continue;
     const float pf = (float)__ldg(pos + 3 * j), pr = (float)__ldg(pos + 3 * j + 1), pc = (float)__ldg(pos + 3 * j + 2);
     bf16* out = dqkv + (size_t)r * 3 * H;
     for (int c = lane * 8; c < H; c += 256) {
@@ -374,5 +378,7 @@ cudaError_t launch_mod_bwd(const float* dmod, const float* c, int S, int H, cons
   mod_dc_kernel<<<g2, 128, 0, st>>>(dmod, S, H, w_mod_txt, w_mod_img, dc);
   return cudaGetLastError();
 }
+
+MF_BOUNDS_EXPORT(block_bwd)
 
 }  // namespace mf

@@ -39,6 +39,7 @@ struct RowBwdArgs {
   bf16* out_bf16;             // kRowGate2, kRowLn2: [rows][H]
   bf16* out_first;            // kRowLn1: text rows of dx
   bf16* out_second;           // kRowLn1: image rows of dx
+  int n_rows, n_seq;          // stream-sorted rows and samples of the pack (bounds of the chunks)
 };
 // H a multiple of 256, at most 4096.
 cudaError_t launch_row_bwd(const RowBwdArgs& a, cudaStream_t st);

@@ -17,6 +17,28 @@ enum : unsigned {
   kStatusTimeout = 1u,  // a bounded wait ran out
 };
 
+// Bounds checks of plan-derived indices (sample ids, joint rows, offsets), compiled in only by
+// the checked build (-DMF_CHECKED, libmageflow_checked.so).  MF_IDX_OK(cond) is `cond` there:
+// a failing check sets this translation unit's flag and the caller skips the access (no trap,
+// no fault); mf_check() reports the flags as MF_ERR_DEVICE_BOUNDS.  Elsewhere it is `true`.
+#ifdef MF_CHECKED
+static __device__ unsigned g_mf_bounds;
+#define MF_IDX_OK(cond) ((cond) || (atomicOr(&g_mf_bounds, 1u), false))
+// Reads and clears this translation unit's flag (host).
+static inline unsigned mf_tu_bounds_flag() {
+  unsigned v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_mf_bounds, sizeof(v)) != cudaSuccess) return 2u;
+  if (v != 0 && cudaMemcpyToSymbol(g_mf_bounds, &z, sizeof(z)) != cudaSuccess) return 2u;
+  return v;
+}
+#define MF_BOUNDS_EXPORT(name) \
+  unsigned bounds_flag_##name() { return mf_tu_bounds_flag(); }
+#else
+#define MF_IDX_OK(cond) true
+#define MF_BOUNDS_EXPORT(name) \
+  unsigned bounds_flag_##name() { return 0u; }
+#endif
+
 // ------------------------------------------------------------------ addresses and timers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

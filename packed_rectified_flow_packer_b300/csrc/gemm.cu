@@ -97,6 +97,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const GemmPr
   } else if constexpr (EPI == kEpiGateResid) {
     const int srow = pr.row_off + row;
     const int seq = __ldg(p.srow_seq + srow);
+    if (!MF_IDX_OK(seq >= 0 && seq < p.n_seq)) return;
     const float4* g = reinterpret_cast<const float4*>(
         p.mod + ((size_t)seq * 2 + pr.stream) * 6 * (size_t)p.H + p.gate_off + col0);
     bf16* x = static_cast<bf16*>(pr.out) + (size_t)row * pr.ldo + col0;
@@ -121,6 +122,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const GemmPr
   } else if constexpr (EPI == kEpiQkvRope) {
     const int srow = pr.row_off + row;
     const int joint = __ldg(p.srow_joint + srow);
+    if (!MF_IDX_OK(joint >= 0 && joint < p.n_tok)) return;
     const int which = col0 / p.H;
     const int cc = col0 - which * p.H;
     bf16* dst = (which == 0 ? p.q : (which == 1 ? p.k : p.v)) + (size_t)joint * p.H + cc;
@@ -251,6 +253,7 @@ __device__ __forceinline__ void epi_row16(const GemmParams& p, const GemmProblem
     }
     if (which < 2) {
       const int joint = __ldg(p.srow_joint + pr.row_off + row);
+      if (!MF_IDX_OK(joint >= 0 && joint < p.n_tok)) return;
       const int* ps = p.pos + (size_t)joint * 3;
       const float pf = (float)__ldg(ps), pr_ = (float)__ldg(ps + 1), pc = (float)__ldg(ps + 2);
       const int g0 = ((col0 - which * p.H) % p.head_dim) >> 1;
@@ -288,6 +291,7 @@ __device__ __forceinline__ void epi_store8(const GemmParams& p, const GemmProble
   bf16* dst;
   if constexpr (E == kEpiQkvRope) {
     const int joint = __ldg(p.srow_joint + pr.row_off + row);
+    if (!MF_IDX_OK(joint >= 0 && joint < p.n_tok)) return;
     const int which = col / p.H;
     dst = (which == 0 ? p.q : (which == 1 ? p.k : p.v)) + (size_t)joint * p.H + (col - which * p.H);
   } else {
@@ -299,6 +303,7 @@ __device__ __forceinline__ void epi_store8(const GemmParams& p, const GemmProble
           make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                      pack_bf16x2(v[6], v[7]));
     const int seq = __ldg(p.srow_seq + pr.row_off + row);
+    if (!MF_IDX_OK(seq >= 0 && seq < p.n_seq)) return;
     const float4* g = reinterpret_cast<const float4*>(
         p.mod + ((size_t)seq * 2 + pr.stream) * 6 * (size_t)p.H + p.gate_off + col);
     const float4 ga = __ldg(g), gb = __ldg(g + 1);
@@ -921,5 +926,7 @@ cudaError_t launch_gemm(const GemmParams& p, int BN, int epi, int num_sms, cudaS
 #undef MF_GEMM_CASE
   return cudaErrorInvalidValue;
 }
+
+MF_BOUNDS_EXPORT(gemm)
 
 }  // namespace mf

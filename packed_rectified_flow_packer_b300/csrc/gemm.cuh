@@ -56,6 +56,7 @@ struct GemmParams {
   const float* mod;       // [S][2][6H] modulation
   int H;
   int head_dim;
+  int n_tok, n_seq;       // pack sizes (bounds of the joint rows and sample ids the epilogues read)
   int gate_off;           // float offset of the gate chunk inside a (sample, stream) mod row
   const bf16* qk_norm[2][2];  // [problem][q, k]: QK-RMSNorm scales [head_dim], or null (off)
   const float* row_scale;     // kEpiF8: dequantisation scale of A's rows (indexed row_off + row)

@@ -66,6 +66,14 @@ constexpr int kRowChunk = 64; // rows of one chunk of the backward's row kernels
 // no device can be queried.
 mf_status current_device(int* dev);
 
+// Bounds-check flags of the checked build, one per translation unit with device code (read and
+// cleared; always 0 in the default build).
+unsigned bounds_flag_gemm();
+unsigned bounds_flag_attention();
+unsigned bounds_flag_attention_bwd();
+unsigned bounds_flag_pointwise();
+unsigned bounds_flag_block_bwd();
+
 // One library launch of `nk` kernels of kind `kind` (mf_kernel_kind): counted always and, while
 // tracing is on (and the stream is not capturing), bracketed by two CUDA events on `st` -
 // the constructor records the first, the destructor the second.

@@ -220,6 +220,7 @@ extern "C" const char* mf_status_str(mf_status s) {
     case MF_ERR_UNSUPPORTED: return "MF_ERR_UNSUPPORTED";
     case MF_ERR_NOT_UPLOADED: return "MF_ERR_NOT_UPLOADED";
     case MF_ERR_WORKSPACE: return "MF_ERR_WORKSPACE";
+    case MF_ERR_DEVICE_BOUNDS: return "MF_ERR_DEVICE_BOUNDS";
   }
   return "MF_ERR_UNKNOWN";
 }

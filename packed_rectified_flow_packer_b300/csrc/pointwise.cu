@@ -185,6 +185,7 @@ __device__ __forceinline__ void ln_row(const LnModArgs& a, int r, int lane, cons
   }
   const float rstd = rsqrtf(warp_sum(q) / (float)H + 1e-6f);
   const int seq = __ldg(a.row_seq + r);
+  if (!MF_IDX_OK(seq >= 0 && seq < a.n_seq)) return;
   const float* mrow = a.mod + (size_t)seq * a.seq_stride + (r >= a.n_first ? a.stream_stride : 0);
   const float4* sh = reinterpret_cast<const float4*>(mrow + a.shift_off);
   const float4* sc = reinterpret_cast<const float4*>(mrow + a.scale_off);
@@ -313,6 +314,7 @@ __global__ void cfg_kernel(const int* __restrict__ img_seq, const int* __restric
       if (out != v) reinterpret_cast<float4*>(out)[i] = reinterpret_cast<const float4*>(v)[i];
     } else if (role == 1) {
       const int u = __ldg(img_pair + r);
+      if (!MF_IDX_OK(u >= 0 && u < Ni)) continue;
       const long long j = (long long)u * c4n + c4;
       const float4 vc = reinterpret_cast<const float4*>(v)[i];
       const float4 vu = reinterpret_cast<const float4*>(v)[j];
@@ -593,5 +595,7 @@ cudaError_t launch_timeout_selftest(unsigned* status, unsigned long long limit_n
   timeout_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
   return cudaGetLastError();
 }
+
+MF_BOUNDS_EXPORT(pointwise)
 
 }  // namespace mf

@@ -43,6 +43,7 @@ struct LnModArgs {
   int shift_off;
   int scale_off;
   bf16* out;
+  int n_seq;        // bound of row_seq's values
 };
 cudaError_t launch_ln_modulate(const LnModArgs& a, cudaStream_t st);
 
