@@ -44,12 +44,13 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=120)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["native16k", "cfg", "gemm", "fp8block", "train", "attn"], default="native16k",
+    ap.add_argument("--workload", choices=["native16k", "cfg", "gemm", "fp8block", "train", "attn", "lnvariants"], default="native16k",
                     help="native16k: the headline block-forward pack; cfg: packed vs unpacked CFG sampler; "
                          "gemm: bf16 and fp8 GEMMs alone at the block's shapes; fp8block: the block "
                          "forward with fp8 projections against the bf16 one on the 16K packs; train: the "
                          "block's training forward + backward on the 16K packs; attn: varlen attention "
-                         "forward and backward alone on the 16K packs")
+                         "forward and backward alone on the 16K packs; lnvariants: the block forward with each LN + "
+                         "modulate variant")
     return ap.parse_args()
 
 
@@ -648,6 +649,95 @@ def run_fp8_block(args, rank, world, local_rank):
             "data": "synthetic (seeded packs; N(0,1) hidden image states instead of the latent embed)"}
 
 
+def run_ln_variants(args, rank, world, local_rank):
+    """The block forward on the eight seeded 16K packs with each LN + modulate variant of
+    mf_block_forward_ex: one warp per row (the default), row groups, and the second LN's
+    statistics fused into the out-projection's epilogue.  Per variant: K block calls timed with
+    CUDA events after W warm-up calls, then one pass over the packs with every launch traced
+    for the LN and out-projection kernel times."""
+    import torch
+    import packed_rectified_flow_packer_b300 as mf
+    from packed_rectified_flow_packer_b300.device import DeviceModel, to_bf16
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dims = synth.FULL
+    H = dims.hidden
+    model = DeviceModel(synth.model_weights(dims, 1, seed=0), device=dev)
+    d = model.dims
+    packs = []
+    for seed in rank_seeds(rank):
+        cands = synth.native_candidates(seed)
+        plan = mf.mf_pack(cands, BUDGET)
+        mf.mf_plan_upload(plan)
+        x, _, _ = synth.pack_inputs(cands, plan.array("order"), dims, seed)
+        xi = torch.randn((plan.n_img, H), device=dev, generator=torch.Generator(device=dev).manual_seed(seed))
+        packs.append({"plan": plan, "x_txt": to_bf16(x, dev), "x_img": xi.to(torch.bfloat16)})
+    ws = torch.empty(max(mf.mf_block_workspace_bytes(p["plan"], d) for p in packs), dtype=torch.uint8, device=dev)
+    xt = torch.empty((BUDGET, H), dtype=torch.bfloat16, device=dev)
+    xi = torch.empty((BUDGET, H), dtype=torch.bfloat16, device=dev)
+    variants = (("warp_rows", 0), ("row_groups", mf.BLOCK_LN_ROW_GROUPS), ("stats_fused", mf.BLOCK_LN_STATS_FUSED))
+    out = {}
+
+    def call(p, flags):
+        nt, ni = p["x_txt"].shape[0], p["x_img"].shape[0]
+        xt[:nt].copy_(p["x_txt"])
+        xi[:ni].copy_(p["x_img"])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mf.mf_block_forward_ex(p["plan"], d, model.block_structs[0], None, xt, xi, ws, flags)
+        e1.record()
+        return e0, e1
+
+    for rep_ in range(2):  # the variants twice, interleaved, so a clock drift shows
+        for tag, flags in variants:
+            for i in range(args.warmup):
+                call(packs[i % N_PACKS], flags)
+            torch.cuda.synchronize(dev)
+            ms, tok = 0.0, 0
+            for i in range(args.steps):
+                p = packs[i % N_PACKS]
+                e0, e1 = call(p, flags)
+                torch.cuda.synchronize(dev)
+                ms += e0.elapsed_time(e1)
+                tok += p["plan"].n_tok
+            mf.mf_trace_kinds(["ln", "gemm_oproj"])
+            mf.mf_trace_enable(True)
+            for i in range(N_PACKS):
+                call(packs[i], flags)
+            tr = mf.mf_trace_read()
+            mf.mf_trace_enable(False)
+            mf.mf_trace_kinds(None)
+            mf.mf_check()
+            ln, op = tr["ln"], tr["gemm_oproj"]
+            out.setdefault(tag, []).append({
+                "ms_per_block": round(ms / args.steps, 4), "tokens_per_s": round(tok / (ms / 1e3), 1),
+                "ln_us_avg": round(1e3 * ln["ms"] / ln["launches"], 2),
+                "ln_gbs": round(ln["bytes"] / (ln["ms"] / 1e3) / 1e9, 1),
+                "oproj_us_avg": round(1e3 * op["ms"] / op["launches"], 2)})
+    # a plain device copy of the same bytes (read [N][H] bf16, write [N][H] bf16) on the same box,
+    # the bandwidth an LN pass could reach
+    n_rows = max(p["plan"].n_tok for p in packs)
+    src = torch.randn((n_rows, H), device=dev).to(torch.bfloat16)
+    dst = torch.empty_like(src)
+    for _ in range(args.warmup):
+        dst.copy_(src)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        dst.copy_(src)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    copy_us = 1e3 * e0.elapsed_time(e1) / args.steps
+    copy = {"rows": n_rows, "us": round(copy_us, 2), "gbs": round(4.0 * n_rows * H / (copy_us / 1e6) / 1e9, 1)}
+    if rank != 0:
+        return None
+    return {"metric": "packed tokens/s per NR-MMDiT block fwd by LN + modulate variant (1xB300)",
+            "workload": "lnvariants", "steps": args.steps, "warmup": args.warmup, "variants": out,
+            "copy_same_bytes": copy,
+            "config": {"workload": "8 seeded native-resolution 16K packs, 1 block, H = 3072"},
+            "data": "synthetic (seeded packs; N(0,1) hidden image states instead of the latent embed)"}
+
+
 def run_train(args, rank, world, local_rank):
     """Training step of one NR-MMDiT block on the eight seeded 16K packs: mf_block_forward_train
     (the forward that keeps what the backward reads), then mf_block_backward with a seeded
@@ -1018,6 +1108,8 @@ def main():
         line = run_fp8_block(args, rank, world, local_rank)
     elif args.workload == "train":
         line = run_train(args, rank, world, local_rank)
+    elif args.workload == "lnvariants":
+        line = run_ln_variants(args, rank, world, local_rank)
     elif args.workload == "attn":
         line = run_attention(args, rank, world, local_rank)
     else:

@@ -206,7 +206,10 @@ size_t mf_block_workspace_bytes(const mf_plan* plan, const mf_dims* dims);
  * [2] a[N_txt+N_img][H] bf16 (last LN+modulate output, stream-sorted),
  * [3] q[N][H], [4] k[N][H], [5] v[N][H] bf16 in joint order (q, k after RoPE),
  * [6] o[N_txt+N_img][H] bf16 attention output, stream-sorted,
- * [7] hidden[N_txt+N_img][rH] bf16 (GELU output), stream-sorted.  n must be >= 8. */
+ * [7] hidden[N_txt+N_img][rH] bf16 (GELU output), stream-sorted,
+ * [8] (written when n >= 9) the LN statistics parts of MF_BLOCK_LN_STATS_FUSED:
+ *     [N_txt+N_img][H/128] pairs of f32 (mean, sum of squared deviations) of each 128-column
+ *     part of the residual after attention.  n must be >= 8. */
 mf_status mf_block_workspace_layout(const mf_plan* plan, const mf_dims* dims, size_t* offsets,
                                     int32_t n);
 
@@ -229,6 +232,29 @@ mf_status mf_block_workspace_layout(const mf_plan* plan, const mf_dims* dims, si
 mf_status mf_block_forward(const mf_plan* plan, const mf_dims* dims, const mf_block_weights* w,
                            const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
                            size_t ws_bytes, void* stream);
+
+/* Variants of the block's LN + modulate (flags of mf_block_forward_ex).
+ *  0 (default)              : one warp per row, statistics from the row held in registers
+ *  MF_BLOCK_LN_ROW_GROUPS   : a row-group kernel: groups of 8 rows staged in shared memory by
+ *                             bulk copies, each thread keeping its 8 columns' shift and scale in
+ *                             registers across the rows of one sample and stream; statistics
+ *                             merged per group with Chan's pairwise update
+ *  MF_BLOCK_LN_STATS_FUSED  : the statistics of the second LN come from the out-projection's
+ *                             epilogue (per 128-column part of each row of the new residual),
+ *                             merged by the row-group kernel; bf16 block only, not with the
+ *                             training forward  [PR 2.2(3): the norm chain fused into the
+ *                             projections]
+ * All compute LN(x) = (x - mean) / sqrt(var + 1e-6) with f32 statistics of the bf16 x; they
+ * differ only in f32 summation order. */
+#define MF_BLOCK_LN_ROW_GROUPS 1
+#define MF_BLOCK_LN_STATS_FUSED 2
+
+/* mf_block_forward with a variant: flags a combination of MF_BLOCK_LN_* (with both, the first
+ * LN runs in row groups and the second takes the fused statistics).  Errors: as
+ * mf_block_forward; MF_ERR_INVALID_ARG for unknown flags. */
+mf_status mf_block_forward_ex(const mf_plan* plan, const mf_dims* dims, const mf_block_weights* w,
+                              const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
+                              size_t ws_bytes, int32_t flags, void* stream);
 
 /* ------------------------------------------------------------------------------------ */
 /* Training: the block forward that keeps what the backward reads, and the block backward  */

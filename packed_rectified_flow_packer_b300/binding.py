@@ -13,7 +13,7 @@ import os
 
 import numpy as np
 
-__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_block_train_workspace_bytes", "mf_block_forward_train", "mf_block_backward_workspace_bytes", "mf_block_backward", "grads_struct", "mf_stream_grads", "mf_block_grads", "GRAD_FIELDS", "mf_block_fp8_workspace_bytes", "mf_block_forward_fp8", "block_struct_fp8", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_attention_lse", "mf_attention_backward_workspace_bytes", "mf_attention_backward", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
+__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_block_forward_ex", "BLOCK_LN_ROW_GROUPS", "BLOCK_LN_STATS_FUSED", "mf_block_train_workspace_bytes", "mf_block_forward_train", "mf_block_backward_workspace_bytes", "mf_block_backward", "grads_struct", "mf_stream_grads", "mf_block_grads", "GRAD_FIELDS", "mf_block_fp8_workspace_bytes", "mf_block_forward_fp8", "block_struct_fp8", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_attention_lse", "mf_attention_backward_workspace_bytes", "mf_attention_backward", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
 
 # MAGEFLOW_LIB=checked selects the bounds-checked build (same ABI; see mf_check)
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
@@ -117,6 +117,8 @@ _sigs = {
     "mf_block_workspace_layout": (_S, [_P, C.POINTER(mf_dims), C.POINTER(C.c_size_t), C.c_int32]),
     "mf_block_forward": (_S, [_P, C.POINTER(mf_dims), C.POINTER(mf_block_weights), _P, _P, _P, _P,
                               C.c_size_t, _P]),
+    "mf_block_forward_ex": (_S, [_P, C.POINTER(mf_dims), C.POINTER(mf_block_weights), _P, _P, _P, _P,
+                                 C.c_size_t, C.c_int32, _P]),
     "mf_block_train_workspace_bytes": (C.c_size_t, [_P, C.POINTER(mf_dims)]),
     "mf_block_forward_train": (_S, [_P, C.POINTER(mf_dims), C.POINTER(mf_block_weights), _P, _P, _P, _P,
                                     C.c_size_t, _P]),
@@ -283,8 +285,8 @@ def mf_block_workspace_bytes(plan: Plan, dims) -> int:
 
 
 def mf_block_workspace_layout(plan: Plan, dims):
-    off = (C.c_size_t * 8)()
-    _ok(lib.mf_block_workspace_layout(plan.handle, C.byref(_dims(dims)), off, 8),
+    off = (C.c_size_t * 9)()
+    _ok(lib.mf_block_workspace_layout(plan.handle, C.byref(_dims(dims)), off, 9),
         "mf_block_workspace_layout")
     return list(off)
 
@@ -294,6 +296,18 @@ def mf_block_forward(plan: Plan, dims, weights: mf_block_weights, t, x_txt, x_im
     nbytes = ws_bytes if ws_bytes is not None else (ws.numel() * ws.element_size() if ws is not None else 0)
     _ok(lib.mf_block_forward(plan.handle, C.byref(_dims(dims)), C.byref(weights), _ptr(t), _ptr(x_txt),
                              _ptr(x_img), _ptr(ws), nbytes, _stream(stream)), "mf_block_forward")
+
+
+# LN + modulate variants of mf_block_forward_ex (the header's MF_BLOCK_LN_*)
+BLOCK_LN_ROW_GROUPS = 1
+BLOCK_LN_STATS_FUSED = 2
+
+
+def mf_block_forward_ex(plan: Plan, dims, weights: mf_block_weights, t, x_txt, x_img, ws, flags, ws_bytes=None,
+                        stream=None):
+    nbytes = ws_bytes if ws_bytes is not None else (ws.numel() * ws.element_size() if ws is not None else 0)
+    _ok(lib.mf_block_forward_ex(plan.handle, C.byref(_dims(dims)), C.byref(weights), _ptr(t), _ptr(x_txt),
+                                _ptr(x_img), _ptr(ws), nbytes, int(flags), _stream(stream)), "mf_block_forward_ex")
 
 
 def mf_block_train_workspace_bytes(plan: Plan, dims) -> int:

@@ -202,7 +202,7 @@ size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ------------------------------------------------------------------ workspace layouts
 struct BlockLayout {
-  size_t off[8];  // c, mod, a, q, k, v, o, hidden
+  size_t off[9];  // c, mod, a, q, k, v, o, hidden, LN statistics parts
   size_t sinus, h1;
   size_t total;
 };
@@ -222,6 +222,7 @@ BlockLayout block_layout(const mf_plan* p, const mf_dims* d) {
   L.off[7] = take(N * R * 2);
   L.sinus = take(S * F * 4);
   L.h1 = take(S * H * 4);
+  L.off[8] = take(N * (H / 128) * 8);
   L.total = o;
   return L;
 }
@@ -498,7 +499,7 @@ extern "C" mf_status mf_block_workspace_layout(const mf_plan* p, const mf_dims* 
   if (p == nullptr || offsets == nullptr || n < 8) return MF_ERR_INVALID_ARG;
   MF_TRY(check_dims(d));
   BlockLayout L = block_layout(p, d);
-  for (int i = 0; i < 8; ++i) offsets[i] = L.off[i];
+  for (int i = 0; i < 8 || (i < 9 && i < n); ++i) offsets[i] = L.off[i];
   return MF_OK;
 }
 
@@ -510,14 +511,21 @@ bool stream8_ok(const mf_stream_weights_fp8& s) {
   return true;
 }
 
+// LN + modulate through the kernel `flags` selects (MF_BLOCK_LN_*; 0 = one warp per row); the
+// row-group kernel also takes the statistics the out-projection's epilogue left (ln.stats).
+cudaError_t launch_ln(const mf::LnModArgs& ln, int flags, cudaStream_t st) {
+  return (flags & MF_BLOCK_LN_ROW_GROUPS || ln.stats != nullptr) ? mf::launch_ln_group(ln, st)
+                                                                 : mf::launch_ln_modulate(ln, st);
+}
+
 // The block forward; with w8 the four projections run on E4M3 operands: each input (a, o, a,
 // hidden) is quantised per row right before its GEMM, into the fp8 region after the bf16
-// workspace.
+// workspace.  `flags` (MF_BLOCK_*) select the LN + modulate variant.
 // With `train`, the workspace has the training layout and the forward also keeps what the
 // backward reads (TrainLayout).
 mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weights* w,
                         const mf_block_weights_fp8* w8, const float* d_t, void* d_x_txt, void* d_x_img,
-                        void* d_ws, size_t ws_bytes, void* stream, bool train = false) {
+                        void* d_ws, size_t ws_bytes, void* stream, bool train = false, int flags = 0) {
   DevInfo* di = nullptr;
   int dev = -1;
   MF_TRY(device_info(&di, &dev));
@@ -526,6 +534,8 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
   if (w == nullptr || !temb_ok(&w->temb) || !stream_ok(w->txt) || !stream_ok(w->img))
     return MF_ERR_INVALID_ARG;
   if (w8 != nullptr && (!stream8_ok(w8->txt) || !stream8_ok(w8->img))) return MF_ERR_INVALID_ARG;
+  if ((flags & ~(MF_BLOCK_LN_ROW_GROUPS | MF_BLOCK_LN_STATS_FUSED)) != 0) return MF_ERR_INVALID_ARG;
+  if (flags & MF_BLOCK_LN_STATS_FUSED && (w8 != nullptr || train)) return MF_ERR_UNSUPPORTED;
   if (p->N == 0) return MF_OK;
   if ((p->Nt > 0 && d_x_txt == nullptr) || (p->Ni > 0 && d_x_img == nullptr) || d_ws == nullptr)
     return MF_ERR_INVALID_ARG;
@@ -551,6 +561,8 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
   bf16* v = reinterpret_cast<bf16*>(ws + L.off[5]);
   bf16* o = reinterpret_cast<bf16*>(ws + L.off[6]);
   bf16* hid = reinterpret_cast<bf16*>(ws + L.off[7]);
+  float2* ln_stats = reinterpret_cast<float2*>(ws + L.off[8]);
+  const int STATS = (flags & MF_BLOCK_LN_STATS_FUSED) ? mf::kEpiStats : 0;
   float* sinus = reinterpret_cast<float*>(ws + L.sinus);
   float* h1 = reinterpret_cast<float*>(ws + L.h1);
   bf16* xt = static_cast<bf16*>(d_x_txt);
@@ -590,10 +602,11 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
 
   // 2. a = LN(x)(1 + scale1) + shift1, stream-sorted
   if (train) MF_TRY(copy_x(x0));
-  mf::LnModArgs ln{xt, xi, Nt, N, H, p->d_srow_seq, mod, 12LL * H, 6LL * H, 0, H, a1, S};
+  mf::LnModArgs ln{xt, xi, Nt, N, H, p->d_srow_seq, mod, 12LL * H, 6LL * H, 0, H, a1, S, nullptr,
+                   di->status, wait_limit_ns()};
   {
     Trace tr(MF_K_LN, st, 0, 4.0 * N * H, 1);
-    MF_CUDA(mf::launch_ln_modulate(ln, st));
+    MF_CUDA(launch_ln(ln, flags, st));
   }
   ln.out = a;
 
@@ -615,6 +628,8 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
   gp.qk_norm[1][0] = static_cast<const bf16*>(w->img.w_qnorm);
   gp.qk_norm[1][1] = static_cast<const bf16*>(w->img.w_knorm);
   gp.row_scale = s8;
+  gp.ln_stats = ln_stats;
+  gp.ln_parts = H / 128;
   if (w8) {
     MF_TRY(quantize(a, H));
     GemmSpec sp[2] = {{Nt, 3 * H, H, q8, w8->txt.q_qkv, w->txt.b_qkv, nullptr, 0, 0, 0, w8->txt.s_qkv},
@@ -661,16 +676,17 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
     GemmSpec sp[2] = {{Nt, H, H, o, w->txt.w_o, w->txt.b_o, xt, H, 0, 0, nullptr, yo},
                       {Ni, H, H, o + (size_t)Nt * H, w->img.w_o, w->img.b_o, xi, H, Nt, 1, nullptr,
                        yo ? yo + (size_t)Nt * H : nullptr}};
-    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid | SAVE, 256, gp, di, st, MF_K_GEMM_OPROJ));
+    MF_TRY(run_gemm(sp, 2, mf::kEpiGateResid | SAVE | STATS, 256, gp, di, st, MF_K_GEMM_OPROJ));
   }
   if (train) MF_TRY(copy_x(x1));
 
-  // 6. a = LN(x)(1 + scale2) + shift2
+  // 6. a = LN(x)(1 + scale2) + shift2 (statistics from the out-projection's epilogue when fused)
   ln.shift_off = 3 * H;
   ln.scale_off = 4 * H;
+  if (STATS) ln.stats = ln_stats;
   {
     Trace tr(MF_K_LN, st, 0, 4.0 * N * H, 1);
-    MF_CUDA(mf::launch_ln_modulate(ln, st));
+    MF_CUDA(launch_ln(ln, flags, st));
   }
 
   // 7. hidden = GELU(a W_1^T + b_1)
@@ -708,6 +724,12 @@ extern "C" mf_status mf_block_forward(const mf_plan* p, const mf_dims* d, const 
                                       const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
                                       size_t ws_bytes, void* stream) {
   return block_forward(p, d, w, nullptr, d_t, d_x_txt, d_x_img, d_ws, ws_bytes, stream);
+}
+
+extern "C" mf_status mf_block_forward_ex(const mf_plan* p, const mf_dims* d, const mf_block_weights* w,
+                                         const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,
+                                         size_t ws_bytes, int32_t flags, void* stream) {
+  return block_forward(p, d, w, nullptr, d_t, d_x_txt, d_x_img, d_ws, ws_bytes, stream, false, flags);
 }
 
 extern "C" size_t mf_block_train_workspace_bytes(const mf_plan* p, const mf_dims* d) {
@@ -1085,10 +1107,11 @@ extern "C" mf_status mf_final(const mf_plan* p, const mf_dims* d, const mf_temb_
                             2 * H, fmod, 2 * H, 0, 0, st));
   }
   mf::LnModArgs ln{static_cast<const bf16*>(d_x_img), nullptr, p->Ni, p->Ni, H,
-                   p->d_srow_seq + p->Nt, fmod, 2LL * H, 0, 0, H, a, p->S};
+                   p->d_srow_seq + p->Nt, fmod, 2LL * H, 0, 0, H, a, p->S, nullptr, di->status,
+                   wait_limit_ns()};
   {
     Trace tr(MF_K_LN, st, 0, 4.0 * p->Ni * H, 1);
-    MF_CUDA(mf::launch_ln_modulate(ln, st));
+    MF_CUDA(launch_ln(ln, 0, st));
   }
   mf::GemmParams gp{};
   GemmSpec sp[1] = {{p->Ni, C, H, a, w_out, b_out, d_v, C, 0, 1}};

@@ -103,7 +103,43 @@ __device__ __forceinline__ void report_status(unsigned* status, unsigned bits) {
   if (status != nullptr) atomicOr(status, bits);
 }
 
+// ------------------------------------------------------------------ packed f32x2 arithmetic
+// One instruction for a pair of f32 values.
+// (a0, a1) += (x0, x1)
+__device__ __forceinline__ void f32x2_add(float& a0, float& a1, float x0, float x1) {
+  asm("{\n\t.reg .b64 a, x;\n\t"
+      "mov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\t"
+      "add.rn.f32x2 a, a, x;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1));
+}
+// (x0, x1) = (x0 * a0 + b0, x1 * a1 + b1)
+__device__ __forceinline__ void f32x2_fma(float& x0, float& x1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, a, b;\n\t"
+      "mov.b64 x, {%0, %1};\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "fma.rn.f32x2 x, x, a, b;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(x0), "+f"(x1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (x0, x1) = (x0 * c + d, x1 * c + d)
+__device__ __forceinline__ void f32x2_fma_s(float& x0, float& x1, float c, float d) {
+  asm("{\n\t.reg .b64 x, c, d;\n\t"
+      "mov.b64 x, {%0, %1};\n\tmov.b64 c, {%2, %2};\n\tmov.b64 d, {%3, %3};\n\t"
+      "fma.rn.f32x2 x, x, c, d;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(x0), "+f"(x1)
+      : "f"(c), "f"(d));
+}
+
 // ------------------------------------------------------------------ TMA
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to
+// this CTA's shared memory, completing on `bar` (which expects the bytes).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }

@@ -275,23 +275,24 @@ __device__ __forceinline__ void epi_row16(const GemmParams& p, const GemmProblem
   }
 }
 
-// Phase 2: 8 columns of one row to global memory.
+// Phase 2: 8 columns of one row to global memory; returns the bf16 word written (zero when the
+// position lies outside the problem).
 template <int EPI>
-__device__ __forceinline__ void epi_store8(const GemmParams& p, const GemmProblem& pr, int row, int col,
-                                           const float4& a, const float4& b) {
+__device__ __forceinline__ uint4 epi_store8(const GemmParams& p, const GemmProblem& pr, int row, int col,
+                                            const float4& a, const float4& b) {
   constexpr int E = EPI & 7;
-  if (row >= pr.M || col >= pr.N) return;
+  if (row >= pr.M || col >= pr.N) return make_uint4(0u, 0u, 0u, 0u);
   if constexpr (E == kEpiBiasF32) {
     float4* o = reinterpret_cast<float4*>(static_cast<float*>(pr.out) + (size_t)row * pr.ldo + col);
     o[0] = a;
     o[1] = b;
-    return;
+    return make_uint4(0u, 0u, 0u, 0u);
   }
   float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   bf16* dst;
   if constexpr (E == kEpiQkvRope) {
     const int joint = __ldg(p.srow_joint + pr.row_off + row);
-    if (!MF_IDX_OK(joint >= 0 && joint < p.n_tok)) return;
+    if (!MF_IDX_OK(joint >= 0 && joint < p.n_tok)) return make_uint4(0u, 0u, 0u, 0u);
     const int which = col / p.H;
     dst = (which == 0 ? p.q : (which == 1 ? p.k : p.v)) + (size_t)joint * p.H + (col - which * p.H);
   } else {
@@ -303,7 +304,7 @@ __device__ __forceinline__ void epi_store8(const GemmParams& p, const GemmProble
           make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                      pack_bf16x2(v[6], v[7]));
     const int seq = __ldg(p.srow_seq + pr.row_off + row);
-    if (!MF_IDX_OK(seq >= 0 && seq < p.n_seq)) return;
+    if (!MF_IDX_OK(seq >= 0 && seq < p.n_seq)) return make_uint4(0u, 0u, 0u, 0u);
     const float4* g = reinterpret_cast<const float4*>(
         p.mod + ((size_t)seq * 2 + pr.stream) * 6 * (size_t)p.H + p.gate_off + col);
     const float4 ga = __ldg(g), gb = __ldg(g + 1);
@@ -321,6 +322,31 @@ __device__ __forceinline__ void epi_store8(const GemmParams& p, const GemmProble
   w.z = pack_bf16x2(v[4], v[5]);
   w.w = pack_bf16x2(v[6], v[7]);
   *reinterpret_cast<uint4*>(dst) = w;
+  return w;
+}
+
+// Running statistics of one row's bf16 outputs in this thread (kEpiStats): sums of the values'
+// deviations from a shift k (the first value seen), so that the sum of squares does not cancel
+// when the row's mean is large next to its spread.
+struct RowStats {
+  float k, s1, s2;
+};
+__device__ __forceinline__ void row_stats_add(RowStats& st, const uint4& w, bool first) {
+  const float2 a = unpack_bf16x2(w.x), b = unpack_bf16x2(w.y), c = unpack_bf16x2(w.z), e = unpack_bf16x2(w.w);
+  const float v[8] = {a.x, a.y, b.x, b.y, c.x, c.y, e.x, e.y};
+  if (first) st = RowStats{v[0], 0.0f, 0.0f};
+  float s1a = 0.0f, s1b = 0.0f, s2a = 0.0f, s2b = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    float d0 = v[i], d1 = v[i + 1];
+    f32x2_add(d0, d1, -st.k, -st.k);
+    f32x2_add(s1a, s1b, d0, d1);
+    f32x2_fma(d0, d1, d0, d1, s2a, s2b);  // d * d + s2
+    s2a = d0;
+    s2b = d1;
+  }
+  st.s1 += s1a + s1b;
+  st.s2 += s2a + s2b;
 }
 
 template <int BN, int EPI>
@@ -803,6 +829,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
           qk_rstd1 = rsqrtf(ss1 / (float)p.head_dim + kQkNormEps);
         }
       }
+      RowStats rs[2];  // kEpiStats: rows 16 it + lane / 2 of this warp's 128 columns
 #pragma unroll 1
       for (int c = c_lo; c < c_lo + BN / 2; c += 16) {
         uint32_t r[16];
@@ -822,9 +849,27 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         for (int it = 0; it < 2; ++it) {  // rows 16 it .. 16 it + 15, two threads per row
           const int rr = 16 * it + (lane >> 1), hh = lane & 1;
           const float4* rp = reinterpret_cast<const float4*>(stg + rr * kStageRow + hh * 8);
-          epi_store8<EPI>(p, pr, row0 + rr, n * BN + c + hh * 8, rp[0], rp[1]);
+          const uint4 w = epi_store8<EPI>(p, pr, row0 + rr, n * BN + c + hh * 8, rp[0], rp[1]);
+          if constexpr ((EPI & kEpiStats) != 0) row_stats_add(rs[it], w, c == c_lo);
         }
         __syncwarp();
+      }
+      if constexpr ((EPI & kEpiStats) != 0) {
+        // each lane holds 64 values of its row, its partner (lane ^ 1) the other 64 of the
+        // 128-column part: (mean, M2) of each, then the two merged (equal counts)
+        const int part = (n * BN + c_lo) >> 7;
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+          const float m = rs[it].k + rs[it].s1 * (1.0f / 64.0f);
+          const float m2 = fmaxf(rs[it].s2 - rs[it].s1 * rs[it].s1 * (1.0f / 64.0f), 0.0f);
+          const float mo = __shfl_xor_sync(0xffffffffu, m, 1);
+          const float m2o = __shfl_xor_sync(0xffffffffu, m2, 1);
+          const float d = mo - m;
+          const int row = row0 + 16 * it + (lane >> 1);
+          if ((lane & 1) == 0 && row < pr.M)
+            p.ln_stats[(size_t)(pr.row_off + row) * p.ln_parts + part] =
+                make_float2(0.5f * (m + mo), m2 + m2o + 32.0f * d * d);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -897,6 +942,7 @@ cudaError_t launch_gemm_pair(const GemmParams& p, int epi, int num_sms, cudaStre
   switch (epi) {
     case kEpiGelu | kEpiSave: return launch_pair<kEpiGelu | kEpiSave>(p, num_sms, stream);
     case kEpiGateResid | kEpiSave: return launch_pair<kEpiGateResid | kEpiSave>(p, num_sms, stream);
+    case kEpiGateResid | kEpiStats: return launch_pair<kEpiGateResid | kEpiStats>(p, num_sms, stream);
     case kEpiBiasBf16: return launch_pair<kEpiBiasBf16>(p, num_sms, stream);
     case kEpiBiasF32: return launch_pair<kEpiBiasF32>(p, num_sms, stream);
     case kEpiQkvRope: return launch_pair<kEpiQkvRope>(p, num_sms, stream);

@@ -20,6 +20,8 @@ enum GemmEpi : int {
                       // accumulator is first multiplied by row_scale[row_off + row] * col_scale[col]
   kEpiSave = 16,      // flag on kEpiGelu / kEpiGateResid (pair kernel, bf16): the value before
                       // GELU / before the gate (acc + bias) is also written to aux[row][col]
+  kEpiStats = 32,     // flag on kEpiGateResid (pair kernel, bf16): the LN statistics of the new x
+                      // (its bf16 values) are written per 128-column part, see GemmParams::ln_stats
 };
 
 // Operand majorness of the pair kernel (bf16 only): bit 0 A, bit 1 B.  K-major (0): the matrix
@@ -60,6 +62,10 @@ struct GemmParams {
   int gate_off;           // float offset of the gate chunk inside a (sample, stream) mod row
   const bf16* qk_norm[2][2];  // [problem][q, k]: QK-RMSNorm scales [head_dim], or null (off)
   const float* row_scale;     // kEpiF8: dequantisation scale of A's rows (indexed row_off + row)
+  // kEpiStats: (mean, sum of squared deviations from it) of each row's 128-column part j of the
+  // output, at ln_stats[(row_off + row) * ln_parts + j], ln_parts = N / 128 (N a multiple of 256)
+  float2* ln_stats;
+  int ln_parts;
   bf16* q;                // [N_tok][H] joint order
   bf16* k;
   bf16* v;

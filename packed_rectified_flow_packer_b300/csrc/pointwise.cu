@@ -230,6 +230,219 @@ __global__ void __launch_bounds__(128) ln_modulate_kernel(const LnModArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ LN + modulate, row groups
+// The CTA walks a contiguous range of stream-sorted rows in groups of 8 (per-element arithmetic
+// in packed f32x2 pairs).  One thread stages
+// each group in shared memory with bulk copies (one per row, plus the group's statistics parts
+// when they are given), `stages` groups ahead: a stage is refilled as soon as every thread has
+// moved its group into registers, so the copies keep HBM busy while the threads work, and two
+// CTAs per SM overlap each other's barriers.  Thread t owns the columns 8t .. 8t + 7 (blockDim.x = H / 8) and keeps their
+// shift and 1 + scale in registers while the rows' (sample, stream) stays the same.  A row's
+// statistics are (mean, M2 = sum of squared deviations from the mean) merged from parts with
+// Chan's pairwise update (Chan, Golub & LeVeque, "Updating formulae and a pairwise algorithm for
+// computing sample variances"): for parts (n_a, m_a, M2_a), (n_b, m_b, M2_b) and n = n_a + n_b,
+// d = m_b - m_a, m = m_a + d n_b / n, M2 = M2_a + M2_b + d^2 n_a n_b / n.
+constexpr int kLnMaxStages = 4;
+constexpr int kLnSmemBudget = 100 * 1024;  // per CTA; two CTAs per SM
+
+__device__ __forceinline__ void chan_merge(float& n, float& m, float& m2, float nb, float mb, float m2b) {
+  const float tot = n + nb;
+  if (nb > 0.0f) {
+    const float d = mb - m;
+    const float f = nb / tot;
+    m = fmaf(d, f, m);
+    m2 += m2b + d * d * n * f;
+    n = tot;
+  }
+}
+
+// All lanes end with the merge of every lane's (n, m, m2).
+__device__ __forceinline__ void chan_merge_warp(float& n, float& m, float& m2) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float nb = __shfl_xor_sync(0xffffffffu, n, o);
+    const float mb = __shfl_xor_sync(0xffffffffu, m, o);
+    const float m2b = __shfl_xor_sync(0xffffffffu, m2, o);
+    if (n == 0.0f) {
+      n = nb; m = mb; m2 = m2b;
+    } else {
+      chan_merge(n, m, m2, nb, mb, m2b);
+    }
+  }
+}
+
+__device__ __forceinline__ const bf16* ln_row_ptr(const LnModArgs& a, int r) {
+  return r >= a.n_first ? a.x_second + (size_t)(r - a.n_first) * a.H : a.x_first + (size_t)r * a.H;
+}
+
+// One level of the warp's row-halving merge: a lane keeps half of its R rows (the upper half
+// when `up`), receives the partner's values for those rows and merges them (equal counts, cnt
+// per side), and sends the other half.
+template <int R>
+__device__ __forceinline__ void ln_halve(float (&m)[8], float (&q)[8], bool up, int mask, float cnt) {
+#pragma unroll
+  for (int k = 0; k < R / 2; ++k) {
+    const float km = up ? m[k + R / 2] : m[k], kq = up ? q[k + R / 2] : q[k];
+    const float sm = up ? m[k] : m[k + R / 2], sq = up ? q[k] : q[k + R / 2];
+    const float rm = __shfl_xor_sync(0xffffffffu, sm, mask);
+    const float rq = __shfl_xor_sync(0xffffffffu, sq, mask);
+    const float d = rm - km;
+    m[k] = 0.5f * (km + rm);
+    q[k] = kq + rq + d * d * (0.5f * cnt);
+  }
+}
+
+template <bool kGiven, int kMaxThreads>
+__global__ void __launch_bounds__(kMaxThreads, 2) ln_group_kernel(const LnModArgs a, int rows_per_cta, int stages) {
+  extern __shared__ __align__(128) uint8_t ln_smem[];
+  __shared__ uint64_t full_bar[kLnMaxStages];
+  __shared__ float2 part_sh[16][8];  // per warp and group row: (mean, M2) over the warp's 256 columns
+  __shared__ float2 row_sh[2][8];    // per group row: (mean, rstd); double-buffered
+  __shared__ int abort_sh;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
+  const int H = a.H, parts = H >> 7;
+  const int r_begin = blockIdx.x * rows_per_cta;
+  const int r_end = min(a.rows, r_begin + rows_per_cta);
+  if (r_begin >= r_end) return;
+  const int n_groups = (r_end - r_begin + 7) >> 3;
+  const uint32_t row_bytes = (uint32_t)H * 2;
+  const uint32_t stage_bytes = 8 * row_bytes + (kGiven ? 8u * parts * 8 : 0u);
+  if (t == 0) {
+    for (int s = 0; s < stages; ++s) mbar_init(&full_bar[s], 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  int issued = 0;  // thread 0: groups whose copies have been issued
+  auto issue = [&](int g) {
+    const int s = g % stages, r0 = r_begin + 8 * g, nr = min(8, r_end - r0);
+    uint8_t* buf = ln_smem + (size_t)s * stage_bytes;
+    mbar_arrive_expect_tx(&full_bar[s], nr * row_bytes + (kGiven ? nr * parts * 8u : 0u));
+    for (int i = 0; i < nr; ++i) bulk_load(buf + i * row_bytes, ln_row_ptr(a, r0 + i), row_bytes, &full_bar[s]);
+    if constexpr (kGiven) bulk_load(buf + 8 * row_bytes, a.stats + (size_t)r0 * parts, nr * parts * 8u, &full_bar[s]);
+    issued = g + 1;
+  };
+  if (t == 0)
+    for (int g = 0; g < min(stages, n_groups); ++g) issue(g);
+  int key = -1;  // sample * 2 + stream whose (shift, 1 + scale) are in sh, sc1
+  float sh[8], sc1[8];
+  int g = 0;
+  for (; g < n_groups; ++g) {
+    const int s = g % stages, r0 = r_begin + 8 * g, nr = min(8, r_end - r0);
+    const uint8_t* buf = ln_smem + (size_t)s * stage_bytes;
+    if (!mbar_wait(&full_bar[s], (uint32_t)(g / stages) & 1u, a.wait_limit_ns)) {
+      report_status(a.status, kStatusTimeout);
+      abort_sh = 1;
+    }
+    float2* ms = row_sh[g & 1];
+    uint4 cur[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cur[i] = reinterpret_cast<const uint4*>(buf + i * row_bytes)[t];
+    if constexpr (kGiven) {
+      const float2* st = reinterpret_cast<const float2*>(buf + 8 * row_bytes);
+      for (int w = warp; w < nr; w += nwarps) {  // warp w: group row w
+        float n = 0.0f, m = 0.0f, m2 = 0.0f;
+        if (lane < parts) {
+          const float2 v = st[w * parts + lane];
+          n = 128.0f; m = v.x; m2 = v.y;
+        }
+        chan_merge_warp(n, m, m2);
+        if (lane == 0) ms[w] = make_float2(m, rsqrtf(m2 / (float)H + 1e-6f));
+      }
+    } else {
+      float m[8], q[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float v[8];
+        unpack8(cur[i], v);
+        float s0 = v[0], s1 = v[1];
+        f32x2_add(s0, s1, v[2], v[3]);
+        f32x2_add(s0, s1, v[4], v[5]);
+        f32x2_add(s0, s1, v[6], v[7]);
+        m[i] = (s0 + s1) * 0.125f;
+        float q0 = 0.0f, q1 = 0.0f;
+#pragma unroll
+        for (int u = 0; u < 8; u += 2) {
+          float d0 = v[u], d1 = v[u + 1];
+          f32x2_add(d0, d1, -m[i], -m[i]);
+          f32x2_fma(d0, d1, d0, d1, q0, q1);  // d * d + q
+          q0 = d0;
+          q1 = d1;
+        }
+        q[i] = q0 + q1;
+      }
+      ln_halve<8>(m, q, (lane & 16) != 0, 16, 8.0f);
+      ln_halve<4>(m, q, (lane & 8) != 0, 8, 16.0f);
+      ln_halve<2>(m, q, (lane & 4) != 0, 4, 32.0f);
+#pragma unroll
+      for (int o = 2, cnt = 64; o > 0; o >>= 1, cnt *= 2) {  // the four lanes of one row
+        const float rm = __shfl_xor_sync(0xffffffffu, m[0], o);
+        const float rq = __shfl_xor_sync(0xffffffffu, q[0], o);
+        const float d = rm - m[0];
+        m[0] = 0.5f * (m[0] + rm);
+        q[0] = q[0] + rq + d * d * (0.5f * (float)cnt);
+      }
+      if ((lane & 3) == 0)
+        part_sh[warp][((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1)] = make_float2(m[0], q[0]);
+      __syncthreads();
+      for (int w = warp; w < 8; w += nwarps) {  // warp w: group row w
+        float n = 0.0f, mm = 0.0f, m2 = 0.0f;
+        if (lane < nwarps) {
+          const float2 v = part_sh[lane][w];
+          n = 256.0f; mm = v.x; m2 = v.y;
+        }
+        chan_merge_warp(n, mm, m2);
+        if (lane == 0) ms[w] = make_float2(mm, rsqrtf(m2 / (float)H + 1e-6f));
+      }
+    }
+    __syncthreads();
+    if (abort_sh) break;
+    // every thread holds group g in registers, so its stage can take group g + stages
+    if (t == 0 && g + stages < n_groups) {
+      fence_proxy_async_smem();
+      issue(g + stages);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i >= nr) break;
+      const int r = r0 + i;
+      const int st = r >= a.n_first ? 1 : 0;
+      const int seq = __ldg(a.row_seq + r);
+      if (!MF_IDX_OK(seq >= 0 && seq < a.n_seq)) break;
+      if (seq * 2 + st != key) {
+        key = seq * 2 + st;
+        const float* mrow = a.mod + (size_t)seq * a.seq_stride + (st ? a.stream_stride : 0);
+        const float4* shp = reinterpret_cast<const float4*>(mrow + a.shift_off) + 2 * t;
+        const float4* scp = reinterpret_cast<const float4*>(mrow + a.scale_off) + 2 * t;
+        const float4 s0 = __ldg(shp), s1 = __ldg(shp + 1), k0 = __ldg(scp), k1 = __ldg(scp + 1);
+        sh[0] = s0.x; sh[1] = s0.y; sh[2] = s0.z; sh[3] = s0.w; sh[4] = s1.x; sh[5] = s1.y; sh[6] = s1.z; sh[7] = s1.w;
+        sc1[0] = 1.0f + k0.x; sc1[1] = 1.0f + k0.y; sc1[2] = 1.0f + k0.z; sc1[3] = 1.0f + k0.w;
+        sc1[4] = 1.0f + k1.x; sc1[5] = 1.0f + k1.y; sc1[6] = 1.0f + k1.z; sc1[7] = 1.0f + k1.w;
+      }
+      const float2 mr = ms[i];                  // (mean, rstd)
+      const float nmr = -mr.x * mr.y;
+      float v[8];
+      unpack8(cur[i], v);
+#pragma unroll
+      for (int u = 0; u < 8; u += 2) {
+        f32x2_fma_s(v[u], v[u + 1], mr.y, nmr);                            // (x - mean) rstd
+        f32x2_fma(v[u], v[u + 1], sc1[u], sc1[u + 1], sh[u], sh[u + 1]);  // ... (1 + scale) + shift
+      }
+      uint4 w;
+      w.x = pack_bf16x2(v[0], v[1]);
+      w.y = pack_bf16x2(v[2], v[3]);
+      w.z = pack_bf16x2(v[4], v[5]);
+      w.w = pack_bf16x2(v[6], v[7]);
+      reinterpret_cast<uint4*>(a.out + (size_t)r * H)[t] = w;
+    }
+  }
+  if (t == 0 && g < n_groups) {
+    // stopped early: let the copies still in flight land before the CTA's shared memory goes
+    for (int gg = g; gg < issued; ++gg)
+      (void)mbar_wait(&full_bar[gg % stages], (uint32_t)(gg / stages) & 1u, a.wait_limit_ns);
+  }
+}
+
 // ------------------------------------------------------------------ fp8 quantisation
 // One warp per row; lane l takes the 16-element chunks l, l + 32, ...  Pass 1 finds the row's
 // largest magnitude, pass 2 (the row again, now from L1 / L2) divides and converts.
@@ -543,6 +756,38 @@ cudaError_t launch_ln_modulate(const LnModArgs& a, cudaStream_t st) {
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+template <bool kGiven, int kMaxThreads>
+cudaError_t launch_ln_group_t(const LnModArgs& a, int sms, cudaStream_t st) {
+  const int stage_bytes = 8 * a.H * 2 + (kGiven ? 8 * (a.H / 128) * 8 : 0);
+  const int stages = std::min(kLnMaxStages, kLnSmemBudget / stage_bytes);
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(ln_group_kernel<kGiven, kMaxThreads>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kLnSmemBudget);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  // two CTAs per SM (shared memory), contiguous row ranges of a multiple of 8 rows
+  const int ctas = 2 * sms;
+  int per_cta = (a.rows + ctas - 1) / ctas;
+  per_cta = (per_cta + 7) / 8 * 8;
+  const int grid = (a.rows + per_cta - 1) / per_cta;
+  ln_group_kernel<kGiven, kMaxThreads><<<grid, a.H / 8, stages * stage_bytes, st>>>(a, per_cta, stages);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ln_group(const LnModArgs& a, cudaStream_t st) {
+  if (a.rows <= 0) return cudaSuccess;
+  if (a.H % 256 != 0 || a.H > 4096) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (a.H <= 3072)
+    return a.stats ? launch_ln_group_t<true, 384>(a, sms, st) : launch_ln_group_t<false, 384>(a, sms, st);
+  return a.stats ? launch_ln_group_t<true, 512>(a, sms, st) : launch_ln_group_t<false, 512>(a, sms, st);
 }
 
 cudaError_t launch_interpolate(const int* img_seq, const int* img_target, const float* t, int Ni,

@@ -44,8 +44,18 @@ struct LnModArgs {
   int scale_off;
   bf16* out;
   int n_seq;        // bound of row_seq's values
+  // optional: per row r, (mean, sum of squared deviations) of each 128-column part j of x[r] at
+  // stats[r * (H / 128) + j], as a GEMM epilogue with kEpiStats writes them; null = computed here
+  const float2* stats;
+  unsigned* status;                 // row-group kernel: bounded waits report here
+  unsigned long long wait_limit_ns;
 };
+// Warp-per-row kernel (statistics from the row in registers).
 cudaError_t launch_ln_modulate(const LnModArgs& a, cudaStream_t st);
+// Row-group kernel: groups of 8 rows staged in shared memory by bulk copies several groups
+// ahead; thread t owns columns 8t .. 8t + 7 and keeps their (shift, scale) in registers across
+// the rows of one (sample, stream); statistics from a.stats when given, else computed per group.
+cudaError_t launch_ln_group(const LnModArgs& a, cudaStream_t st);
 
 cudaError_t launch_interpolate(const int* img_seq, const int* img_target, const float* t, int Ni,
                                int C, const float* z, const float* eps, float* zt,

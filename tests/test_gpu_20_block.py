@@ -170,6 +170,71 @@ def test_mid_pack_block(seed):
     _stack_and_loss(case, 1)
 
 
+def _part_stats(x):
+    """(mean, sum of squared deviations) of each 128-column part of each row, float64."""
+    r = x.reshape(len(x), -1, 128)
+    m = r.mean(axis=2)
+    return m, ((r - m[..., None]) ** 2).sum(axis=2)
+
+
+@pytest.mark.parametrize("size", ["tiny", "mid"])
+def test_ln_variants(size):
+    """The LN + modulate variants of mf_block_forward_ex - one warp per row (the default), row
+    groups, and the second LN's statistics fused into the out-projection's epilogue - each match the
+    oracle's block.  The fused statistics themselves match (mean, M2) of every 128-column part of
+    the residual after attention, x + gate1 (o W_o^T + b_o), formed by the oracle's functions from
+    the GPU's own attention output o."""
+    if size == "tiny":
+        case = Case(synth.tiny_samples(), synth.TINY, 1, seed=3)
+    else:
+        case = Case(_mid_samples(7), MID, 1, seed=17)
+    d, ref = case.dims, case.ref
+    H = d.hidden
+    g = np.random.default_rng(40)
+    xi0 = synth.round_bf16(g.standard_normal((ref.n_img, H)).astype(np.float32) + 0.5)
+    xt0 = case.x_txt_np
+    xt_ref, xi_ref, _ = oracle_stack(case.samples, ref, case.w, case.batch, d.heads, x_img_in=xi0, n_blocks=1)
+    off = mf.mf_block_workspace_layout(case.plan, case.model.dims)
+    outs = {}
+    for name, flags in (("warp rows", 0), ("row groups", mf.BLOCK_LN_ROW_GROUPS),
+                        ("fused stats", mf.BLOCK_LN_STATS_FUSED),
+                        ("row groups + fused stats", mf.BLOCK_LN_ROW_GROUPS | mf.BLOCK_LN_STATS_FUSED)):
+        xt = to_bf16(xt0 if len(xt0) else np.zeros((1, H), np.float32))
+        xi = to_bf16(xi0)
+        case.ws.block.zero_()
+        mf.mf_block_forward_ex(case.plan, case.model.dims, case.model.block_structs[0], None, xt, xi,
+                               case.ws.block, flags)
+        mf.mf_check()
+        got_t, got_i = _f(xt)[:ref.n_txt], _f(xi)
+        if ref.n_txt:
+            assert_close(got_t, xt_ref, f"{name}: block x_txt")
+        assert_close(got_i, xi_ref, f"{name}: block x_img")
+        outs[name] = np.concatenate([got_t, got_i])
+        if flags & mf.BLOCK_LN_STATS_FUSED:
+            N = ref.n_txt + ref.n_img
+            wsb = case.ws.block
+            st = wsb[off[8]:off[8] + N * (H // 128) * 8].view(torch.float32).cpu().numpy().astype(np.float64)
+            st = st.reshape(N, H // 128, 2)
+            o = _f(wsb[off[6]:off[6] + N * H * 2].view(torch.bfloat16).reshape(N, H))
+            x_in = np.concatenate([xt0[:ref.n_txt], xi0]).astype(np.float64)
+            x1 = np.empty((N, H))
+            for k, c in enumerate(ref.order):
+                cond = M.condition(case.samples[c].t, case.w.temb, d.freq_dim)
+                rows = {"txt": np.arange(ref.cu_txt[k], ref.cu_txt[k + 1]),
+                        "img": ref.n_txt + np.arange(ref.cu_img[k], ref.cu_img[k + 1])}
+                for s_ in M.STREAMS:
+                    bw = case.w.blocks[0][s_]
+                    gate1 = M.modulation(cond, bw["w_mod"], bw["b_mod"], 6)[2]
+                    r = rows[s_]
+                    x1[r] = x_in[r] + gate1 * M.linear(o[r], bw["w_o"], bw["b_o"])
+            m_ref, q_ref = _part_stats(x1)
+            assert_close(st[..., 0], m_ref, "fused statistics: part means")
+            assert_close(st[..., 1], q_ref, "fused statistics: part M2")
+    # the variants differ only in the f32 order of the statistics' sums
+    for name in ("row groups", "fused stats", "row groups + fused stats"):
+        assert_close(outs[name], outs["warp rows"], f"{name} vs warp rows", rel=1e-2, cos=0.99999)
+
+
 def test_tiny_stack_qk_norm():
     """QK-RMSNorm variant at the tiny size (D = 64: each epilogue warp's 128 columns hold two
     heads, each normalised on its own)."""
