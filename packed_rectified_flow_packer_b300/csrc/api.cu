@@ -831,7 +831,7 @@ namespace {
 // bf16; dx1 [N][H] f32; do [N][H] bf16; dqkv [N][3H] bf16; dk, dv [N][H] bf16 joint order; the
 // attention backward's own workspace.
 struct BwdLayout {
-  size_t dmod, dy, du, da, dx1, dout, dqkv, dk, dv, attn, total;
+  size_t dmod, dy, du, da, dx1, dout, dqkv, dk, dv, attn, rstats, total;
 };
 
 BwdLayout bwd_layout(const mf_plan* p, const mf_dims* d) {
@@ -849,6 +849,7 @@ BwdLayout bwd_layout(const mf_plan* p, const mf_dims* d) {
   L.dk = take(N * H * 2);
   L.dv = take(N * H * 2);
   L.attn = take(attn_bwd_layout(p, d->heads, H / d->heads).total);
+  L.rstats = take(N * 16);
   L.total = o;
   return L;
 }
@@ -943,6 +944,8 @@ extern "C" mf_status mf_block_backward(const mf_plan* p, const mf_dims* d, const
   ra.dmod = dmod;
   ra.n_rows = N;
   ra.n_seq = S;
+  ra.row_seq = p->d_srow_seq;
+  ra.stats = reinterpret_cast<float4*>(ws + L.rstats);
   mf::GemmParams gp{};
   // input-gradient GEMM per stream: out[rows][N] = A[rows][K] W, W stored [K][N]
   auto dgrad = [&](const bf16* A, int K, int Nn, const void* W0, const void* W1, bf16* out, int epi,

@@ -40,6 +40,8 @@ struct RowBwdArgs {
   bf16* out_first;            // kRowLn1: text rows of dx
   bf16* out_second;           // kRowLn1: image rows of dx
   int n_rows, n_seq;          // stream-sorted rows and samples of the pack (bounds of the chunks)
+  const int* row_seq;         // kRowLn*: [rows] sample of each stream-sorted row
+  float4* stats;              // kRowLn*: [rows] scratch for the rows' LN statistics
 };
 // H a multiple of 256, at most 4096.
 cudaError_t launch_row_bwd(const RowBwdArgs& a, cudaStream_t st);
