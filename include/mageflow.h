@@ -248,9 +248,16 @@ mf_status mf_block_forward(const mf_plan* plan, const mf_dims* dims, const mf_bl
  * differ only in f32 summation order. */
 #define MF_BLOCK_LN_ROW_GROUPS 1
 #define MF_BLOCK_LN_STATS_FUSED 2
+/* The timestep condition c [S][H] (workspace offset [0], see mf_block_workspace_layout) already
+ * holds SiLU(temb(t)) for this plan, these flow times and these timestep weights, as a previous
+ * block call with the same workspace left it (the blocks of a stack share the timestep
+ * embedder); the timestep MLP is skipped and only the block's own modulation GEMV runs.  A
+ * stale c (another plan or other t) gives wrong results, never an out-of-bounds access. */
+#define MF_BLOCK_COND_GIVEN 4
 
-/* mf_block_forward with a variant: flags a combination of MF_BLOCK_LN_* (with both, the first
- * LN runs in row groups and the second takes the fused statistics).  Errors: as
+/* mf_block_forward with variants: flags a combination of MF_BLOCK_LN_* (with both LN flags, the
+ * first LN runs in row groups and the second takes the fused statistics) and
+ * MF_BLOCK_COND_GIVEN.  Errors: as
  * mf_block_forward; MF_ERR_INVALID_ARG for unknown flags. */
 mf_status mf_block_forward_ex(const mf_plan* plan, const mf_dims* dims, const mf_block_weights* w,
                               const float* d_t, void* d_x_txt, void* d_x_img, void* d_ws,

@@ -13,7 +13,7 @@ import os
 
 import numpy as np
 
-__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_block_forward_ex", "BLOCK_LN_ROW_GROUPS", "BLOCK_LN_STATS_FUSED", "mf_block_train_workspace_bytes", "mf_block_forward_train", "mf_block_backward_workspace_bytes", "mf_block_backward", "grads_struct", "mf_stream_grads", "mf_block_grads", "GRAD_FIELDS", "mf_block_fp8_workspace_bytes", "mf_block_forward_fp8", "block_struct_fp8", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_attention_lse", "mf_attention_backward_workspace_bytes", "mf_attention_backward", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
+__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_block_forward_ex", "BLOCK_LN_ROW_GROUPS", "BLOCK_LN_STATS_FUSED", "BLOCK_COND_GIVEN", "mf_block_train_workspace_bytes", "mf_block_forward_train", "mf_block_backward_workspace_bytes", "mf_block_backward", "grads_struct", "mf_stream_grads", "mf_block_grads", "GRAD_FIELDS", "mf_block_fp8_workspace_bytes", "mf_block_forward_fp8", "block_struct_fp8", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_attention_lse", "mf_attention_backward_workspace_bytes", "mf_attention_backward", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
 
 # MAGEFLOW_LIB=checked selects the bounds-checked build (same ABI; see mf_check)
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
@@ -301,6 +301,7 @@ def mf_block_forward(plan: Plan, dims, weights: mf_block_weights, t, x_txt, x_im
 # LN + modulate variants of mf_block_forward_ex (the header's MF_BLOCK_LN_*)
 BLOCK_LN_ROW_GROUPS = 1
 BLOCK_LN_STATS_FUSED = 2
+BLOCK_COND_GIVEN = 4
 
 
 def mf_block_forward_ex(plan: Plan, dims, weights: mf_block_weights, t, x_txt, x_img, ws, flags, ws_bytes=None,

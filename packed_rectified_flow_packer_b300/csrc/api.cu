@@ -534,7 +534,8 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
   if (w == nullptr || !temb_ok(&w->temb) || !stream_ok(w->txt) || !stream_ok(w->img))
     return MF_ERR_INVALID_ARG;
   if (w8 != nullptr && (!stream8_ok(w8->txt) || !stream8_ok(w8->img))) return MF_ERR_INVALID_ARG;
-  if ((flags & ~(MF_BLOCK_LN_ROW_GROUPS | MF_BLOCK_LN_STATS_FUSED)) != 0) return MF_ERR_INVALID_ARG;
+  if ((flags & ~(MF_BLOCK_LN_ROW_GROUPS | MF_BLOCK_LN_STATS_FUSED | MF_BLOCK_COND_GIVEN)) != 0)
+    return MF_ERR_INVALID_ARG;
   if (flags & MF_BLOCK_LN_STATS_FUSED && (w8 != nullptr || train)) return MF_ERR_UNSUPPORTED;
   if (p->N == 0) return MF_OK;
   if ((p->Nt > 0 && d_x_txt == nullptr) || (p->Ni > 0 && d_x_img == nullptr) || d_ws == nullptr)
@@ -591,7 +592,7 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
   };
 
   // 1. timestep condition c = SiLU(temb(t)) and the per-sample adaLN modulation of both streams
-  MF_TRY(conditioning(p, d, &w->temb, t, sinus, h1, c, st));
+  if (!(flags & MF_BLOCK_COND_GIVEN)) MF_TRY(conditioning(p, d, &w->temb, t, sinus, h1, c, st));
   {
     // both streams' modulation GEMVs share c and run as one launch per group of four samples
     Trace tr(MF_K_COND, st, 2.0 * 2 * S * 6.0 * H * H, 2.0 * 2 * 6.0 * H * H, (S + 3) / 4);

@@ -56,8 +56,10 @@ def run_stack(plan, model: DeviceModel, x_txt, zt_bf16, x_img, v, ws: Workspace,
     [N_img][H] bf16 buffer the call overwrites; v is [N_img][C] f32."""
     d = model.dims
     B.mf_embed(plan, d, model.embed["w_in"], model.embed["b_in"], zt_bf16, x_img, stream=stream)
-    for bs in model.block_structs[:n_blocks]:
-        B.mf_block_forward(plan, d, bs, t, x_txt, x_img, ws.block, stream=stream)
+    # the first block leaves the timestep condition in the shared workspace; the rest reuse it
+    for i, bs in enumerate(model.block_structs[:n_blocks]):
+        B.mf_block_forward_ex(plan, d, bs, t, x_txt, x_img, ws.block, B.BLOCK_COND_GIVEN if i else 0,
+                              stream=stream)
     f = model.final
     B.mf_final(plan, d, model.temb_struct, f["w_fmod"], f["b_fmod"], f["w_out"], f["b_out"], t, x_img, v,
                ws.final, stream=stream)

@@ -235,6 +235,26 @@ def test_ln_variants(size):
         assert_close(outs[name], outs["warp rows"], f"{name} vs warp rows", rel=1e-2, cos=0.99999)
 
 
+def test_cond_given_reuse():
+    """Two blocks on a ragged H = 512 pack: the second block reusing the first block's timestep
+    condition from the shared workspace (MF_BLOCK_COND_GIVEN) gives the same output bit for bit
+    as recomputing it."""
+    case = Case(_mid_samples(3), MID, 2, seed=21)
+    ref, H = case.ref, case.dims.hidden
+    g = np.random.default_rng(8)
+    xi0 = synth.round_bf16(g.standard_normal((ref.n_img, H)).astype(np.float32))
+    outs = []
+    for flags in ((0, 0), (0, mf.BLOCK_COND_GIVEN)):
+        xt = to_bf16(case.x_txt_np if len(case.x_txt_np) else np.zeros((1, H), np.float32))
+        xi = to_bf16(xi0)
+        for b, fl in enumerate(flags):
+            mf.mf_block_forward_ex(case.plan, case.model.dims, case.model.block_structs[b], None, xt, xi,
+                                   case.ws.block, fl)
+        mf.mf_check()
+        outs.append((xt.cpu(), xi.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 def test_tiny_stack_qk_norm():
     """QK-RMSNorm variant at the tiny size (D = 64: each epilogue warp's 128 columns hold two
     heads, each normalised on its own)."""
