@@ -850,6 +850,11 @@ def run_train(args, rank, world, local_rank):
     de = trace[dom]
     achieved = de["flops"] / (de["ms"] / 1e3) / 1e12
     tflops = (fl_f + fl_b) / el / 1e12
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            traffic = json.load(f).get(dom)
     return {"metric": "packed tokens/s per NR-MMDiT block training step (fwd + bwd, 1xB300)",
             "value": round(tokens / el, 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
@@ -863,7 +868,8 @@ def run_train(args, rank, world, local_rank):
             "fwd_flops_share": round(fl_f / (fl_f + fl_b), 4),
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                         "peak_kind": f"dense bf16 burst ({peaks['source']})", "traffic": None},
+                         "peak_kind": f"dense bf16 burst ({peaks['source']})", "traffic": traffic,
+                         "avg_ms": round(de["ms"] / de["launches"], 4)},
             "gpu_launches": int(launches), "clocks": clocks, "kernels": kernels,
             "pages_context": "training step 1.9259 s -> 0.7748 s, MFU 33.20 % -> 77.26 % on 8xB200 "
                              "(PaperReading review, section 3, Table 4; whole model, 50K-token packs)"}
