@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
+  mf_pdl_enter();  // the prologue above touched no global memory the previous kernel writes
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -426,7 +427,7 @@ cudaError_t launch_d(const AttnParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.n_items * p.heads;
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
+  launch_k(kern, (unsigned)grid, kThreads, smem, stream, p);
   return cudaGetLastError();
 }
 

@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
+  mf_pdl_enter();  // the prologue above touched no global memory the previous kernel writes
   auto stage_ptr = [&](int st) { return smem + kOffStage + st * kStageBytes; };
 
   if (warp == 0) {
@@ -522,6 +523,7 @@ __global__ void attn_bwd_prep_kernel(const bf16* __restrict__ o, const bf16* __r
                                      int dout_joint, const int* __restrict__ joint_srow, int N, int H,
                                      int head_dim, bf16* __restrict__ do_joint, float* __restrict__ delta,
                                      float* __restrict__ dq_acc) {
+  mf_pdl_enter();
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int cph = head_dim / 8;  // 16-byte chunks per head (8 or 16), a power of two <= 16
@@ -552,6 +554,7 @@ __global__ void attn_bwd_prep_kernel(const bf16* __restrict__ o, const bf16* __r
 
 // dq[j] = bf16(dq_acc[j]) for the whole [N][H] accumulator (already scaled by 1 / sqrt(D)).
 __global__ void attn_bwd_dq_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, long long n4) {
+  mf_pdl_enter();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
     const float4 v = __ldg(acc + i);
     dq[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
@@ -565,7 +568,7 @@ cudaError_t launch_attention_bwd_prep(const bf16* o, const bf16* dout, int dout_
                                       int num_sms, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
   const int blocks = min((N + 7) / 8, num_sms * 8);
-  attn_bwd_prep_kernel<<<blocks, 256, 0, st>>>(o, dout, dout_joint, joint_srow, N, H, head_dim, do_joint, delta,
+  launch_k(attn_bwd_prep_kernel, blocks, 256, 0, st, o, dout, dout_joint, joint_srow, N, H, head_dim, do_joint, delta,
                                                dq_acc);
   return cudaGetLastError();
 }
@@ -575,7 +578,7 @@ cudaError_t launch_attention_bwd(const AttnBwdParams& p, long long n_ctas, cudaS
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (n_ctas <= 0) return cudaSuccess;
-  attn_bwd_kernel<<<(unsigned)n_ctas, kThreads, smem, st>>>(p);
+  launch_k(attn_bwd_kernel, (unsigned)n_ctas, kThreads, smem, st, p);
   return cudaGetLastError();
 }
 
@@ -583,7 +586,7 @@ cudaError_t launch_attention_bwd_dq(const float* acc, bf16* dq, long long n, int
   if (n <= 0) return cudaSuccess;
   const long long n4 = n / 4;
   const int blocks = (int)min((n4 + 255) / 256, (long long)num_sms * 8);
-  attn_bwd_dq_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(acc), reinterpret_cast<uint2*>(dq), n4);
+  launch_k(attn_bwd_dq_kernel, blocks, 256, 0, st, reinterpret_cast<const float4*>(acc), reinterpret_cast<uint2*>(dq), n4);
   return cudaGetLastError();
 }
 

@@ -55,6 +55,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <int NV>
 __global__ void __launch_bounds__(128) ln_bwd_stats_kernel(const RowBwdArgs a, const int* __restrict__ row_seq,
                                                            int scale_off, float4* __restrict__ stats) {
+  mf_pdl_enter();
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= a.n_rows) return;
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__(128) ln_bwd_stats_kernel(const RowBwdArgs a, c
 template <int MODE, int kMaxThreads, int kMinBlocks>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) row_bwd_kernel(const RowBwdArgs a,
                                                                           const float4* __restrict__ stats) {
+  mf_pdl_enter();
   constexpr int RB = MODE == kRowLn2 ? 2 : 4;  // rows per step, their loads in flight together
   extern __shared__ float sm[];
   const int H = a.H;
@@ -244,6 +246,7 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) row_bwd_kernel(const 
 // bias[stream][c..c+7] += column sums of x over the chunk's rows; grid (chunks, C / 2048).
 __global__ void col_sum_kernel(const bf16* __restrict__ x, int C, const int* __restrict__ chunks,
                                float* bias_txt, float* bias_img) {
+  mf_pdl_enter();
   const int* ch = chunks + 4 * blockIdx.x;
   const int row0 = __ldg(ch), row1 = __ldg(ch + 1), stream = __ldg(ch + 3);
   const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
@@ -279,6 +282,7 @@ __global__ void qkv_grad_gather_kernel(const float* __restrict__ dq_acc, const b
                                        const bf16* __restrict__ dv, const int* __restrict__ srow_joint,
                                        const int* __restrict__ pos, int rows, int H, int D,
                                        bf16* __restrict__ dqkv) {
+  mf_pdl_enter();
   __shared__ float rope_inv[64];
   __shared__ int rope_axis[64];
   if ((int)threadIdx.x < D / 2) {
@@ -342,6 +346,7 @@ constexpr int kDwRows = 16;
 __global__ void __launch_bounds__(256) mod_dw_kernel(const float* __restrict__ dmod, const float* __restrict__ c,
                                                      int S, int H, float* dw_txt, float* db_txt, float* dw_img,
                                                      float* db_img) {
+  mf_pdl_enter();
   __shared__ float g_sm[kDwRows][8];
   const int m = blockIdx.y;
   const int o0 = blockIdx.x * kDwRows;
@@ -394,6 +399,7 @@ template <int NS>
 __global__ void __launch_bounds__(128) mod_dc_kernel(const float* __restrict__ dmod, int S, int H,
                                                      const bf16* __restrict__ w_txt, const bf16* __restrict__ w_img,
                                                      float* dc) {
+  mf_pdl_enter();
   __shared__ float g_sm[kDcRows][NS];
   const int i = (blockIdx.x * 128 + threadIdx.x) * 8;
   const int o0 = blockIdx.y * kDcRows;            // row in the stacked [12H] range
@@ -452,7 +458,7 @@ cudaError_t launch_row_bwd(const RowBwdArgs& a, cudaStream_t st) {
     const int blocks = (a.n_rows + 3) / 4;
     switch (a.H / 256) {
 #define MF_STATS_CASE(nv) \
-  case nv: ln_bwd_stats_kernel<nv><<<blocks, 128, 0, st>>>(a, a.row_seq, scale_off, a.stats); break;
+  case nv: launch_k(ln_bwd_stats_kernel<nv>, blocks, 128, 0, st, a, a.row_seq, scale_off, a.stats); break;
       MF_STATS_CASE(1) MF_STATS_CASE(2) MF_STATS_CASE(3) MF_STATS_CASE(4) MF_STATS_CASE(5) MF_STATS_CASE(6)
       MF_STATS_CASE(7) MF_STATS_CASE(8) MF_STATS_CASE(9) MF_STATS_CASE(10) MF_STATS_CASE(11) MF_STATS_CASE(12)
       MF_STATS_CASE(13) MF_STATS_CASE(14) MF_STATS_CASE(15) MF_STATS_CASE(16)
@@ -469,16 +475,16 @@ cudaError_t launch_row_bwd(const RowBwdArgs& a, cudaStream_t st) {
   const bool two = threads <= 384;
   switch (a.mode) {
     case kRowGate2:
-      if (two) row_bwd_kernel<kRowGate2, 384, 2><<<grid, threads, smem, st>>>(a, a.stats);
-      else row_bwd_kernel<kRowGate2, 512, 1><<<grid, threads, smem, st>>>(a, a.stats);
+      if (two) launch_k(row_bwd_kernel<kRowGate2, 384, 2>, grid, threads, smem, st, a, a.stats);
+      else launch_k(row_bwd_kernel<kRowGate2, 512, 1>, grid, threads, smem, st, a, a.stats);
       break;
     case kRowLn2:
-      if (two) row_bwd_kernel<kRowLn2, 384, 2><<<grid, threads, smem, st>>>(a, a.stats);
-      else row_bwd_kernel<kRowLn2, 512, 1><<<grid, threads, smem, st>>>(a, a.stats);
+      if (two) launch_k(row_bwd_kernel<kRowLn2, 384, 2>, grid, threads, smem, st, a, a.stats);
+      else launch_k(row_bwd_kernel<kRowLn2, 512, 1>, grid, threads, smem, st, a, a.stats);
       break;
     case kRowLn1:
-      if (two) row_bwd_kernel<kRowLn1, 384, 2><<<grid, threads, smem, st>>>(a, a.stats);
-      else row_bwd_kernel<kRowLn1, 512, 1><<<grid, threads, smem, st>>>(a, a.stats);
+      if (two) launch_k(row_bwd_kernel<kRowLn1, 384, 2>, grid, threads, smem, st, a, a.stats);
+      else launch_k(row_bwd_kernel<kRowLn1, 512, 1>, grid, threads, smem, st, a, a.stats);
       break;
     default: return cudaErrorInvalidValue;
   }
@@ -489,7 +495,7 @@ cudaError_t launch_col_sum(const bf16* x, int C, const int* chunks, int n_chunks
                            cudaStream_t st) {
   if (n_chunks <= 0) return cudaSuccess;
   dim3 grid(n_chunks, (C / 8 + 255) / 256);
-  col_sum_kernel<<<grid, 256, 0, st>>>(x, C, chunks, bias_txt, bias_img);
+  launch_k(col_sum_kernel, grid, 256, 0, st, x, C, chunks, bias_txt, bias_img);
   return cudaGetLastError();
 }
 
@@ -498,7 +504,7 @@ cudaError_t launch_qkv_grad_gather(const float* dq_acc, const bf16* dk, const bf
                                    cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int blocks = min((rows + 7) / 8, num_sms * 8);
-  qkv_grad_gather_kernel<<<blocks, 256, 0, st>>>(dq_acc, dk, dv, srow_joint, pos, rows, H, head_dim, dqkv);
+  launch_k(qkv_grad_gather_kernel, blocks, 256, 0, st, dq_acc, dk, dv, srow_joint, pos, rows, H, head_dim, dqkv);
   return cudaGetLastError();
 }
 
@@ -507,7 +513,7 @@ cudaError_t launch_mod_bwd(const float* dmod, const float* c, int S, int H, cons
                            float* dc, cudaStream_t st) {
   if (S <= 0) return cudaSuccess;
   dim3 g1((6 * H + kDwRows - 1) / kDwRows, 2);
-  mod_dw_kernel<<<g1, 256, 0, st>>>(dmod, c, S, H, dw_txt, db_txt, dw_img, db_img);
+  launch_k(mod_dw_kernel, g1, 256, 0, st, dmod, c, S, H, dw_txt, db_txt, dw_img, db_img);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(dc, 0, (size_t)S * H * sizeof(float), st);
@@ -516,11 +522,11 @@ cudaError_t launch_mod_bwd(const float* dmod, const float* c, int S, int H, cons
   const int ns = S <= 2 ? 2 : (S <= 4 ? 4 : 8);
   dim3 g2((H / 8 + 127) / 128, (12 * H + kDcRows - 1) / kDcRows, (S + ns - 1) / ns);
   if (ns == 2)
-    mod_dc_kernel<2><<<g2, 128, 0, st>>>(dmod, S, H, w_mod_txt, w_mod_img, dc);
+    launch_k(mod_dc_kernel<2>, g2, 128, 0, st, dmod, S, H, w_mod_txt, w_mod_img, dc);
   else if (ns == 4)
-    mod_dc_kernel<4><<<g2, 128, 0, st>>>(dmod, S, H, w_mod_txt, w_mod_img, dc);
+    launch_k(mod_dc_kernel<4>, g2, 128, 0, st, dmod, S, H, w_mod_txt, w_mod_img, dc);
   else
-    mod_dc_kernel<8><<<g2, 128, 0, st>>>(dmod, S, H, w_mod_txt, w_mod_img, dc);
+    launch_k(mod_dc_kernel<8>, g2, 128, 0, st, dmod, S, H, w_mod_txt, w_mod_img, dc);
   return cudaGetLastError();
 }
 

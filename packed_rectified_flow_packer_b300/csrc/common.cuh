@@ -7,10 +7,53 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <utility>
 
 namespace mf {
 
 typedef __nv_bfloat16 bf16;
+
+// ------------------------------------------------------------------ programmatic dependent launch
+// Every kernel calls mf_pdl_enter() before its first access to global memory that an earlier
+// kernel of the stream writes: griddepcontrol.wait returns once the previous grid has completed
+// and its memory is visible (at once for a launch without the programmatic attribute), and
+// griddepcontrol.launch_dependents lets the next kernel's launch begin.  With MF_PDL=1 in the
+// environment every launch carries programmatic stream serialisation, so a kernel may be
+// scheduled and run its prologue (barrier initialisation, TMEM allocation, descriptor
+// prefetch) while the previous one finishes; on the 16K packs this measured no faster than
+// plain stream order, so it is off by default.
+__device__ __forceinline__ void mf_pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// MF_PDL=1 in the environment turns the attribute on; read once.
+inline bool pdl_allowed() {
+  static const bool on = [] {
+    const char* e = std::getenv("MF_PDL");
+    return e != nullptr && e[0] == '1';
+  }();
+  return on;
+}
+
+// kern<<<grid, block, smem, st>>>(args...), with the programmatic serialisation attribute when
+// pdl_allowed().
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_allowed() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Device status word bits (OR-ed by kernels; read and cleared by mf_check).
 enum : unsigned {

@@ -412,6 +412,7 @@ __global__ void __launch_bounds__(192, 1) gemm_kernel(const __grid_constant__ Ge
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
+  mf_pdl_enter();  // the prologue above touched no global memory the previous kernel writes
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -539,7 +540,7 @@ cudaError_t launch_t(const GemmParams& p, int num_sms, cudaStream_t stream) {
   const int total = p.tile_begin[p.n_prob];
   if (total <= 0) return cudaSuccess;
   const int grid = total < num_sms ? total : num_sms;
-  kern<<<grid, 192, smem, stream>>>(p);
+  launch_k(kern, grid, 192, smem, stream, p);
   return cudaGetLastError();
 }
 
@@ -630,6 +631,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
   cluster_sync();  // barriers of both CTAs initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
+  mf_pdl_enter();  // the prologue above touched no global memory the previous kernel writes
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
@@ -896,11 +898,13 @@ cudaError_t launch_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
   const int smem = STAGES * (kBM * kBK * 2 + 128 * kBK * 2) + kStaging + 1024;
   auto kern = gemm_pair_kernel<EPI, MAJ>;
   static int max_pairs = 0;  // clusters of two that fit on the device at once (per instantiation)
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
@@ -921,6 +925,7 @@ cudaError_t launch_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
   if (total <= 0) return cudaSuccess;
   const int pairs = total < max_pairs ? total : max_pairs;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.numAttrs = pdl_allowed() ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

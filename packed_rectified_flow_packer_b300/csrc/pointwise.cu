@@ -37,6 +37,7 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 
 // ------------------------------------------------------------------ conditioning
 __global__ void sinusoid_kernel(const float* __restrict__ t, int S, int F, float* __restrict__ out) {
+  mf_pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   const int half = F / 2;
   if (i >= S * half) return;
@@ -89,6 +90,7 @@ struct GemvArgs {
 
 template <int ACT, int NCH>
 __global__ void __launch_bounds__(128) gemv_kernel(const GemvArgs g) {
+  mf_pdl_enter();
   constexpr int K = NCH * 256;
   constexpr int R = kGemvRows, D = kGemvDepth;
   const int pb = blockIdx.y;
@@ -212,6 +214,7 @@ __device__ __forceinline__ void ln_row(const LnModArgs& a, int r, int lane, cons
 
 template <int NV>
 __global__ void __launch_bounds__(128) ln_modulate_kernel(const LnModArgs a) {
+  mf_pdl_enter();
   const int lane = threadIdx.x & 31;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -294,6 +297,7 @@ __device__ __forceinline__ void ln_halve(float (&m)[8], float (&q)[8], bool up, 
 
 template <bool kGiven, int kMaxThreads>
 __global__ void __launch_bounds__(kMaxThreads, 2) ln_group_kernel(const LnModArgs a, int rows_per_cta, int stages) {
+  mf_pdl_enter();
   extern __shared__ __align__(128) uint8_t ln_smem[];
   __shared__ uint64_t full_bar[kLnMaxStages];
   __shared__ float2 part_sh[16][8];  // per warp and group row: (mean, M2) over the warp's 256 columns
@@ -449,6 +453,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) ln_group_kernel(const LnModArg
 __global__ void __launch_bounds__(128) quantize_e4m3_rows_kernel(const bf16* __restrict__ x, int M, int K,
                                                                  uint8_t* __restrict__ q,
                                                                  float* __restrict__ s) {
+  mf_pdl_enter();
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= M) return;
@@ -489,6 +494,7 @@ __global__ void interpolate_kernel(const int* __restrict__ img_seq, const int* _
                                    const float* __restrict__ t, int Ni, int C,
                                    const float* __restrict__ z, const float* __restrict__ eps,
                                    float* __restrict__ zt, bf16* __restrict__ zt_bf16) {
+  mf_pdl_enter();
   const long long n4 = (long long)Ni * C / 4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
@@ -516,6 +522,7 @@ __global__ void interpolate_kernel(const int* __restrict__ img_seq, const int* _
 __global__ void cfg_kernel(const int* __restrict__ img_seq, const int* __restrict__ seq_role,
                            const int* __restrict__ img_pair, int Ni, int C, float w,
                            const float* v, float* out) {
+  mf_pdl_enter();
   const long long n4 = (long long)Ni * C / 4;
   const int c4n = C / 4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
@@ -541,6 +548,7 @@ __global__ void cfg_kernel(const int* __restrict__ img_seq, const int* __restric
 
 __global__ void euler_kernel(long long n4, float dt, const float* __restrict__ v, float* z,
                              bf16* __restrict__ z_bf16) {
+  mf_pdl_enter();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(v)[i];
@@ -563,6 +571,7 @@ __global__ void euler_kernel(long long n4, float dt, const float* __restrict__ v
 __global__ void loss_row_kernel(const int* __restrict__ img_target, int Ni, int C,
                                 const float* __restrict__ z, const float* __restrict__ eps,
                                 const float* __restrict__ v, double* __restrict__ ws) {
+  mf_pdl_enter();
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= Ni) return;
@@ -592,6 +601,7 @@ __global__ void nft_row_kernel(const int* __restrict__ img_seq, const int* __res
                                const float* __restrict__ z, const float* __restrict__ eps,
                                const float* __restrict__ vp, const float* __restrict__ vn,
                                double* __restrict__ ws) {
+  mf_pdl_enter();
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= Ni) return;
@@ -622,6 +632,7 @@ __global__ void nft_row_kernel(const int* __restrict__ img_seq, const int* __res
 __global__ void loss_seq_kernel(const int* __restrict__ cu_img, const int* __restrict__ img_target,
                                 int C, const double* __restrict__ ws, double* __restrict__ loss_sum,
                                 long long* __restrict__ count) {
+  mf_pdl_enter();
   __shared__ double sd[256];
   __shared__ long long sc[256];
   const int s = blockIdx.x;
@@ -650,6 +661,7 @@ __global__ void loss_seq_kernel(const int* __restrict__ cu_img, const int* __res
 
 __global__ void loss_mean_kernel(int S, const double* __restrict__ loss_sum,
                                  const long long* __restrict__ count, double* __restrict__ mean) {
+  mf_pdl_enter();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   double a = 0.0;
   long long n = 0;
@@ -661,6 +673,7 @@ __global__ void loss_mean_kernel(int S, const double* __restrict__ loss_sum,
 }
 
 __global__ void timeout_selftest_kernel(unsigned* status, unsigned long long limit_ns) {
+  mf_pdl_enter();
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -682,7 +695,7 @@ int grid_for(long long n, int threads) {
 cudaError_t launch_sinusoid(const float* t, int S, int F, float* out, cudaStream_t st) {
   const int n = S * (F / 2);
   if (n <= 0) return cudaSuccess;
-  sinusoid_kernel<<<(n + 255) / 256, 256, 0, st>>>(t, S, F, out);
+  launch_k(sinusoid_kernel, (n + 255) / 256, 256, 0, st, t, S, F, out);
   return cudaGetLastError();
 }
 
@@ -702,10 +715,10 @@ cudaError_t gemv_groups(GemvArgs g, int np, int K, int act, const float* x, floa
     switch (nch * 2 + (act == 1 ? 1 : 0)) {
 #define MF_GEMV_CASE(n)                                 \
   case 2 * n:                                          \
-    gemv_kernel<0, n><<<grid, 128, 0, st>>>(g);        \
+    launch_k(gemv_kernel<0, n>, grid, 128, 0, st, g);        \
     break;                                             \
   case 2 * n + 1:                                      \
-    gemv_kernel<1, n><<<grid, 128, 0, st>>>(g);        \
+    launch_k(gemv_kernel<1, n>, grid, 128, 0, st, g);        \
     break;
       MF_GEMV_CASE(1) MF_GEMV_CASE(2) MF_GEMV_CASE(3) MF_GEMV_CASE(4) MF_GEMV_CASE(5) MF_GEMV_CASE(6)
       MF_GEMV_CASE(7) MF_GEMV_CASE(8) MF_GEMV_CASE(9) MF_GEMV_CASE(10) MF_GEMV_CASE(11) MF_GEMV_CASE(12)
@@ -735,7 +748,7 @@ cudaError_t launch_gemv2(const bf16* W0, const bf16* b0, int y_off0, const bf16*
 cudaError_t launch_quantize_e4m3_rows(const bf16* x, int M, int K, uint8_t* q, float* s, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   if (K <= 0 || K % 16 != 0) return cudaErrorInvalidValue;
-  quantize_e4m3_rows_kernel<<<(M + 3) / 4, 128, 0, st>>>(x, M, K, q, s);
+  launch_k(quantize_e4m3_rows_kernel, (M + 3) / 4, 128, 0, st, x, M, K, q, s);
   return cudaGetLastError();
 }
 
@@ -748,7 +761,7 @@ cudaError_t launch_ln_modulate(const LnModArgs& a, cudaStream_t st) {
   const int blocks = std::min((a.rows + 3) / 4, 2 * sms);  // two resident blocks per SM
   switch (a.H / 256) {
 #define MF_LN_CASE(nv) \
-  case nv: ln_modulate_kernel<nv><<<blocks, 128, 0, st>>>(a); break;
+  case nv: launch_k(ln_modulate_kernel<nv>, blocks, 128, 0, st, a); break;
     MF_LN_CASE(1) MF_LN_CASE(2) MF_LN_CASE(3) MF_LN_CASE(4) MF_LN_CASE(5) MF_LN_CASE(6)
     MF_LN_CASE(7) MF_LN_CASE(8) MF_LN_CASE(9) MF_LN_CASE(10) MF_LN_CASE(11) MF_LN_CASE(12)
     MF_LN_CASE(13) MF_LN_CASE(14) MF_LN_CASE(15) MF_LN_CASE(16)
@@ -774,7 +787,7 @@ cudaError_t launch_ln_group_t(const LnModArgs& a, int sms, cudaStream_t st) {
   int per_cta = (a.rows + ctas - 1) / ctas;
   per_cta = (per_cta + 7) / 8 * 8;
   const int grid = (a.rows + per_cta - 1) / per_cta;
-  ln_group_kernel<kGiven, kMaxThreads><<<grid, a.H / 8, stages * stage_bytes, st>>>(a, per_cta, stages);
+  launch_k(ln_group_kernel<kGiven, kMaxThreads>, grid, a.H / 8, stages * stage_bytes, st, a, per_cta, stages);
   return cudaGetLastError();
 }
 
@@ -795,7 +808,7 @@ cudaError_t launch_interpolate(const int* img_seq, const int* img_target, const 
                                cudaStream_t st) {
   const long long n4 = (long long)Ni * C / 4;
   if (n4 <= 0) return cudaSuccess;
-  interpolate_kernel<<<grid_for(n4, 256), 256, 0, st>>>(img_seq, img_target, t, Ni, C, z, eps, zt,
+  launch_k(interpolate_kernel, grid_for(n4, 256), 256, 0, st, img_seq, img_target, t, Ni, C, z, eps, zt,
                                                         zt_bf16);
   return cudaGetLastError();
 }
@@ -804,7 +817,7 @@ cudaError_t launch_cfg(const int* img_seq, const int* seq_role, const int* img_p
                        float w, const float* v, float* out, cudaStream_t st) {
   const long long n4 = (long long)Ni * C / 4;
   if (n4 <= 0) return cudaSuccess;
-  cfg_kernel<<<grid_for(n4, 256), 256, 0, st>>>(img_seq, seq_role, img_pair, Ni, C, w, v, out);
+  launch_k(cfg_kernel, grid_for(n4, 256), 256, 0, st, img_seq, seq_role, img_pair, Ni, C, w, v, out);
   return cudaGetLastError();
 }
 
@@ -812,16 +825,16 @@ cudaError_t launch_euler(int Ni, int C, float dt, const float* v, float* z, bf16
                          cudaStream_t st) {
   const long long n4 = (long long)Ni * C / 4;
   if (n4 <= 0) return cudaSuccess;
-  euler_kernel<<<grid_for(n4, 256), 256, 0, st>>>(n4, dt, v, z, z_bf16);
+  launch_k(euler_kernel, grid_for(n4, 256), 256, 0, st, n4, dt, v, z, z_bf16);
   return cudaGetLastError();
 }
 
 cudaError_t launch_flow_loss(const int* cu_img, const int* img_target, int S, int Ni, int C,
                              const float* z, const float* eps, const float* v, double* ws,
                              double* loss_sum, long long* count, double* mean, cudaStream_t st) {
-  if (Ni > 0) loss_row_kernel<<<(Ni + 7) / 8, 256, 0, st>>>(img_target, Ni, C, z, eps, v, ws);
-  if (S > 0) loss_seq_kernel<<<S, 256, 0, st>>>(cu_img, img_target, C, ws, loss_sum, count);
-  loss_mean_kernel<<<1, 32, 0, st>>>(S, loss_sum, count, mean);
+  if (Ni > 0) launch_k(loss_row_kernel, (Ni + 7) / 8, 256, 0, st, img_target, Ni, C, z, eps, v, ws);
+  if (S > 0) launch_k(loss_seq_kernel, S, 256, 0, st, cu_img, img_target, C, ws, loss_sum, count);
+  launch_k(loss_mean_kernel, 1, 32, 0, st, S, loss_sum, count, mean);
   return cudaGetLastError();
 }
 
@@ -830,14 +843,14 @@ cudaError_t launch_nft_loss(const int* cu_img, const int* img_seq, const int* im
                             const float* eps, const float* vp, const float* vn, double* ws,
                             double* loss_sum, long long* count, double* mean, cudaStream_t st) {
   if (Ni > 0)
-    nft_row_kernel<<<(Ni + 7) / 8, 256, 0, st>>>(img_seq, img_target, reward, Ni, C, z, eps, vp, vn, ws);
-  if (S > 0) loss_seq_kernel<<<S, 256, 0, st>>>(cu_img, img_target, C, ws, loss_sum, count);
-  loss_mean_kernel<<<1, 32, 0, st>>>(S, loss_sum, count, mean);
+    launch_k(nft_row_kernel, (Ni + 7) / 8, 256, 0, st, img_seq, img_target, reward, Ni, C, z, eps, vp, vn, ws);
+  if (S > 0) launch_k(loss_seq_kernel, S, 256, 0, st, cu_img, img_target, C, ws, loss_sum, count);
+  launch_k(loss_mean_kernel, 1, 32, 0, st, S, loss_sum, count, mean);
   return cudaGetLastError();
 }
 
 cudaError_t launch_timeout_selftest(unsigned* status, unsigned long long limit_ns, cudaStream_t st) {
-  timeout_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  launch_k(timeout_selftest_kernel, 1, 32, 0, st, status, limit_ns);
   return cudaGetLastError();
 }
 
