@@ -13,7 +13,8 @@ STREAMS = ("txt", "img")
 
 
 def to_bf16(a, device="cuda") -> torch.Tensor:
-    """A float32 array whose values are bf16-representable, as a bf16 device tensor (exact)."""
+    """A float32 array as a bf16 device tensor, rounded to nearest even (exact when the values are
+    bf16-representable, as the seeded inputs are)."""
     t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
     return t.to(device=device).to(torch.bfloat16)
 
