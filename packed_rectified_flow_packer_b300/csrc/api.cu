@@ -355,16 +355,17 @@ mf_status run_gemm(const GemmSpec* specs, int nspec, int epi, int BN, mf::GemmPa
 }
 
 mf_status conditioning(const mf_plan* p, const mf_dims* d, const mf_temb_weights* tw,
-                       const float* t, float* sinus, float* h1, float* c, cudaStream_t st) {
+                       const float* t, float* sinus, float* h1, float* c, const DevInfo* di,
+                       cudaStream_t st) {
   const int S = p->S, H = d->hidden, F = d->freq_dim;
   const int groups = (S + 3) / 4;  // one GEMV launch per group of four samples
   Trace tr(MF_K_COND, st, 2.0 * S * ((double)F * H + (double)H * H), 2.0 * ((double)F * H + (double)H * H),
            1 + 2 * groups);
   MF_CUDA(mf::launch_sinusoid(t, S, F, sinus, st));
   MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(tw->w_t1), static_cast<const bf16*>(tw->b_t1),
-                          sinus, S, F, H, h1, H, 0, 1, st));
+                          sinus, S, F, H, h1, H, 0, 1, di->status, wait_limit_ns(), st));
   MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(tw->w_t2), static_cast<const bf16*>(tw->b_t2), h1,
-                          S, H, H, c, H, 0, 1, st));
+                          S, H, H, c, H, 0, 1, di->status, wait_limit_ns(), st));
   return MF_OK;
 }
 
@@ -592,13 +593,13 @@ mf_status block_forward(const mf_plan* p, const mf_dims* d, const mf_block_weigh
   };
 
   // 1. timestep condition c = SiLU(temb(t)) and the per-sample adaLN modulation of both streams
-  if (!(flags & MF_BLOCK_COND_GIVEN)) MF_TRY(conditioning(p, d, &w->temb, t, sinus, h1, c, st));
+  if (!(flags & MF_BLOCK_COND_GIVEN)) MF_TRY(conditioning(p, d, &w->temb, t, sinus, h1, c, di, st));
   {
     // both streams' modulation GEMVs share c and run as one launch per group of four samples
     Trace tr(MF_K_COND, st, 2.0 * 2 * S * 6.0 * H * H, 2.0 * 2 * 6.0 * H * H, (S + 3) / 4);
     MF_CUDA(mf::launch_gemv2(static_cast<const bf16*>(w->txt.w_mod), static_cast<const bf16*>(w->txt.b_mod), 0,
                              static_cast<const bf16*>(w->img.w_mod), static_cast<const bf16*>(w->img.b_mod),
-                             6 * H, c, S, H, 6 * H, mod, 12 * H, st));
+                             6 * H, c, S, H, 6 * H, mod, 12 * H, di->status, wait_limit_ns(), st));
   }
 
   // 2. a = LN(x)(1 + scale1) + shift1, stream-sorted
@@ -1104,11 +1105,11 @@ extern "C" mf_status mf_final(const mf_plan* p, const mf_dims* d, const mf_temb_
   float* fmod = reinterpret_cast<float*>(ws + L.fmod);
   bf16* a = reinterpret_cast<bf16*>(ws + L.a);
   MF_TRY(conditioning(p, d, temb, t, reinterpret_cast<float*>(ws + L.sinus),
-                      reinterpret_cast<float*>(ws + L.h1), c, st));
+                      reinterpret_cast<float*>(ws + L.h1), c, di, st));
   {
     Trace tr(MF_K_COND, st, 2.0 * S * 2.0 * H * H, 2.0 * 2.0 * H * H, (S + 3) / 4);
     MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w_fmod), static_cast<const bf16*>(b_fmod), c, S, H,
-                            2 * H, fmod, 2 * H, 0, 0, st));
+                            2 * H, fmod, 2 * H, 0, 0, di->status, wait_limit_ns(), st));
   }
   mf::LnModArgs ln{static_cast<const bf16*>(d_x_img), nullptr, p->Ni, p->Ni, H,
                    p->d_srow_seq + p->Nt, fmod, 2LL * H, 0, 0, H, a, p->S, nullptr, di->status,

@@ -86,6 +86,8 @@ struct GemvArgs {
   int S, O;
   float* y;
   int y_stride;
+  unsigned* status;                 // bulk kernel: bounded waits report here
+  unsigned long long wait_limit_ns;
 };
 
 template <int ACT, int NCH>
@@ -146,6 +148,119 @@ __global__ void __launch_bounds__(128) gemv_kernel(const GemvArgs g) {
         y[(size_t)si * g.y_stride + r] = ACT == 1 ? silu_f(t) : t;
       }
     }
+  }
+}
+
+// The same product for wide K (the H x H and 6H x H matrices): groups of kBulkRows rows are
+// staged in shared memory by bulk copies (one per 2K-byte row), two groups per CTA in flight and
+// two CTAs per SM, so the weight stream keeps HBM busy without holding the bytes in registers.
+// The four warps split a group's K chunks (chunk i to warp i mod 4) over all its rows, so each
+// chunk of x is read once per group from L1 for kBulkRows rows; the per-warp partial sums meet
+// in shared memory.  CTAs take groups blockIdx.x, blockIdx.x + gridDim.x, ...
+constexpr int kBulkRows = 8;
+
+template <int ACT, int NCH>
+__global__ void __launch_bounds__(128, 2) gemv_bulk_kernel(const GemvArgs g, int n_groups) {
+  mf_pdl_enter();
+  constexpr int K = NCH * 256;
+  constexpr uint32_t kRowBytes = K * 2, kStage = kBulkRows * kRowBytes;
+  extern __shared__ __align__(128) uint8_t gsm[];
+  __shared__ uint64_t full_bar[2];
+  __shared__ float part[2][4][kBulkRows][4];  // [group parity][warp][row][sample]
+  __shared__ int abort_sh;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int pb = blockIdx.y;
+  const bf16* W = pb ? g.W[1] : g.W[0];
+  const bf16* bias = pb ? g.b[1] : g.b[0];
+  float* y = g.y + (pb ? g.y_off[1] : g.y_off[0]);
+  const int O = g.O, S = g.S;
+  if ((int)blockIdx.x >= n_groups) return;
+  if (t == 0) {
+    mbar_init(&full_bar[0], 1);
+    mbar_init(&full_bar[1], 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  int issued = 0;  // thread 0: groups of this CTA whose copies have been issued
+  auto issue = [&](int gi, int s) {
+    const int o0 = gi * kBulkRows, nr = min(kBulkRows, O - o0);
+    mbar_arrive_expect_tx(&full_bar[s], nr * kRowBytes);
+    for (int r = 0; r < nr; ++r)
+      bulk_load(gsm + s * kStage + r * kRowBytes, W + (size_t)(o0 + r) * K, kRowBytes, &full_bar[s]);
+    ++issued;
+  };
+  if (t == 0) {
+    issue(blockIdx.x, 0);
+    if ((int)(blockIdx.x + gridDim.x) < n_groups) issue(blockIdx.x + gridDim.x, 1);
+  }
+  int it = 0;
+  for (int gi = blockIdx.x; gi < n_groups; gi += gridDim.x, ++it) {
+    const int s = it & 1;
+    const int o0 = gi * kBulkRows, nr = min(kBulkRows, O - o0);
+    if (!mbar_wait(&full_bar[s], (uint32_t)(it >> 1) & 1u, g.wait_limit_ns)) {
+      report_status(g.status, kStatusTimeout);
+      abort_sh = 1;
+    }
+    const uint8_t* buf = gsm + s * kStage;
+    float acc[kBulkRows][4][2];
+#pragma unroll
+    for (int r = 0; r < kBulkRows; ++r)
+#pragma unroll
+      for (int si = 0; si < 4; ++si) acc[r][si][0] = acc[r][si][1] = 0.f;
+#pragma unroll
+    for (int i0 = 0; i0 < NCH; i0 += 4) {
+      const int i = i0 + warp;
+      if (i < NCH) {
+        const int k = lane * 8 + 256 * i;
+        float xv[4][8];
+#pragma unroll
+        for (int si = 0; si < 4; ++si) {
+          const float4* xp = reinterpret_cast<const float4*>(g.x + (size_t)min(si, S - 1) * K + k);
+          const float4 a = __ldg(xp), c = __ldg(xp + 1);
+          xv[si][0] = a.x; xv[si][1] = a.y; xv[si][2] = a.z; xv[si][3] = a.w;
+          xv[si][4] = c.x; xv[si][5] = c.y; xv[si][6] = c.z; xv[si][7] = c.w;
+        }
+#pragma unroll
+        for (int r = 0; r < kBulkRows; ++r) {
+          // rows past nr hold stale shared memory; their sums are never stored
+          const uint4 wq = *reinterpret_cast<const uint4*>(buf + r * kRowBytes + k * 2);
+          float wf[8];
+          unpack8(wq, wf);
+#pragma unroll
+          for (int si = 0; si < 4; ++si)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              ffma2(acc[r][si][0], acc[r][si][1], wf[2 * j], wf[2 * j + 1], xv[si][2 * j], xv[si][2 * j + 1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kBulkRows; ++r)
+#pragma unroll
+      for (int si = 0; si < 4; ++si) {
+        const float v = warp_sum(acc[r][si][0] + acc[r][si][1]);
+        if (lane == 0) part[it & 1][warp][r][si] = v;
+      }
+    __syncthreads();
+    if (abort_sh) break;
+    // every thread is done with stage s: it takes the group two steps ahead
+    if (t == 0 && gi + 2 * (int)gridDim.x < n_groups) {
+      fence_proxy_async_smem();
+      issue(gi + 2 * gridDim.x, s);
+    }
+    if (t < kBulkRows * 4) {
+      const int r = t >> 2, si = t & 3;
+      if (r < nr && si < S) {
+        const float v = part[it & 1][0][r][si] + part[it & 1][1][r][si] + part[it & 1][2][r][si] +
+                        part[it & 1][3][r][si] + (bias ? __bfloat162float(bias[o0 + r]) : 0.0f);
+        y[(size_t)si * g.y_stride + o0 + r] = ACT == 1 ? silu_f(v) : v;
+      }
+    }
+  }
+  if (t == 0 && abort_sh) {
+    // stopped early: let the copies still in flight land before the CTA's shared memory goes
+    for (int j = it; j < issued; ++j) (void)mbar_wait(&full_bar[j & 1], (uint32_t)(j >> 1) & 1u, g.wait_limit_ns);
   }
 }
 
@@ -708,6 +823,41 @@ cudaError_t gemv_groups(GemvArgs g, int np, int K, int act, const float* x, floa
   const int warps = (g.O + kGemvRows - 1) / kGemvRows;
   const dim3 grid((warps + 3) / 4, np);
   const int nch = K % 256 == 0 ? K / 256 : 0;
+  if (nch >= 4 && nch <= 16) {  // wide K: the bulk-copy kernel
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int n_groups = (g.O + kBulkRows - 1) / kBulkRows;
+    const int per_problem = std::max(1, std::min(n_groups, 2 * sms / np));
+    const dim3 bgrid(per_problem, np);
+    const size_t smem = 2 * (size_t)kBulkRows * K * 2;
+    for (int s0 = 0; s0 < S; s0 += 4) {
+      g.S = S - s0 < 4 ? S - s0 : 4;
+      g.x = x + (size_t)s0 * K;
+      g.y = y + (size_t)s0 * g.y_stride;
+      switch (nch * 2 + (act == 1 ? 1 : 0)) {
+#define MF_GEMV_BULK_CASE(n)                                                                           \
+  case 2 * n:                                                                                         \
+    e = cudaFuncSetAttribute(gemv_bulk_kernel<0, n>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    if (e == cudaSuccess) e = launch_k(gemv_bulk_kernel<0, n>, bgrid, 128, smem, st, g, n_groups);   \
+    break;                                                                                            \
+  case 2 * n + 1:                                                                                     \
+    e = cudaFuncSetAttribute(gemv_bulk_kernel<1, n>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    if (e == cudaSuccess) e = launch_k(gemv_bulk_kernel<1, n>, bgrid, 128, smem, st, g, n_groups);   \
+    break;
+        MF_GEMV_BULK_CASE(4) MF_GEMV_BULK_CASE(5) MF_GEMV_BULK_CASE(6) MF_GEMV_BULK_CASE(7)
+        MF_GEMV_BULK_CASE(8) MF_GEMV_BULK_CASE(9) MF_GEMV_BULK_CASE(10) MF_GEMV_BULK_CASE(11)
+        MF_GEMV_BULK_CASE(12) MF_GEMV_BULK_CASE(13) MF_GEMV_BULK_CASE(14) MF_GEMV_BULK_CASE(15)
+        MF_GEMV_BULK_CASE(16)
+#undef MF_GEMV_BULK_CASE
+        default: return cudaErrorInvalidValue;
+      }
+      if (e != cudaSuccess) return e;
+      if (launches) ++*launches;
+    }
+    return cudaGetLastError();
+  }
   for (int s0 = 0; s0 < S; s0 += 4) {
     g.S = S - s0 < 4 ? S - s0 : 4;
     g.x = x + (size_t)s0 * K;
@@ -733,15 +883,16 @@ cudaError_t gemv_groups(GemvArgs g, int np, int K, int act, const float* x, floa
 }  // namespace
 
 cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int K, int O, float* y,
-                        int y_stride, int y_off, int act, cudaStream_t st, int* launches) {
-  GemvArgs g{{W, W}, {b, b}, {y_off, y_off}, x, 0, O, y, y_stride};
+                        int y_stride, int y_off, int act, unsigned* status, unsigned long long wait_limit_ns,
+                        cudaStream_t st, int* launches) {
+  GemvArgs g{{W, W}, {b, b}, {y_off, y_off}, x, 0, O, y, y_stride, status, wait_limit_ns};
   return gemv_groups(g, 1, K, act, x, y, S, st, launches);
 }
 
 cudaError_t launch_gemv2(const bf16* W0, const bf16* b0, int y_off0, const bf16* W1, const bf16* b1,
                          int y_off1, const float* x, int S, int K, int O, float* y, int y_stride,
-                         cudaStream_t st, int* launches) {
-  GemvArgs g{{W0, W1}, {b0, b1}, {y_off0, y_off1}, x, 0, O, y, y_stride};
+                         unsigned* status, unsigned long long wait_limit_ns, cudaStream_t st, int* launches) {
+  GemvArgs g{{W0, W1}, {b0, b1}, {y_off0, y_off1}, x, 0, O, y, y_stride, status, wait_limit_ns};
   return gemv_groups(g, 2, K, 0, x, y, S, st, launches);
 }
 

@@ -11,15 +11,17 @@ cudaError_t launch_sinusoid(const float* t, int S, int F, float* out, cudaStream
 // y[s][y_off + o] = act(W[o] . x[s] + b[o]) for o < O, W bf16 [O][K], x f32 [S][K];
 // act 0 = identity, 1 = SiLU.  K multiple of 256, at most 4096.  *launches (if not null)
 // receives the number of kernels launched (one per group of four samples).
+// Wide K (at least 1024) runs a kernel with bounded waits, which report to *status.
 cudaError_t launch_gemv(const bf16* W, const bf16* b, const float* x, int S, int K, int O,
-                        float* y, int y_stride, int y_off, int act, cudaStream_t st,
-                        int* launches = nullptr);
+                        float* y, int y_stride, int y_off, int act, unsigned* status,
+                        unsigned long long wait_limit_ns, cudaStream_t st, int* launches = nullptr);
 
 // Two GEMVs with the same x, K and O in one launch per group of four samples:
 // y[s][y_off_p + o] = W_p[o] . x[s] + b_p[o] for p = 0, 1 (no activation).
 cudaError_t launch_gemv2(const bf16* W0, const bf16* b0, int y_off0, const bf16* W1, const bf16* b1,
                          int y_off1, const float* x, int S, int K, int O, float* y, int y_stride,
-                         cudaStream_t st, int* launches = nullptr);
+                         unsigned* status, unsigned long long wait_limit_ns, cudaStream_t st,
+                         int* launches = nullptr);
 
 // Per-row E4M3 quantisation of x bf16 [M][K] (K multiple of 16): s[r] = amax(|x[r]|) / 448
 // (1 for an all-zero row), q[r][k] = E4M3(x[r][k] / s[r]) with the division correctly rounded

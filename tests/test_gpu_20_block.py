@@ -112,6 +112,36 @@ def test_tiny_block_and_intermediates():
     assert_update_close(got_i, xi_ref, emb, "block update img")
 
 
+def test_wide_conditioning_intermediates():
+    """H = 1024 (the conditioning GEMVs take the bulk-copy kernel from K = 1024 on) with six
+    samples (two launches of at most four samples each): the timestep condition c and both
+    streams' modulation rows left in the workspace, and the block output, against the oracle."""
+    d = synth.Dims(hidden=1024, heads=8, channels=64)
+    samples = [synth.Sample(5 + 7 * i, 1, 3 + i, 4, 0.1 + 0.15 * i) for i in range(6)]
+    case = Case(samples, d, 1, seed=5)
+    ref, H = case.ref, d.hidden
+    g = np.random.default_rng(12)
+    xi0 = synth.round_bf16(g.standard_normal((ref.n_img, H)).astype(np.float32))
+    xt = to_bf16(case.x_txt_np)
+    xi = to_bf16(xi0)
+    x_txt0 = _f(xt)
+    mf.mf_block_forward(case.plan, case.model.dims, case.model.block_structs[0], None, xt, xi, case.ws.block)
+    mf.mf_check()
+    off = mf.mf_block_workspace_layout(case.plan, case.model.dims)
+    S = ref.n_seq
+    wsb = case.ws.block
+    cg = wsb[off[0]:off[0] + S * H * 4].view(torch.float32).cpu().numpy().reshape(S, H)
+    mg = wsb[off[1]:off[1] + S * 12 * H * 4].view(torch.float32).cpu().numpy().reshape(S, 2, 6 * H)
+    for k in range(S):
+        it = _block_intermediates(case, x_txt0, xi0, k)
+        assert_close(cg[k], it["c"], f"c[{k}]")
+        assert_close(mg[k, 0], it["mod_txt"], f"mod_txt[{k}]")
+        assert_close(mg[k, 1], it["mod_img"], f"mod_img[{k}]")
+    xt_ref, xi_ref, _ = oracle_stack(case.samples, ref, case.w, case.batch, d.heads, x_img_in=xi0, n_blocks=1)
+    assert_close(_f(xt)[:ref.n_txt], xt_ref, "block x_txt")
+    assert_close(_f(xi), xi_ref, "block x_img")
+
+
 def _stack_and_loss(case, n_blocks, round_zt=True):
     d, ref = case.dims, case.ref
     H, C = d.hidden, d.channels
