@@ -223,6 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           tma_load_2d(sp + a * kQTAtom, &p.tmQ, h * Dr + a * 64, kv0 + i * kQT, &full[st]);
           tma_load_2d(sp + kQTBytes + a * kQTAtom, &p.tmDO, h * Dr + a * 64, kv0 + i * kQT, &full[st]);
         }
+        // the next tile into L2 while its stage is still in use, so its load starts from L2
+        if (i + 1 < n_q)
+          for (int a = 0; a < natoms; ++a) {
+            tma_prefetch_l2_2d(&p.tmQ, h * Dr + a * 64, kv0 + (i + 1) * kQT);
+            tma_prefetch_l2_2d(&p.tmDO, h * Dr + a * 64, kv0 + (i + 1) * kQT);
+          }
       }
       armed |= 1u << st;
       armed_par = (armed_par & ~(1u << st)) | (ph << st);
@@ -313,13 +319,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       tc_fence_after();
       mma_group_ss<4>(el, tmem_base + kColDK, sdesc_sw128(ds_addr, 16, 1024), kStepK,
                       sdesc_sw128(q_addr, kQTAtom, 1024), kStepMN, IDESC_KV, i > 0 ? 1u : 0u);
+      // dK_i is the stage's last reader (S_i, dP_i, dV_i before it; lse / delta were read before
+      // dS_i was released): the producer may refill it while dQ_i waits and runs
+      mma_commit_if(el, &empty[st]);
       if (i >= 1 && !wait_all(&dq_free, (i - 1) & 1)) { ok = false; break; }
       tc_fence_after();
       mma_group_ss<8>(el, tmem_base + kColDQ, k_desc_mn, kStepMN, sdesc_sw128(ds_addr, kKVAtom, 1024), kStepMN,
                       IDESC_DQ, 0u);
       mma_commit_if(el, &dq_full);
       mma_commit_if(el, &ds_free[b]);
-      mma_commit_if(el, &empty[st]);
       // S_{i+2} into buffer b (its P_i was read by the dV above)
       if (i + 2 < n_q) {
         if (!stage_wait(i + 2)) { ok = false; break; }

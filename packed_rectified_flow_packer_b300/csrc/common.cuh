@@ -198,6 +198,15 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* t
       : "memory");
 }
 
+// L2 prefetch of one 2-D box (no shared memory, no completion): warms L2 for a later tile load.
+// The same alignment rule as a load applies to x.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // 2-D tiled store of one box from shared memory (bulk-group completion).  The shared-memory
 // data must be made visible to the async proxy first (fence_proxy_async_smem by the writers).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int x, int y, const void* smem_src) {
