@@ -218,7 +218,7 @@ def _part_stats(x):
     return m, ((r - m[..., None]) ** 2).sum(axis=2)
 
 
-@pytest.mark.parametrize("size", ["tiny", "mid"])
+@pytest.mark.parametrize("size", ["tiny", "mid", "wide"])
 def test_ln_variants(size):
     """The LN + modulate variants of mf_block_forward_ex - one warp per row (the default), row
     groups, and the second LN's statistics fused into the out-projection's epilogue - each match the
@@ -227,8 +227,11 @@ def test_ln_variants(size):
     the GPU's own attention output o."""
     if size == "tiny":
         case = Case(synth.tiny_samples(), synth.TINY, 1, seed=3)
-    else:
+    elif size == "mid":
         case = Case(_mid_samples(7), MID, 1, seed=17)
+    else:  # the widest supported hidden size: 512-thread row kernels, three shared-memory stages
+        case = Case([synth.Sample(19, 1, 3, 5, 0.3), synth.Sample(0, 2, 4, 3, 0.8)],
+                    synth.Dims(hidden=4096, heads=32, channels=64), 1, seed=23)
     d, ref = case.dims, case.ref
     H = d.hidden
     g = np.random.default_rng(40)

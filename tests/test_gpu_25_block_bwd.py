@@ -105,3 +105,12 @@ def test_mid_pack_block_backward(seed):
     """Ragged H = 512 packs: GEMM row tiles with tails, edit samples (two frames), text lengths
     from 0, row chunks that end inside a sample."""
     _run_case(_mid_samples(seed + 40), MID, seed=seed + 50)
+
+
+@pytest.mark.slow
+def test_wide_block_backward():
+    """H = 4096 (32 heads x 128), the widest supported hidden size: the 512-thread row kernels
+    and the widest statistics and GEMV instantiations; one text + image sample and one
+    two-frame edit sample without text."""
+    samples = [synth.Sample(13, 1, 3, 4, 0.4), synth.Sample(0, 2, 3, 3, 0.7)]
+    _run_case(samples, synth.Dims(hidden=4096, heads=32, channels=64), seed=61)
