@@ -218,7 +218,7 @@ def _part_stats(x):
     return m, ((r - m[..., None]) ** 2).sum(axis=2)
 
 
-@pytest.mark.parametrize("size", ["tiny", "mid", "wide"])
+@pytest.mark.parametrize("size", ["tiny", "mid", "h768", "wide"])
 def test_ln_variants(size):
     """The LN + modulate variants of mf_block_forward_ex - one warp per row (the default), row
     groups, and the second LN's statistics fused into the out-projection's epilogue - each match the
@@ -229,6 +229,8 @@ def test_ln_variants(size):
         case = Case(synth.tiny_samples(), synth.TINY, 1, seed=3)
     elif size == "mid":
         case = Case(_mid_samples(7), MID, 1, seed=17)
+    elif size == "h768":  # 6 heads x 128: an N tile count (3) that leaves a ragged last column
+        case = Case(_mid_samples(9), synth.Dims(hidden=768, heads=6, channels=64), 1, seed=29)
     else:  # the widest supported hidden size: 512-thread row kernels, three shared-memory stages
         case = Case([synth.Sample(19, 1, 3, 5, 0.3), synth.Sample(0, 2, 4, 3, 0.8)],
                     synth.Dims(hidden=4096, heads=32, channels=64), 1, seed=23)

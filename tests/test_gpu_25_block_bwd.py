@@ -107,6 +107,12 @@ def test_mid_pack_block_backward(seed):
     _run_case(_mid_samples(seed + 40), MID, seed=seed + 50)
 
 
+def test_h768_block_backward():
+    """H = 768 (6 heads x 128): hidden sizes that are not a power of two, 3 N tiles of 256 in
+    the H-wide products and 12 in the MLP."""
+    _run_case(_mid_samples(70), synth.Dims(hidden=768, heads=6, channels=64), seed=71)
+
+
 @pytest.mark.slow
 def test_wide_block_backward():
     """H = 4096 (32 heads x 128), the widest supported hidden size: the 512-thread row kernels
