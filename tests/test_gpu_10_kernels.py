@@ -31,8 +31,10 @@ def test_bounded_wait_reports_timeout():
     assert float((x * 2).sum()) == 8.0
 
 
+# the last two give 78 and 75 tiles of 256 x 256: more than one wave on 74 co-resident CTA
+# pairs, with a nearly empty last wave (in the second, N = 640 ends inside the last tile)
 GEMM_SHAPES = [(1, 64, 64), (100, 128, 64), (128, 256, 128), (129, 384, 256), (300, 512, 1024),
-               (1000, 96, 192), (257, 256, 3072)]
+               (1000, 96, 192), (257, 256, 3072), (6656, 768, 256), (6400, 640, 128)]
 
 
 @pytest.mark.parametrize("M_,N_,K_", GEMM_SHAPES)
