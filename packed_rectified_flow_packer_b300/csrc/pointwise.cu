@@ -682,7 +682,34 @@ __global__ void euler_kernel(long long n4, float dt, const float* __restrict__ v
   }
 }
 
-// per image row: sum over channels of (v - (z - eps))^2 in f64 (0 for source-frame rows)
+// Exact f32 building blocks for the loss rows (the FP64 pipe of this GPU is far narrower than
+// its f32 pipe): Knuth's TwoSum (s + t = a + b exactly) and, with an FMA, the exact square
+// (p + e = x * x).  A row's sum is carried as an unevaluated pair hi + lo of f32 values.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& t) {
+  s = a + b;
+  const float bb = s - a;
+  t = (a - (s - bb)) + (b - bb);
+}
+
+// hi + lo += d^2 for d = u - (a - e): a - e = s + t and u - s = s2 + t2 exactly, so
+// d = s2 + (t2 - t) with the second term rounded once (to 2^-24 of itself); s2^2 is split
+// exactly and the cross and square terms of the small part are added with FMAs.
+__device__ __forceinline__ void acc_sq_diff(float u, float a, float e, float& hi, float& lo) {
+  float s, t, s2, t2;
+  two_sum(a, -e, s, t);
+  two_sum(u, -s, s2, t2);
+  const float dl = t2 - t;
+  const float p = s2 * s2;
+  const float pe = fmaf(s2, s2, -p);
+  const float c = fmaf(dl, dl, fmaf(2.0f * s2, dl, pe));
+  float h, ht;
+  two_sum(hi, p, h, ht);
+  hi = h;
+  lo += ht + c;
+}
+
+// per image row: sum over channels of (v - (z - eps))^2 (0 for source-frame rows), one warp per
+// row, carried to within about 2^-44 of the row sum and stored as an f64
 __global__ void loss_row_kernel(const int* __restrict__ img_target, int Ni, int C,
                                 const float* __restrict__ z, const float* __restrict__ eps,
                                 const float* __restrict__ v, double* __restrict__ ws) {
@@ -690,22 +717,28 @@ __global__ void loss_row_kernel(const int* __restrict__ img_target, int Ni, int 
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= Ni) return;
-  double acc = 0.0;
+  float hi = 0.0f, lo = 0.0f;
   if (__ldg(img_target + r)) {
     const size_t base = (size_t)r * C;
     for (int c = lane * 4; c < C; c += 128) {
       const float4 a = *reinterpret_cast<const float4*>(z + base + c);
       const float4 e = *reinterpret_cast<const float4*>(eps + base + c);
       const float4 u = *reinterpret_cast<const float4*>(v + base + c);
-      const double d0 = (double)u.x - ((double)a.x - (double)e.x);
-      const double d1 = (double)u.y - ((double)a.y - (double)e.y);
-      const double d2 = (double)u.z - ((double)a.z - (double)e.z);
-      const double d3 = (double)u.w - ((double)a.w - (double)e.w);
-      acc += d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3;
+      acc_sq_diff(u.x, a.x, e.x, hi, lo);
+      acc_sq_diff(u.y, a.y, e.y, hi, lo);
+      acc_sq_diff(u.z, a.z, e.z, hi, lo);
+      acc_sq_diff(u.w, a.w, e.w, hi, lo);
     }
   }
-  acc = warp_sum_d(acc);
-  if (lane == 0) ws[r] = acc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ho = __shfl_xor_sync(0xffffffffu, hi, o), lo2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    float h, t;
+    two_sum(hi, ho, h, t);
+    hi = h;
+    lo += lo2 + t;
+  }
+  if (lane == 0) ws[r] = (double)hi + (double)lo;
 }
 
 // Diffusion-NFT objective, per image row: sum over channels of
@@ -743,22 +776,31 @@ __global__ void nft_row_kernel(const int* __restrict__ img_seq, const int* __res
   if (lane == 0) ws[r] = acc;
 }
 
-// one block per sample, fixed reduction order
+// one block of 1024 threads per sample (four rows in flight each), fixed reduction order
 __global__ void loss_seq_kernel(const int* __restrict__ cu_img, const int* __restrict__ img_target,
                                 int C, const double* __restrict__ ws, double* __restrict__ loss_sum,
                                 long long* __restrict__ count) {
   mf_pdl_enter();
-  __shared__ double sd[256];
-  __shared__ long long sc[256];
+  __shared__ double sd[1024];
+  __shared__ long long sc[1024];
   const int s = blockIdx.x;
   const int lo = cu_img[s], hi = cu_img[s + 1];
-  double a = 0.0;
+  const int bd = blockDim.x;
+  double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;  // four loads in flight per step
   long long n = 0;
-  for (int r = lo + threadIdx.x; r < hi; r += blockDim.x) {
-    a += ws[r];
+  int r = lo + threadIdx.x;
+  for (; r + 3 * bd < hi; r += 4 * bd) {
+    a0 += ws[r];
+    a1 += ws[r + bd];
+    a2 += ws[r + 2 * bd];
+    a3 += ws[r + 3 * bd];
+    n += img_target[r] + img_target[r + bd] + img_target[r + 2 * bd] + img_target[r + 3 * bd];
+  }
+  for (; r < hi; r += bd) {
+    a0 += ws[r];
     n += img_target[r];
   }
-  sd[threadIdx.x] = a;
+  sd[threadIdx.x] = (a0 + a1) + (a2 + a3);
   sc[threadIdx.x] = n;
   __syncthreads();
   for (int o = blockDim.x / 2; o > 0; o >>= 1) {
@@ -984,7 +1026,7 @@ cudaError_t launch_flow_loss(const int* cu_img, const int* img_target, int S, in
                              const float* z, const float* eps, const float* v, double* ws,
                              double* loss_sum, long long* count, double* mean, cudaStream_t st) {
   if (Ni > 0) launch_k(loss_row_kernel, (Ni + 7) / 8, 256, 0, st, img_target, Ni, C, z, eps, v, ws);
-  if (S > 0) launch_k(loss_seq_kernel, S, 256, 0, st, cu_img, img_target, C, ws, loss_sum, count);
+  if (S > 0) launch_k(loss_seq_kernel, S, 1024, 0, st, cu_img, img_target, C, ws, loss_sum, count);
   launch_k(loss_mean_kernel, 1, 32, 0, st, S, loss_sum, count, mean);
   return cudaGetLastError();
 }
@@ -995,7 +1037,7 @@ cudaError_t launch_nft_loss(const int* cu_img, const int* img_seq, const int* im
                             double* loss_sum, long long* count, double* mean, cudaStream_t st) {
   if (Ni > 0)
     launch_k(nft_row_kernel, (Ni + 7) / 8, 256, 0, st, img_seq, img_target, reward, Ni, C, z, eps, vp, vn, ws);
-  if (S > 0) launch_k(loss_seq_kernel, S, 256, 0, st, cu_img, img_target, C, ws, loss_sum, count);
+  if (S > 0) launch_k(loss_seq_kernel, S, 1024, 0, st, cu_img, img_target, C, ws, loss_sum, count);
   launch_k(loss_mean_kernel, 1, 32, 0, st, S, loss_sum, count, mean);
   return cudaGetLastError();
 }
