@@ -285,8 +285,9 @@ def run_mageflow(args, rank, world, local_rank):
         mf.mf_block_forward(plan, d, blk, None, x_txt, x_img, ws_block)
         if timed_block is not None:
             timed_block[1].record(stream)
-        mf.mf_final(plan, d, model.temb_struct, fin["w_fmod"], fin["b_fmod"], fin["w_out"], fin["b_out"],
-                    None, x_img, v, ws_final)
+        # the final layer reuses the timestep condition the block left at offset 0 of its workspace
+        mf.mf_final_ex(plan, d, model.temb_struct, fin["w_fmod"], fin["b_fmod"], fin["w_out"], fin["b_out"],
+                       None, x_img, v, ws_final, ws_block)
         mf.mf_flow_loss(plan, C, p["z"], p["eps"], v, ls, cnt, mean, ws_loss)
 
     def barrier():
@@ -405,8 +406,8 @@ def run_mageflow(args, rank, world, local_rank):
             mf.mf_interpolate(plan, C, None, b["z"], b["e"], None, ztb)
             mf.mf_embed(plan, d, emb["w_in"], emb["b_in"], ztb, x_img)
             mf.mf_block_forward(plan, d, blk, None, b["x"], x_img, ws_block)
-            mf.mf_final(plan, d, model.temb_struct, fin["w_fmod"], fin["b_fmod"], fin["w_out"], fin["b_out"],
-                        None, x_img, v, ws_final)
+            mf.mf_final_ex(plan, d, model.temb_struct, fin["w_fmod"], fin["b_fmod"], fin["w_out"], fin["b_out"],
+                           None, x_img, v, ws_final, ws_block)
             mf.mf_flow_loss(plan, C, b["z"], b["e"], v, ls, cnt, mean, ws_loss)
             S = plan.n_seq
             ho = host_out[slot]

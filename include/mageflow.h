@@ -372,6 +372,15 @@ mf_status mf_final(const mf_plan* plan, const mf_dims* dims, const mf_temb_weigh
                    const float* d_t, const void* d_x_img, float* d_v, void* d_ws,
                    size_t ws_bytes, void* stream);
 
+/* mf_final with the timestep condition given: d_c, device f32 [S][H] (16-byte aligned), holds
+ * c_s = SiLU(temb(t_s)) of this plan's samples for the same t and timestep weights, as a block
+ * call leaves it at offset [0] of its workspace (mf_block_workspace_layout); the timestep MLP is
+ * skipped.  d_c NULL behaves as mf_final.  Errors: as mf_final. */
+mf_status mf_final_ex(const mf_plan* plan, const mf_dims* dims, const mf_temb_weights* temb,
+                      const void* w_fmod, const void* b_fmod, const void* w_out, const void* b_out,
+                      const float* d_t, const void* d_x_img, float* d_v, void* d_ws, size_t ws_bytes,
+                      const float* d_c, void* stream);
+
 /* ------------------------------------------------------------------------------------ */
 /* Rectified-flow epilogues  [PR 2.2(2)], [PR 2.2(3)], [PR 5], [HA M], [HA E]            */
 /* ------------------------------------------------------------------------------------ */

@@ -13,7 +13,7 @@ import os
 
 import numpy as np
 
-__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_block_forward_ex", "BLOCK_LN_ROW_GROUPS", "BLOCK_LN_STATS_FUSED", "BLOCK_COND_GIVEN", "mf_block_train_workspace_bytes", "mf_block_forward_train", "mf_block_backward_workspace_bytes", "mf_block_backward", "grads_struct", "mf_stream_grads", "mf_block_grads", "GRAD_FIELDS", "mf_block_fp8_workspace_bytes", "mf_block_forward_fp8", "block_struct_fp8", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_attention_lse", "mf_attention_backward_workspace_bytes", "mf_attention_backward", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
+__all__ = ["MageflowError", "mf_sample", "mf_plan_info", "mf_dims", "mf_temb_weights", "mf_stream_weights", "mf_block_weights", "temb_struct", "block_struct", "Plan", "samples_struct", "mf_pack", "mf_pack_status", "mf_plan_upload", "mf_block_workspace_bytes", "mf_block_workspace_layout", "mf_block_forward", "mf_block_forward_ex", "BLOCK_LN_ROW_GROUPS", "BLOCK_LN_STATS_FUSED", "BLOCK_COND_GIVEN", "mf_block_train_workspace_bytes", "mf_block_forward_train", "mf_block_backward_workspace_bytes", "mf_block_backward", "grads_struct", "mf_stream_grads", "mf_block_grads", "GRAD_FIELDS", "mf_block_fp8_workspace_bytes", "mf_block_forward_fp8", "block_struct_fp8", "mf_stream_weights_fp8", "mf_block_weights_fp8", "mf_embed", "mf_final_workspace_bytes", "mf_final", "mf_final_ex", "mf_interpolate", "mf_cfg_combine", "mf_euler_step", "mf_flow_loss_workspace_bytes", "mf_flow_loss", "mf_flow_loss_noalloc", "NOALLOC_MAX_IMG_ROWS", "mf_nft_loss", "mf_attention", "mf_attention_lse", "mf_attention_backward_workspace_bytes", "mf_attention_backward", "mf_gemm", "mf_quantize_fp8_rows", "mf_gemm_fp8", "mf_check", "mf_selftest_timeout", "mf_status_str", "mf_version", "mf_trace_entry", "mf_trace_enable", "mf_trace_kinds", "mf_trace_read", "mf_launch_count", "KERNEL_KINDS", "LIB_PATH", "STATUS", "STATUS_CODE", "EXPORTED", "PLAN_ARRAYS", "STREAM_FIELDS", "lib"]
 
 # MAGEFLOW_LIB=checked selects the bounds-checked build (same ABI; see mf_check)
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
@@ -129,6 +129,8 @@ _sigs = {
     "mf_final_workspace_bytes": (C.c_size_t, [_P, C.POINTER(mf_dims)]),
     "mf_final": (_S, [_P, C.POINTER(mf_dims), C.POINTER(mf_temb_weights), _P, _P, _P, _P, _P, _P,
                       _P, _P, C.c_size_t, _P]),
+    "mf_final_ex": (_S, [_P, C.POINTER(mf_dims), C.POINTER(mf_temb_weights), _P, _P, _P, _P, _P, _P,
+                         _P, _P, C.c_size_t, _P, _P]),
     "mf_interpolate": (_S, [_P, C.c_int32, _P, _P, _P, _P, _P, _P]),
     "mf_cfg_combine": (_S, [_P, C.c_int32, C.c_float, _P, _P, _P]),
     "mf_euler_step": (_S, [_P, C.c_int32, C.c_float, _P, _P, _P, _P]),
@@ -374,6 +376,15 @@ def mf_final(plan: Plan, dims, temb: mf_temb_weights, w_fmod, b_fmod, w_out, b_o
     _ok(lib.mf_final(plan.handle, C.byref(_dims(dims)), C.byref(temb), _ptr(w_fmod), _ptr(b_fmod),
                      _ptr(w_out), _ptr(b_out), _ptr(t), _ptr(x_img), _ptr(v), _ptr(ws), nbytes,
                      _stream(stream)), "mf_final")
+
+
+def mf_final_ex(plan: Plan, dims, temb: mf_temb_weights, w_fmod, b_fmod, w_out, b_out, t, x_img, v, ws, c,
+                ws_bytes=None, stream=None):
+    """mf_final with the timestep condition c (device f32 [S][H], or an address) given."""
+    nbytes = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _ok(lib.mf_final_ex(plan.handle, C.byref(_dims(dims)), C.byref(temb), _ptr(w_fmod), _ptr(b_fmod),
+                        _ptr(w_out), _ptr(b_out), _ptr(t), _ptr(x_img), _ptr(v), _ptr(ws), nbytes, _ptr(c),
+                        _stream(stream)), "mf_final_ex")
 
 
 # ------------------------------------------------------------------ rectified-flow epilogues

@@ -1079,10 +1079,13 @@ extern "C" size_t mf_final_workspace_bytes(const mf_plan* p, const mf_dims* d) {
   return final_layout(p, d).total;
 }
 
-extern "C" mf_status mf_final(const mf_plan* p, const mf_dims* d, const mf_temb_weights* temb,
-                              const void* w_fmod, const void* b_fmod, const void* w_out,
-                              const void* b_out, const float* d_t, const void* d_x_img, float* d_v,
-                              void* d_ws, size_t ws_bytes, void* stream) {
+namespace {
+// The final layer; d_c (device f32 [S][H]) is the timestep condition when the caller already has
+// it, else it is computed into the workspace.
+mf_status final_layer(const mf_plan* p, const mf_dims* d, const mf_temb_weights* temb, const void* w_fmod,
+                      const void* b_fmod, const void* w_out, const void* b_out, const float* d_t,
+                      const void* d_x_img, float* d_v, void* d_ws, size_t ws_bytes, const float* d_c,
+                      void* stream) {
   DevInfo* di = nullptr;
   int dev = -1;
   MF_TRY(device_info(&di, &dev));
@@ -1101,11 +1104,13 @@ extern "C" mf_status mf_final(const mf_plan* p, const mf_dims* d, const mf_temb_
   char* ws = static_cast<char*>(d_ws);
   const int S = p->S, H = d->hidden, C = d->channels;
   const float* t = d_t ? d_t : p->d_t;
-  float* c = reinterpret_cast<float*>(ws + L.c);
+  if (!aligned(d_c, 16)) return MF_ERR_ALIGNMENT;
+  const float* c = d_c ? d_c : reinterpret_cast<const float*>(ws + L.c);
   float* fmod = reinterpret_cast<float*>(ws + L.fmod);
   bf16* a = reinterpret_cast<bf16*>(ws + L.a);
-  MF_TRY(conditioning(p, d, temb, t, reinterpret_cast<float*>(ws + L.sinus),
-                      reinterpret_cast<float*>(ws + L.h1), c, di, st));
+  if (d_c == nullptr)
+    MF_TRY(conditioning(p, d, temb, t, reinterpret_cast<float*>(ws + L.sinus),
+                        reinterpret_cast<float*>(ws + L.h1), reinterpret_cast<float*>(ws + L.c), di, st));
   {
     Trace tr(MF_K_COND, st, 2.0 * S * 2.0 * H * H, 2.0 * 2.0 * H * H, (S + 3) / 4);
     MF_CUDA(mf::launch_gemv(static_cast<const bf16*>(w_fmod), static_cast<const bf16*>(b_fmod), c, S, H,
@@ -1121,6 +1126,22 @@ extern "C" mf_status mf_final(const mf_plan* p, const mf_dims* d, const mf_temb_
   mf::GemmParams gp{};
   GemmSpec sp[1] = {{p->Ni, C, H, a, w_out, b_out, d_v, C, 0, 1}};
   return run_gemm(sp, 1, mf::kEpiBiasF32, 128, gp, di, st, MF_K_GEMM_FINAL);
+}
+}  // namespace
+
+extern "C" mf_status mf_final(const mf_plan* p, const mf_dims* d, const mf_temb_weights* temb,
+                              const void* w_fmod, const void* b_fmod, const void* w_out,
+                              const void* b_out, const float* d_t, const void* d_x_img, float* d_v,
+                              void* d_ws, size_t ws_bytes, void* stream) {
+  return final_layer(p, d, temb, w_fmod, b_fmod, w_out, b_out, d_t, d_x_img, d_v, d_ws, ws_bytes, nullptr,
+                     stream);
+}
+
+extern "C" mf_status mf_final_ex(const mf_plan* p, const mf_dims* d, const mf_temb_weights* temb,
+                                 const void* w_fmod, const void* b_fmod, const void* w_out,
+                                 const void* b_out, const float* d_t, const void* d_x_img, float* d_v,
+                                 void* d_ws, size_t ws_bytes, const float* d_c, void* stream) {
+  return final_layer(p, d, temb, w_fmod, b_fmod, w_out, b_out, d_t, d_x_img, d_v, d_ws, ws_bytes, d_c, stream);
 }
 
 // ====================================================================== rectified-flow epilogues

@@ -62,5 +62,10 @@ def run_stack(plan, model: DeviceModel, x_txt, zt_bf16, x_img, v, ws: Workspace,
         B.mf_block_forward_ex(plan, d, bs, t, x_txt, x_img, ws.block, B.BLOCK_COND_GIVEN if i else 0,
                               stream=stream)
     f = model.final
-    B.mf_final(plan, d, model.temb_struct, f["w_fmod"], f["b_fmod"], f["w_out"], f["b_out"], t, x_img, v,
-               ws.final, stream=stream)
+    if model.block_structs[:n_blocks]:  # the blocks left the timestep condition in their workspace
+        c = ws.block.data_ptr() + B.mf_block_workspace_layout(plan, d)[0]
+        B.mf_final_ex(plan, d, model.temb_struct, f["w_fmod"], f["b_fmod"], f["w_out"], f["b_out"], t, x_img, v,
+                      ws.final, c, stream=stream)
+    else:
+        B.mf_final(plan, d, model.temb_struct, f["w_fmod"], f["b_fmod"], f["w_out"], f["b_out"], t, x_img, v,
+                   ws.final, stream=stream)

@@ -284,7 +284,7 @@ def test_ln_variants(size):
 def test_cond_given_reuse():
     """Two blocks on a ragged H = 512 pack: the second block reusing the first block's timestep
     condition from the shared workspace (MF_BLOCK_COND_GIVEN) gives the same output bit for bit
-    as recomputing it."""
+    as recomputing it, and so does the final layer given that condition (mf_final_ex)."""
     case = Case(_mid_samples(3), MID, 2, seed=21)
     ref, H = case.ref, case.dims.hidden
     g = np.random.default_rng(8)
@@ -299,6 +299,21 @@ def test_cond_given_reuse():
         mf.mf_check()
         outs.append((xt.cpu(), xi.cpu()))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    # the final layer with the condition the blocks left (mf_final_ex) equals mf_final
+    f = case.model.final
+    vs = []
+    for given in (False, True):
+        v = torch.empty((ref.n_img, case.dims.channels), dtype=torch.float32, device="cuda")
+        args = (case.plan, case.model.dims, case.model.temb_struct, f["w_fmod"], f["b_fmod"], f["w_out"],
+                f["b_out"], None, xi, v, case.ws.final)
+        if given:
+            off = mf.mf_block_workspace_layout(case.plan, case.model.dims)
+            mf.mf_final_ex(*args, case.ws.block.data_ptr() + off[0])
+        else:
+            mf.mf_final(*args)
+        mf.mf_check()
+        vs.append(v.cpu())
+    assert torch.equal(vs[0], vs[1])
 
 
 def test_tiny_stack_qk_norm():
