@@ -292,12 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     bool ok = true;
     if (t < n_t) {
       for (int j = 0; j < n_kv; ++j) {
-        // one lane polls (eight warps spinning with all lanes would crowd the barrier unit the
-        // MMA issuer needs); the warp then synchronises before reading TMEM
-        uint32_t okw = 1;
-        if (lane == 0) okw = mbar_wait(&s_full[t], j & 1, lim) ? 1u : 0u;
-        ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
-        __syncwarp();
+        // every lane polls: a completed phase is seen by each lane's own try_wait, without a
+        // shuffle and warp barrier on the path from S to the exponentials
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, lim));
         if (!ok) break;
         tc_fence_after();
         uint32_t sr[4][32];

@@ -257,14 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     const uint32_t el = elect_one();
-    // one lane polls (every lane spinning would take issue slots from the P / dS warps on this
-    // scheduler and crowd the barrier unit), then the warp continues together
+    // every lane polls: a completed phase is seen by each lane's own try_wait, with no shuffle
+    // and warp barrier between the barrier and the next issue
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-      uint32_t okw = 1;
-      if (lane == 0) okw = mbar_wait(bar, parity, lim) ? 1u : 0u;
-      const bool r_ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
-      __syncwarp();
-      return r_ok;
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, lim));
     };
     const uint32_t k_addr = smem_u32(smem + kOffK), v_addr = smem_u32(smem + kOffV);
     // K-major operands step 32 bytes per K = 16 (descriptor +2); MN-major ones 16 rows (+128)
@@ -359,15 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const uint32_t lane_base = tmem_addr(tmem_base, q4 * 32, 0);
     const float c = p.scale_log2;
     bool ok = true;
-    // a barrier that has completed is seen by one try_wait of every lane; otherwise one lane
-    // polls and the warp continues together
+    // every lane polls: a completed phase is seen by each lane's own try_wait
     auto poll = [&](uint64_t* bar, uint32_t parity) -> bool {
-      if (__all_sync(0xffffffffu, mbar_try_wait(smem_u32(bar), parity))) return true;
-      uint32_t okw = 1;
-      if (lane == 0) okw = mbar_wait(bar, parity, lim) ? 1u : 0u;
-      const bool r_ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
-      __syncwarp();
-      return r_ok;
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, lim));
     };
     for (int i = 0; i < n_q; ++i) {
       const int b = i & 1;
