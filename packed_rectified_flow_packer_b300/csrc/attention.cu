@@ -78,6 +78,18 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
 }
 
+// O_t += P_t V: A operand (P, 128 x 16 bf16 per instruction) read from TMEM; issued by the
+// lane whose `pred` is nonzero.
+__device__ __forceinline__ void mma_bf16_ts_if(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem,
+                                               uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+      : "memory");
+}
+
 template <int D>
 struct AttnSmem {
   static constexpr uint32_t Q = kT * D * 2;                 // one query tile
@@ -213,14 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, lim));
     };
-    // S_t = Q_t K^T: one group of four K = 16 MMAs per 64-dim atom (32-byte steps inside it)
     auto issue_s = [&](int t, int slot) {
       const uint64_t kd = kv0d + ((slot * L::KV) >> 4);
-      const uint64_t ad = qd + ((t * L::Q) >> 4);
 #pragma unroll
-      for (int a = 0; a < D / 64; ++a)
-        mma_group_ss<4>(el, tmem_base + t * kT, ad + ((a * kAtom) >> 4), 2, kd + ((a * kAtom) >> 4), 2, IDESC_S,
-                        a > 0 ? 1u : 0u);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t o = ((kk >> 2) * kAtom + (kk & 3) * 32) >> 4;
+        mma_bf16_if(el, tmem_base + t * kT, qd + ((t * L::Q) >> 4) + o, kd + o, IDESC_S, kk > 0 ? 1u : 0u);
+      }
       mma_commit_if(el, &s_full[t]);
     };
     auto slot_wait = [&](int idx) -> bool { return wait_all(&kv_full[idx % NS], (idx / NS) & 1); };
@@ -240,11 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           break;
         }
         tc_fence_after();
-        // O_t += P_t V_j: pairs of K = 16 MMAs, P from TMEM (8 columns per 16 keys), V 16 rows on
 #pragma unroll
-        for (int kp = 0; kp < kT / 32; ++kp)
-          mma_group2_ts(el, tmem_base + O_COL + t * D, tmem_base + t * kT + kp * 16, 8, vd + ((kp * 4096) >> 4),
-                        2048 >> 4, IDESC_PV, (j > 0 || kp > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_bf16_ts_if(el, tmem_base + O_COL + t * D, tmem_base + t * kT + kk * 8, vd + ((kk * 2048) >> 4),
+                         IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
         if (next) {
           if (t == 0 && !slot_wait(ik)) {
             ok = false;
